@@ -1,0 +1,10 @@
+"""fp64 CPU oracle of the SimSD verification step (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package. It is independent of the CUDA library: the two share no
+code, and neither imports the other.
+"""
+from .simsd import (ERR_PROMPT_LEN, ERR_TAU, ERR_TOKEN, INVALID_LABEL, SEG_DATA,  # noqa: F401
+                    SEG_MASK, accept, build_layout, rope, softmax, temporal_causal_mask,
+                    verify_attention)
+from . import philox  # noqa: F401

@@ -1,0 +1,273 @@
+"""Plain fp64 CPU oracle of the SimSD single-forward speculative verification step.
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg are the only code that may import this module. The CUDA library
+shares no code with it (no kernels, headers, helpers, tables or constants) and the
+product path never calls it.
+
+Each function restates a definition from the pages, in their notation:
+
+* layout    -- SimSD notes, "关键设计" items 1 and 3 (paired data/mask layout; RoPE copy);
+               gist.science SimSD summary, sections 1 and 3.
+* mask      -- SimSD notes, item 2, the four-case equation for A_ij; step labels tau are
+               a permutation of 1..B (gist.science summary, section 2, "Mapa de Passo").
+* attention -- one softmax-attention layer over [prompt | D | D~] under A_ij, with the
+               RoPE ids of D~_k copied from D_k (SimSD notes items 2-3).
+* accept    -- SimSD notes item 4, equation for alpha_r = min(1, p_theta / p_phi), walked in
+               the draft's time order; the first rejected slot is resampled from the
+               normalised residual max(0, p - q) (S2D2 page, "方法步骤详情" step (5));
+               the race draw is the Gumbel-max / exponential-race identity (SPOT page,
+               "Gumbel-Max 技巧与随机耦合").
+
+Readings taken where the pages are silent (all listed in the design notes):
+  prompt tokens carry tau = 0 and are visible to every response row; RoPE pairs are
+  half-split (d, d + D/2) with omega_d = theta^(-2d/D); the prompt keys arrive already
+  rotated; softmax scale 1/sqrt(D); q-head h uses kv-head h // G; every slot of D and
+  D~ is computed; no bonus token when all gamma drafts are accepted.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import philox
+
+SEG_DATA = 0        # D_k   (reference data slot)
+SEG_MASK = 1        # D~_k  ([MASK] prediction slot)
+INVALID_LABEL = 0xFF
+
+# Error bits of the per-call device error word (same meaning as the C interface).
+ERR_TAU = 1          # step labels are not a permutation of 1..B
+ERR_PROMPT_LEN = 2   # negative prompt length
+ERR_TOKEN = 4        # draft token id outside [0, V)
+
+
+# ----------------------------------------------------------------------------- layout
+def build_layout(tau, prompt_len):
+    """Paired layout [prompt | D_1..D_B | D~_1..D~_B].
+
+    Position ids: prompt token j -> j (implicit); D_k -> P + k; D~_k copies D_k's id
+    (0-based k). Labels: one byte per response slot, (segment << 7) | tau, segment 0
+    for D and 1 for D~. A request whose tau is not a permutation of 1..B, or whose
+    prompt length is negative, gets pos = -1 and labels = 0xFF on all 2B slots and
+    raises the matching error bit.
+    """
+    tau = np.asarray(tau, dtype=np.int64)
+    prompt_len = np.asarray(prompt_len, dtype=np.int64)
+    b, B = tau.shape
+    pos = np.zeros((b, 2 * B), dtype=np.int32)
+    labels = np.zeros((b, 2 * B), dtype=np.uint8)
+    err = 0
+    for r in range(b):
+        P = int(prompt_len[r])
+        bad = 0
+        if sorted(tau[r].tolist()) != list(range(1, B + 1)):
+            bad |= ERR_TAU
+        if P < 0:
+            bad |= ERR_PROMPT_LEN
+        err |= bad
+        for k in range(B):
+            if bad:
+                pos[r, k] = pos[r, B + k] = -1
+                labels[r, k] = labels[r, B + k] = INVALID_LABEL
+                continue
+            pos[r, k] = P + k            # data slot D_k: next response position
+            pos[r, B + k] = P + k         # mask slot D~_k reuses the id of D_k
+            labels[r, k] = (SEG_DATA << 7) | int(tau[r, k])
+            labels[r, B + k] = (SEG_MASK << 7) | int(tau[r, k])
+    return pos, labels, err
+
+
+# ------------------------------------------------------------------------------- mask
+def temporal_causal_mask(tau_row):
+    """A_ij over the 2B response slots (index < B: D, index >= B: D~), the four cases
+    of the SimSD mask equation written out literally."""
+    tau_row = [int(t) for t in tau_row]
+    B = len(tau_row)
+    A = np.zeros((2 * B, 2 * B), dtype=bool)
+    for i in range(2 * B):
+        for j in range(2 * B):
+            ti, tj = tau_row[i % B], tau_row[j % B]
+            i_in_D, j_in_D = i < B, j < B
+            if i_in_D and j_in_D:
+                A[i, j] = tj <= ti
+            elif i_in_D and not j_in_D:
+                A[i, j] = tj > ti
+            elif not i_in_D and j_in_D:
+                A[i, j] = tj < ti
+            else:
+                A[i, j] = tj >= ti
+    return A
+
+
+# ------------------------------------------------------------------------------- RoPE
+def rope(x, pos, theta):
+    """Rotate x [n, H, D] at positions pos [n]: pairs (d, d + D/2) turn by
+    pos * theta^(-2d/D), in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    omega = float(theta) ** (-2.0 * np.arange(half, dtype=np.float64) / D)
+    ang = pos[:, None] * omega[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+# -------------------------------------------------------------------------- attention
+def _cache_rows(cache, layout, start, P, h):
+    cache = np.asarray(cache)
+    if layout == "NHD":
+        return cache[start:start + P, h, :]
+    return cache[h, start:start + P, :]
+
+
+def verify_attention(q, k_resp, v_resp, k_cache, v_cache, cache_offsets, prompt_len,
+                     pos_ids, labels, rope_theta, softmax_scale=0.0, cache_layout="NHD",
+                     requests=None, kv_heads=None):
+    """One attention layer of the verify forward.
+
+    q [b, 2B, Hq, D], k_resp/v_resp [b, 2B, Hkv, D] (pre-RoPE), k_cache/v_cache packed
+    (NHD [sumP, Hkv, D] or HND [Hkv, sumP, D], keys already rotated), cache_offsets
+    [b+1], prompt_len [b], pos_ids/labels [b, 2B]. Returns (out [b, 2B, Hq, D] fp64,
+    lse [b, 2B, Hq] fp64 natural-log sum-exp of the scaled scores). Only the listed
+    requests / kv heads are computed (others stay 0 / -inf).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_resp = np.asarray(k_resp, dtype=np.float64)
+    v_resp = np.asarray(v_resp, dtype=np.float64)
+    b, twoB, Hq, D = q.shape
+    B = twoB // 2
+    Hkv = k_resp.shape[2]
+    G = Hq // Hkv
+    scale = softmax_scale if softmax_scale and softmax_scale > 0 else 1.0 / math.sqrt(D)
+    labels = np.asarray(labels)
+    pos_ids = np.asarray(pos_ids)
+    out = np.zeros((b, twoB, Hq, D), dtype=np.float64)
+    lse = np.full((b, twoB, Hq), -np.inf, dtype=np.float64)
+    req_list = range(b) if requests is None else requests
+    head_list = range(Hkv) if kv_heads is None else kv_heads
+    for r in req_list:
+        if int(labels[r, 0]) == INVALID_LABEL or int(prompt_len[r]) < 0:
+            continue
+        P = int(prompt_len[r])
+        start = int(cache_offsets[r])
+        tau_row = (labels[r, :B] & 0x7F).astype(np.int64)
+        A = temporal_causal_mask(tau_row)
+        # every response row sees the whole prompt (tau = 0 < tau(i)), then A_ij
+        visible = np.concatenate([np.ones((twoB, P), dtype=bool), A], axis=1)
+        q_rot = rope(q[r], pos_ids[r], rope_theta)
+        k_rot = rope(k_resp[r], pos_ids[r], rope_theta)
+        for h in head_list:
+            K = np.concatenate([np.asarray(_cache_rows(k_cache, cache_layout, start, P, h),
+                                           dtype=np.float64), k_rot[:, h, :]], axis=0)
+            Vm = np.concatenate([np.asarray(_cache_rows(v_cache, cache_layout, start, P, h),
+                                            dtype=np.float64), v_resp[r, :, h, :]], axis=0)
+            for g in range(G):
+                hq = h * G + g
+                S = (q_rot[:, hq, :] @ K.T) * scale          # [2B, P + 2B]
+                S = np.where(visible, S, -np.inf)
+                m = S.max(axis=1, keepdims=True)
+                E = np.exp(S - m)
+                denom = E.sum(axis=1, keepdims=True)
+                out[r, :, hq, :] = (E @ Vm) / denom
+                lse[r, :, hq] = (m + np.log(denom))[:, 0]
+    return out, lse
+
+
+# ----------------------------------------------------------------------------- accept
+def softmax(logits, temperature):
+    z = np.asarray(logits, dtype=np.float64) / float(temperature)
+    z = z - z.max()
+    e = np.exp(z)
+    return e / e.sum()
+
+
+def _order_from_labels(labels_row, B):
+    """o_r = the slot whose step label is r (r = 1..B), or None if the D half is not a
+    permutation of 1..B."""
+    if int(labels_row[0]) == INVALID_LABEL:
+        return None
+    tau = [int(x) & 0x7F for x in labels_row[:B]]
+    if sorted(tau) != list(range(1, B + 1)):
+        return None
+    order = [0] * B
+    for k, t in enumerate(tau):
+        order[t - 1] = k
+    return order
+
+
+def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
+           seed, offset, requests=None):
+    """Speculative acceptance along the draft's time order, then residual resampling.
+
+    For steps r = 1..gamma: slot k = o_r, x = draft token at k, p = softmax(target
+    logits at k / T), q = softmax(draft logits at k / T); accept if p_x >= q_x, else
+    accept iff u_r * q_x < p_x (u_r uniform in (0,1)); stop at the first rejection.
+    At the first rejected slot draw y from max(0, p - q) (normalised) by the race
+    argmax_v r_v / E_v, E_v = -ln(u_v) (ties: smallest v; if the residual is all zero,
+    race on p instead). Returns dict with accepted_len [b], n_commit [b], out_tokens
+    [b, B], out_pos [b, B] (slot index, step order, -1 past n_commit), err, and
+    per-request diagnostics (decision margins, race top-2 keys).
+    """
+    tl = np.asarray(target_logits)
+    dl = np.asarray(draft_logits)
+    toks = np.asarray(draft_tokens)
+    labels = np.asarray(labels)
+    b, B, V = tl.shape
+    acc_len = np.full(b, -1, dtype=np.int32)
+    n_commit = np.zeros(b, dtype=np.int32)
+    out_tokens = np.full((b, B), -1, dtype=np.int32)
+    out_pos = np.full((b, B), -1, dtype=np.int32)
+    err = 0
+    diag = {}
+    req_list = range(b) if requests is None else requests
+    for r in req_list:
+        order = _order_from_labels(labels[r], B)
+        if order is None:
+            err |= ERR_TAU
+            continue
+        steps = order[:gamma]
+        if any(not (0 <= int(toks[r, k]) < V) for k in steps):
+            err |= ERR_TOKEN
+            continue
+        u = philox.accept_uniforms(seed, offset, r, gamma)
+        a = 0
+        margins = []
+        p = q = None
+        for step, k in enumerate(steps):
+            x = int(toks[r, k])
+            p = softmax(tl[r, k], temperature)
+            q = softmax(dl[r, k], temperature)
+            px, qx = p[x], q[x]
+            margins.append(abs(u[step] * qx - px) / qx if qx > 0 else np.inf)
+            if px >= qx or u[step] * qx < px:
+                a += 1
+                continue
+            break
+        for step in range(a):
+            out_tokens[r, step] = int(toks[r, steps[step]])
+            out_pos[r, step] = steps[step]
+        race = None
+        if a < gamma:
+            k = steps[a]
+            p = softmax(tl[r, k], temperature)
+            q = softmax(dl[r, k], temperature)
+            res = np.maximum(p - q, 0.0)
+            if not np.any(res > 0):
+                res = p
+            uv = philox.resample_uniforms(seed, offset, r, V)
+            keys = res / (-np.log(uv))
+            y = int(np.argmax(keys))          # first maximum = smallest v on ties
+            top2 = np.sort(keys)[-2:] if V > 1 else np.array([0.0, keys[0]])
+            race = (float(top2[1]), float(top2[0]))
+            out_tokens[r, a] = y
+            out_pos[r, a] = k
+        acc_len[r] = a
+        n_commit[r] = a + (1 if a < gamma else 0)
+        diag[r] = {"margins": margins, "race_top2": race}
+    return {"accepted_len": acc_len, "n_commit": n_commit, "out_tokens": out_tokens,
+            "out_pos": out_pos, "err": err, "diag": diag}

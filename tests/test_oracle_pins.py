@@ -1,0 +1,394 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+* Philox4x32-10 against the published known-answer vectors.
+* The masked single forward against a brute-force rebuild of every denoising state
+  (SimSD notes, item 2: at the prediction slot D~_i the model sees the prompt, the data
+  slots decided before step tau(i) and the still-masked slots -- exactly the
+  autoregressive prefix view), with an independent complex-number RoPE.
+* Perturbation invariance, B = 1 against a textbook attention routine (torch SDPA),
+  identity tau = the 2L / AR verification view (S2D2 page, "2L 技巧"), RoPE shift
+  invariance and the D = 2 rotation, the key count of every row.
+* Acceptance: special cases, the closed form E[a] = sum_k prod_{r<=k} (1 - TV(p_r, q_r))
+  (total-variation bound on the SPOT page), and Monte Carlo: committed tokens follow the
+  target distribution (speculative decoding is lossless, S2D2 / SPOT pages).
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import philox
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------- Philox
+def _kat_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x, 16) for x in line.split()])
+    return rows
+
+
+@pytest.mark.parametrize("row", _kat_rows())
+def test_philox_known_answers(row):
+    out = philox.philox4x32_10(np.array(row[:4], np.uint32), np.array(row[4:6], np.uint32))
+    assert [int(x) for x in out] == row[6:]
+    assert philox.philox_scalar(row[:4], row[4:6]) == row[6:]
+
+
+def test_philox_vector_matches_scalar_random_inputs():
+    rng = np.random.default_rng(1)
+    ctr = rng.integers(0, 2**32, size=(64, 4), dtype=np.uint64).astype(np.uint32)
+    key = rng.integers(0, 2**32, size=(64, 2), dtype=np.uint64).astype(np.uint32)
+    out = philox.philox4x32_10(ctr, key)
+    for i in range(64):
+        assert [int(x) for x in out[i]] == philox.philox_scalar(ctr[i], key[i])
+
+
+def test_uniforms_open_interval_and_exact_in_fp32():
+    u = philox.resample_uniforms(seed=123, offset=7, request=3, V=200_000)
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert np.all(u.astype(np.float32).astype(np.float64) == u)
+    # uniformity (Kolmogorov-Smirnov against U(0,1))
+    from scipy import stats
+    assert stats.kstest(u, "uniform").pvalue > 1e-3
+    # accept and resample streams differ; requests and offsets differ
+    a = philox.accept_uniforms(123, 7, 3, 8)
+    b = philox.accept_uniforms(123, 7, 4, 8)
+    c = philox.accept_uniforms(123, 8, 3, 8)
+    assert not np.array_equal(a, b) and not np.array_equal(a, c)
+    assert not np.array_equal(a, u[:8])
+
+
+# --------------------------------------------------------------------------- layout
+def test_layout_positions_and_labels():
+    tau = np.array([[2, 3, 1], [1, 2, 3]])
+    plen = np.array([5, 0])
+    pos, labels, err = oracle.build_layout(tau, plen)
+    assert err == 0
+    assert pos.tolist() == [[5, 6, 7, 5, 6, 7], [0, 1, 2, 0, 1, 2]]
+    assert labels.tolist() == [[2, 3, 1, 130, 131, 129], [1, 2, 3, 129, 130, 131]]
+
+
+def test_layout_invalid_requests():
+    tau = np.array([[1, 1, 3], [1, 2, 3], [0, 2, 3]])
+    plen = np.array([4, -1, 2])
+    pos, labels, err = oracle.build_layout(tau, plen)
+    assert err == (oracle.ERR_TAU | oracle.ERR_PROMPT_LEN)
+    for r in range(3):
+        assert pos[r].tolist() == [-1] * 6
+        assert labels[r].tolist() == [0xFF] * 6
+
+
+# ---------------------------------------------------------------- attention helpers
+def _complex_rope(x, pos, theta):
+    """Independent restatement of RoPE: pairs (d, d + D/2) as one complex number,
+    multiplied by exp(i * pos * theta^(-2d/D))."""
+    D = x.shape[-1]
+    half = D // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    w = np.exp(1j * np.outer(pos, theta ** (-2.0 * np.arange(half) / D)))
+    z = z * w.reshape(w.shape[0], *([1] * (z.ndim - 2)), half)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _random_case(rng, b, B, Hq, Hkv, D, plens, taus=None):
+    q = rng.standard_normal((b, 2 * B, Hq, D))
+    k = rng.standard_normal((b, 2 * B, Hkv, D))
+    v = rng.standard_normal((b, 2 * B, Hkv, D))
+    total = int(sum(plens))
+    kc = rng.standard_normal((total, Hkv, D))
+    vc = rng.standard_normal((total, Hkv, D))
+    offs = np.concatenate([[0], np.cumsum(plens)]).astype(np.int64)
+    if taus is None:
+        taus = np.stack([rng.permutation(B) + 1 for _ in range(b)])
+    pos, labels, err = oracle.build_layout(taus, plens)
+    assert err == 0
+    return dict(q=q, k_resp=k, v_resp=v, k_cache=kc, v_cache=vc, cache_offsets=offs,
+                prompt_len=np.array(plens), pos_ids=pos, labels=labels, tau=taus)
+
+
+def _run(case, theta, **kw):
+    return oracle.verify_attention(case["q"], case["k_resp"], case["v_resp"], case["k_cache"],
+                                   case["v_cache"], case["cache_offsets"], case["prompt_len"],
+                                   case["pos_ids"], case["labels"], theta, **kw)
+
+
+def _softmax_attend(qv, K, V, scale):
+    s = K @ qv * scale
+    s = s - s.max()
+    e = np.exp(s)
+    return e @ V / e.sum()
+
+
+# ----------------------------------------------------- P1: explicit-state brute force
+@pytest.mark.parametrize("B", [1, 2, 3, 4])
+def test_single_forward_equals_explicit_denoising_states(B):
+    rng = np.random.default_rng(10 + B)
+    Hq, Hkv, D, P, theta = 4, 2, 8, 5, 100.0
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    for perm in itertools.permutations(range(1, B + 1)):
+        case = _random_case(rng, 1, B, Hq, Hkv, D, [P], taus=np.array([perm]))
+        out, _ = _run(case, theta)
+        tau = list(perm)
+        q_rot = _complex_rope(case["q"][0], np.array(case["pos_ids"][0], float), theta)
+        pos_slot = P + np.arange(B)
+        kD = _complex_rope(case["k_resp"][0, :B], pos_slot.astype(float), theta)
+        kM = _complex_rope(case["k_resp"][0, B:], pos_slot.astype(float), theta)
+        vD, vM = case["v_resp"][0, :B], case["v_resp"][0, B:]
+        for i in range(2 * B):
+            slot = i % B
+            t = tau[slot]
+            # state seen by row i: slot k holds its decided token if tau(k) < t for a
+            # prediction slot (D~), or tau(k) <= t for a data slot (D)
+            decided = [(tau[k] < t) if i >= B else (tau[k] <= t) for k in range(B)]
+            for h in range(Hkv):
+                K = np.concatenate([case["k_cache"][:P, h],
+                                    np.stack([kD[k, h] if decided[k] else kM[k, h]
+                                              for k in range(B)])])
+                Vv = np.concatenate([case["v_cache"][:P, h],
+                                     np.stack([vD[k, h] if decided[k] else vM[k, h]
+                                               for k in range(B)])])
+                for g in range(G):
+                    hq = h * G + g
+                    ref = _softmax_attend(q_rot[i, hq], K, Vv, scale)
+                    np.testing.assert_allclose(out[0, i, hq], ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------ P2: perturbation invariance
+def test_perturbing_invisible_slots_leaves_prediction_rows_unchanged():
+    rng = np.random.default_rng(2)
+    B, Hq, Hkv, D, P, theta = 4, 2, 1, 16, 6, 1e4
+    case = _random_case(rng, 1, B, Hq, Hkv, D, [P], taus=np.array([[3, 1, 4, 2]]))
+    base, _ = _run(case, theta)
+    tau = case["tau"][0]
+    for j in range(B):
+        for seg in (0, 1):
+            pert = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in case.items()}
+            pert["k_resp"][0, seg * B + j] += 3.0
+            pert["v_resp"][0, seg * B + j] -= 2.0
+            out, _ = _run(pert, theta)
+            for i in range(B):
+                row = B + i          # D~_i
+                if seg == 0:
+                    invisible = tau[j] >= tau[i]       # future or own data token
+                else:
+                    invisible = tau[j] < tau[i]        # mask slot already decided
+                same = np.array_equal(out[0, row], base[0, row])
+                assert same == invisible, (i, j, seg)
+    # the prompt is visible to every row
+    pert = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in case.items()}
+    pert["v_cache"][0] += 1.0
+    out, _ = _run(pert, theta)
+    for row in range(2 * B):
+        assert not np.array_equal(out[0, row], base[0, row])
+
+
+# -------------------------------------------------- P3: B = 1 is prefix attention
+def test_block_of_one_is_plain_prefix_attention():
+    rng = np.random.default_rng(3)
+    Hq, Hkv, D, theta = 4, 2, 32, 1e4
+    plens = [7, 0, 12]
+    case = _random_case(rng, 3, 1, Hq, Hkv, D, plens)
+    out, lse = _run(case, theta)
+    for r, P in enumerate(plens):
+        off = int(case["cache_offsets"][r])
+        q_rot = _complex_rope(case["q"][r], np.array([P, P], float), theta)
+        k_rot = _complex_rope(case["k_resp"][r], np.array([P, P], float), theta)
+        for row in range(2):
+            for hq in range(Hq):
+                h = hq // (Hq // Hkv)
+                K = np.concatenate([case["k_cache"][off:off + P, h], k_rot[row:row + 1, h]])
+                V = np.concatenate([case["v_cache"][off:off + P, h],
+                                    case["v_resp"][r, row:row + 1, h]])
+                ref = torch.nn.functional.scaled_dot_product_attention(
+                    torch.tensor(q_rot[row, hq])[None, None, None],
+                    torch.tensor(K)[None, None], torch.tensor(V)[None, None])[0, 0, 0].numpy()
+                np.testing.assert_allclose(out[r, row, hq], ref, rtol=0, atol=1e-12)
+                s = torch.tensor(K) @ torch.tensor(q_rot[row, hq]) / math.sqrt(D)
+                assert abs(lse[r, row, hq] - torch.logsumexp(s, 0).item()) < 1e-12
+
+
+# --------------------------------------------- P4: identity tau is the 2L / AR view
+def test_identity_tau_is_autoregressive_prefix_view():
+    B = 5
+    A = oracle.temporal_causal_mask(list(range(1, B + 1)))
+    for i in range(B):
+        # prediction slot D~_i: data tokens strictly before i, mask slots from i on
+        assert A[B + i, :B].tolist() == [j < i for j in range(B)]
+        assert A[B + i, B:].tolist() == [j >= i for j in range(B)]
+        # data slot D_i: data tokens up to and including i, mask slots after i
+        assert A[i, :B].tolist() == [j <= i for j in range(B)]
+        assert A[i, B:].tolist() == [j > i for j in range(B)]
+
+
+# ------------------------------------------------------------- P5: RoPE properties
+def test_rope_matches_complex_rotation_and_d2_case():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((6, 3, 16))
+    pos = np.array([0, 1, 5, 100, 4096, 32790])
+    np.testing.assert_allclose(oracle.rope(x, pos, 1e6), _complex_rope(x, pos, 1e6),
+                               atol=1e-12, rtol=0)
+    x2 = rng.standard_normal((4, 1, 2))
+    p2 = np.array([0.0, 1.0, 2.5, 7.0])
+    got = oracle.rope(x2, p2, 1e4)
+    for n in range(4):
+        c, s = math.cos(p2[n]), math.sin(p2[n])
+        exp = np.array([[c, -s], [s, c]]) @ x2[n, 0]
+        np.testing.assert_allclose(got[n, 0], exp, atol=1e-14)
+
+
+def test_attention_invariant_to_a_common_position_shift():
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, P, theta = 3, 2, 1, 16, 9, 1e4
+    case = _random_case(rng, 1, B, Hq, Hkv, D, [P])
+    raw_k = rng.standard_normal((P, Hkv, D))
+    outs = []
+    for shift in (0, 37):
+        c = dict(case)
+        c["k_cache"] = oracle.rope(raw_k, np.arange(P) + shift, theta)
+        c["pos_ids"] = case["pos_ids"] + shift
+        outs.append(_run(c, theta)[0])
+    np.testing.assert_allclose(outs[0], outs[1], atol=1e-10, rtol=0)
+
+
+def test_unaligned_positions_change_prediction_rows():
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D, P, theta = 4, 2, 1, 16, 6, 1e4
+    case = _random_case(rng, 1, B, Hq, Hkv, D, [P])
+    base, _ = _run(case, theta)
+    c = dict(case)
+    c["pos_ids"] = (P + np.arange(2 * B))[None].astype(np.int32)  # physical positions
+    out, _ = _run(c, theta)
+    assert np.abs(out[0, B:] - base[0, B:]).max() > 1e-3
+
+
+# ---------------------------------------------------------- P6: keys seen per row
+@pytest.mark.parametrize("B", [1, 2, 5, 8, 16, 32])
+def test_every_row_sees_exactly_B_response_keys(B):
+    rng = np.random.default_rng(B)
+    A = oracle.temporal_causal_mask(rng.permutation(B) + 1)
+    assert np.all(A.sum(axis=1) == B)
+    # exactly one of (D_k, D~_k) is visible to each row, for every slot k
+    assert np.all(A[:, :B] ^ A[:, B:])
+
+
+# ------------------------------------------------------------- P7: accept cases
+def _accept_case(tl, dl, toks, tau, gamma, seed=1, offset=0, T=1.0):
+    _, labels, err = oracle.build_layout(np.array(tau), np.zeros(len(tau), int))
+    assert err == 0
+    return oracle.accept(np.array(tl), np.array(dl), np.array(toks), labels, gamma, T,
+                         seed, offset)
+
+
+def test_equal_distributions_accept_everything():
+    rng = np.random.default_rng(8)
+    b, B, V = 6, 5, 50
+    tl = rng.standard_normal((b, B, V)) * 2
+    toks = rng.integers(0, V, (b, B))
+    tau = [list(rng.permutation(B) + 1) for _ in range(b)]
+    res = _accept_case(tl, tl.copy(), toks, tau, B)
+    assert res["accepted_len"].tolist() == [B] * b
+    assert res["n_commit"].tolist() == [B] * b
+    for r in range(b):
+        order = [tau[r].index(t) for t in range(1, B + 1)]
+        assert res["out_pos"][r].tolist() == order
+        assert res["out_tokens"][r].tolist() == [int(toks[r, k]) for k in order]
+
+
+def test_one_hot_target_disagreeing_with_draft_rejects_and_resamples_argmax():
+    B, V = 3, 20
+    tl = np.full((1, B, V), -1e4)
+    tl[0, :, 7] = 10.0                       # p is one-hot on token 7 in fp64
+    dl = np.zeros((1, B, V))
+    toks = np.array([[3, 3, 3]])
+    res = _accept_case(tl, dl, toks, [[2, 1, 3]], B)
+    assert res["accepted_len"][0] == 0
+    assert res["n_commit"][0] == 1
+    assert res["out_pos"][0].tolist() == [1, -1, -1]   # slot with tau = 1
+    assert res["out_tokens"][0].tolist() == [7, -1, -1]
+
+
+def test_one_hot_draft_on_a_certain_target_token_accepts():
+    B, V = 2, 10
+    tl = np.full((1, B, V), -1e4)
+    tl[0, :, 4] = 5.0
+    dl = tl.copy()
+    dl[0, 1, 4] = 4.0   # still one-hot after softmax in fp64
+    res = _accept_case(tl, dl, np.array([[4, 4]]), [[1, 2]], B)
+    assert res["accepted_len"][0] == 2
+
+
+def test_invalid_tau_and_token_sentinels():
+    B, V = 3, 10
+    tl = np.zeros((2, B, V))
+    labels = np.array([[1, 1, 3, 129, 129, 131], [1, 2, 3, 129, 130, 131]], dtype=np.uint8)
+    toks = np.array([[0, 0, 0], [0, 12, 0]])
+    res = oracle.accept(tl, tl, toks, labels, B, 1.0, 0, 0)
+    assert res["err"] == (oracle.ERR_TAU | oracle.ERR_TOKEN)
+    assert res["accepted_len"].tolist() == [-1, -1]
+    assert res["n_commit"].tolist() == [0, 0]
+    assert (res["out_tokens"] == -1).all() and (res["out_pos"] == -1).all()
+
+
+def test_temperature_scales_logits():
+    B, V = 1, 6
+    rng = np.random.default_rng(9)
+    tl = rng.standard_normal((1, B, V))
+    p_t2 = oracle.softmax(tl[0, 0], 2.0)
+    p_half = oracle.softmax(tl[0, 0] / 2.0, 1.0)
+    np.testing.assert_allclose(p_t2, p_half, atol=1e-15)
+
+
+# ----------------------------------------------- P8: Monte Carlo, lossless accept
+def test_monte_carlo_commits_follow_target_and_mean_length_closed_form():
+    from scipy import stats
+    rng = np.random.default_rng(11)
+    B = gamma = 4
+    V = 16
+    tl1 = rng.standard_normal((B, V)) * 1.5
+    dl1 = tl1 + rng.standard_normal((B, V)) * 1.0
+    p = np.stack([oracle.softmax(tl1[k], 1.0) for k in range(B)])
+    q = np.stack([oracle.softmax(dl1[k], 1.0) for k in range(B)])
+    N = 40_000
+    tau = np.array([3, 1, 4, 2])
+    order = [int(np.where(tau == t)[0][0]) for t in range(1, B + 1)]
+    toks = np.stack([rng.choice(V, size=N, p=q[k]) for k in range(B)], axis=1)
+    _, labels1, _ = oracle.build_layout(tau[None], np.array([0]))
+    labels = np.broadcast_to(labels1, (N, 2 * B))
+    tl = np.broadcast_to(tl1, (N, B, V))
+    dl = np.broadcast_to(dl1, (N, B, V))
+    res = oracle.accept(tl, dl, toks, labels, gamma, 1.0, seed=2024, offset=0)
+    a = res["accepted_len"]
+    beta = 1.0 - 0.5 * np.abs(p - q).sum(axis=1)          # per slot
+    beta_steps = [beta[k] for k in order]
+    expected = sum(np.prod(beta_steps[:k + 1]) for k in range(gamma))
+    se = a.std() / math.sqrt(N)
+    assert abs(a.mean() - expected) < 4 * se + 1e-3
+    # step 1 commit ~ p at slot o_1; step 2 commit (given step 1 accepted) ~ p at o_2
+    for step in (0, 1):
+        sel = a >= step if step > 0 else np.ones(N, bool)
+        if step > 0:
+            sel = a >= 1
+        counts = np.bincount(res["out_tokens"][sel, step], minlength=V)
+        exp_p = p[order[step]] * sel.sum()
+        keep = exp_p > 5
+        chi2 = ((counts[keep] - exp_p[keep]) ** 2 / exp_p[keep]).sum()
+        pval = stats.chi2.sf(chi2, keep.sum() - 1)
+        assert pval > 1e-3, (step, pval)
+    # a plausible mistake -- resampling from p instead of the residual -- is detectable
+    counts_rej = np.bincount(res["out_tokens"][a == 0, 0], minlength=V)
+    resid = np.maximum(p[order[0]] - q[order[0]], 0)
+    resid /= resid.sum()
+    exp_rej = resid * (a == 0).sum()
+    keep = exp_rej > 5
+    chi2 = ((counts_rej[keep] - exp_rej[keep]) ** 2 / exp_rej[keep]).sum()
+    assert stats.chi2.sf(chi2, keep.sum() - 1) > 1e-3
