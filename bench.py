@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the SimSD verification step on GB300.
+
+One step = simsd_build_layout + simsd_verify_attention (one layer) + simsd_accept over one
+batch of synthetic input of a named workload (default: the 8B-class GQA layer, batch 16,
+32 q / 8 kv heads, D 128, prompt 512, block 4, vocab 151936). Prints ONE JSON line.
+
+Metric: verified candidate tokens/s = batch * gamma / step time.
+  value      device-resident inputs; K steps replayed back to back (one CUDA graph per
+             step), rotating over input sets whose total exceeds L2 so no step reads
+             another step's data from L2.
+  e2e        the public Python API with host buffers: pinned host -> device copy of every
+             input, the step, device -> host copy of the accept results, every step.
+  roofline   the call with the most algorithmic bytes, timed on its own (CUDA events on
+             its launch stream, graph replays over the rotating sets).
+  cpu_baseline  the fp64 oracle on the host cores (rank 0, N = 1), bounded sample.
+--impl reference times the oracle itself (the CPU reference implementation of the step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified candidate tokens/s (verify-attn+accept), % of HBM roofline, 1xGB300"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa8b_bf16")
+    ap.add_argument("--cache-layout", choices=["NHD", "HND"], default="NHD")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------ CPU side
+def _oracle_sample(job):
+    """Runs the oracle on `n` freshly generated single-request copies of the workload
+    (same shapes and distributions) and returns (tokens, seconds)."""
+    name, first_seed, n, deadline = job
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import torch
+    torch.set_num_threads(1)
+    import oracle
+    import workloads
+    w = workloads.WORKLOADS[name]
+    tokens, spent = 0, 0.0
+    for i in range(n):
+        if time.time() > deadline and i > 0:
+            break
+        seed = first_seed + i
+        one = w.with_(batch=1)
+        lay = workloads.make_layout_inputs(one, seed=seed)
+        if w.prompt_len is None:   # ragged: draw this request's length from the range
+            lo, hi = w.prompt_len_range
+            g = torch.Generator().manual_seed(seed)
+            lay["prompt_len"] = torch.randint(lo, hi + 1, (1,), generator=g).to(torch.int32)
+        att = workloads.make_attention_inputs(one, lay["prompt_len"], seed=seed)
+        acc = workloads.make_accept_inputs(one, seed=seed)
+        f = lambda t: (t.float() if t.dtype == torch.bfloat16 else t).numpy()
+        t0 = time.perf_counter()
+        pos, labels, _ = oracle.build_layout(lay["tau"].numpy(), lay["prompt_len"].numpy())
+        oracle.verify_attention(f(att["q"]), f(att["k_resp"]), f(att["v_resp"]),
+                                f(att["k_cache"]), f(att["v_cache"]),
+                                att["cache_offsets"].numpy(), lay["prompt_len"].numpy(), pos,
+                                labels, one.rope_theta)
+        oracle.accept(acc["target_logits"].numpy(), acc["draft_logits"].numpy(),
+                      acc["draft_tokens"].numpy(), labels, one.gamma, one.temperature,
+                      acc["philox_seed"], 0)
+        spent += time.perf_counter() - t0
+        tokens += one.gamma
+    return tokens, spent
+
+
+def _oracle_pool(cores):
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    return mp.get_context("spawn").Pool(cores)
+
+
+def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000):
+    """tokens/s of the oracle over all host cores (one single-threaded worker per core,
+    each timing only its own oracle calls; input generation is not timed)."""
+    cores = cores or len(os.sched_getaffinity(0))
+    own = pool is None
+    if own:
+        pool = _oracle_pool(cores)
+    try:
+        deadline = time.time() + seconds
+        jobs = [(name, first_seed + 10000 * c, 10 ** 6, deadline) for c in range(cores)]
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_sample, jobs)
+        wall = time.perf_counter() - t0
+    finally:
+        if own:
+            pool.close()
+            pool.join()
+    tokens = sum(r[0] for r in res)
+    busy = max(r[1] for r in res)
+    g = _gamma(name)
+    return {"value": tokens / busy, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens // g} single-request copies of {name} (fresh seeds, same "
+                      f"shapes and distributions), fp64 NumPy oracle (layout + attention + "
+                      f"accept), {cores} single-threaded workers, {busy:.1f} s busy / "
+                      f"{wall:.1f} s wall"}
+
+
+def _gamma(name):
+    import workloads
+    return workloads.WORKLOADS[name].gamma
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import workloads
+    w = workloads.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    t0 = time.perf_counter()
+    with _oracle_pool(cores) as pool:
+        for k in range(args.warmup + args.steps):
+            v = cpu_oracle_throughput(args.workload, per_step, cores, pool, 1000 + 97 * k)
+            if k >= args.warmup:
+                vals.append(v)
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(v["value"] for v in vals)
+    tokens_step = w.batch * w.gamma
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tokens_step / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, args, "fp64 oracle on host cores"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": vals[0]["sample"] +
+                             f"; median over {args.steps} steps of {per_step:.1f} s each"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": elapsed}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU side
+def _config(w, args, launch):
+    cfg = {"workload": w.name, "batch": w.batch, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+           "D": w.D, "gamma": w.gamma, "V": w.V, "rope_theta": w.rope_theta,
+           "temperature": w.temperature, "cache_layout": args.cache_layout,
+           "parallelism": f"dp{args.gpus} (independent requests per rank)"}
+    if w.prompt_len is not None:
+        cfg["P"] = w.prompt_len
+    else:
+        cfg["P_range"] = list(w.prompt_len_range)
+    cfg["launch"] = launch
+    return cfg
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"simsd_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _make_sets(w, args, device, n_sets, rank):
+    import torch
+    import workloads
+    sets = []
+    for i in range(n_sets):
+        seed = w.seed + 1000 * rank + i
+        lay = workloads.make_layout_inputs(w, seed=seed)
+        att = workloads.make_attention_inputs(w, lay["prompt_len"], seed=seed, device=device,
+                                              cache_layout=args.cache_layout)
+        acc = workloads.make_accept_inputs(w, seed=seed, device=device)
+        sets.append({
+            "tau": lay["tau"].to(device), "prompt_len": lay["prompt_len"].to(device),
+            "q": att["q"], "k_resp": att["k_resp"], "v_resp": att["v_resp"],
+            "k_cache": att["k_cache"], "v_cache": att["v_cache"],
+            "cache_start": att["cache_offsets"][:-1].contiguous().to(device),
+            "target_logits": acc["target_logits"], "draft_logits": acc["draft_logits"],
+            "draft_tokens": acc["draft_tokens"], "_seed": acc["philox_seed"],
+            "_prompt_len_cpu": lay["prompt_len"]})
+    return sets
+
+
+def _time_graphs(graphs, count, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(count):
+        graphs[k % len(graphs)].replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import workloads
+    import diffusion_speculative_verify_gb300 as pkg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    w = workloads.WORKLOADS[args.workload]
+
+    from diffusion_speculative_verify_gb300 import _build
+    if rank == 0 or not os.path.exists(pkg.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    pkg.load_library()
+
+    probe = workloads.make_layout_inputs(w)
+    alg = workloads.algorithmic_bytes(w, probe["prompt_len"])
+    n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / max(1, alg["total_bytes"]))))
+    sets = _make_sets(w, args, device, n_sets, rank)
+    steps = [pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
+                            temperature=w.temperature, cache_layout=args.cache_layout,
+                            philox_seed=s["_seed"]) for s in sets]
+    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"]) for s in sets]
+    stream = torch.cuda.Stream(device=device)
+    torch.cuda.synchronize()
+
+    # one CUDA graph per step (and per call, for the per-call roofline timing)
+    use_graph = not args.no_graph
+    g_step, g_calls = [], {"layout": [], "attention": [], "accept": []}
+    if use_graph:
+        with torch.cuda.stream(stream):
+            for st in steps:          # untimed eager pass: module loading, first launches
+                st.run(stream)
+        stream.synchronize()
+        for st in steps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run(torch.cuda.current_stream())
+            g_step.append(g)
+            for name in g_calls:
+                gc = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gc, stream=stream):
+                    getattr(st, name)(torch.cuda.current_stream())
+                g_calls[name].append(gc)
+
+    def run_step(k):
+        if use_graph:
+            g_step[k % n_sets].replay()
+        else:
+            steps[k % n_sets].run(stream)
+
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            run_step(k)
+    stream.synchronize()
+
+    # ---- timed region: exactly K steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for k in range(args.steps):
+            run_step(args.warmup + k)
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    tokens_step = w.batch * w.gamma
+    value = world * tokens_step * args.steps / elapsed
+    errs = [int(st.dev_err.item()) for st in steps]
+
+    # ---- per-call timing (roofline of the dominant call)
+    per_call = {}
+    if use_graph:
+        reps = max(args.steps, 3 * n_sets)
+        with torch.cuda.stream(stream):
+            for name, gl in g_calls.items():
+                per_call[name] = _time_graphs(gl, reps, stream) / reps
+    mean_alg = {k: statistics.mean(a[k] for a in algs)
+                for k in ("attn_bytes", "accept_bytes", "total_bytes", "attn_flops")}
+    peak, peak_kind = _peaks()
+    roofline = None
+    if per_call:
+        call_bytes = {"attention": mean_alg["attn_bytes"], "accept": mean_alg["accept_bytes"]}
+        dom = max(call_bytes, key=lambda k: per_call[k])
+        achieved = call_bytes[dom] / per_call[dom] / 1e9
+        roofline = {"bound": "hbm", "kernel": "simsd_accept (accept_stats + accept_finish)"
+                    if dom == "accept" else "simsd_verify_attention",
+                    "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                    "algorithmic_bytes_per_launch": call_bytes[dom],
+                    "avg_launch_us": per_call[dom] * 1e6,
+                    "per_call_us": {k: v * 1e6 for k, v in per_call.items()}}
+    step_s = elapsed / args.steps
+    step_frac = mean_alg["total_bytes"] / step_s / 1e9 / peak
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(w, sets[0], steps[0], args, stream, world, device)
+    clk = clocks.stop()
+
+    # ---- CPU baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds)
+
+    launches_per_step = 4   # layout, attention, accept_stats, accept_finish
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": _config(w, args, "one CUDA graph per step" if use_graph else "eager"),
+            "l2": f"{n_sets} rotating input sets of {alg['total_bytes'] / 1e6:.1f} MB "
+                  f"(> L2 {L2_BYTES / 2**20:.0f} MiB in total)",
+            "pct_hbm_roofline_step": 100.0 * step_frac,
+            "algorithmic_bytes_per_step": mean_alg["total_bytes"],
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+            "dev_err": errs, "wall_s_timed": wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(w, s, st, args, stream, world, device):
+    """Same metric through VerifyStep with host buffers: every step copies all inputs
+    from pinned host memory and reads the accept results back."""
+    import torch
+    import torch.distributed as dist
+    keys = ["tau", "prompt_len", "q", "k_resp", "v_resp", "k_cache", "v_cache", "cache_start",
+            "target_logits", "draft_logits", "draft_tokens"]
+    host = {k: s[k].cpu().pin_memory() for k in keys}
+    outs = [st.accepted_len, st.n_commit, st.out_tokens, st.out_pos]
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    n = max(3, min(args.steps, 50))
+
+    def one():
+        for k in keys:
+            s[k].copy_(host[k], non_blocking=True)
+        st.run(stream)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+    e1.synchronize()
+    el = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([el], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": world * w.batch * w.gamma * n / el, "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "api": "VerifyStep.run (simsd_build_layout, simsd_verify_attention, simsd_accept)"}
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

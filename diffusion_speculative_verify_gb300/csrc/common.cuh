@@ -1,0 +1,76 @@
+// Shared device/host helpers of the SimSD verification library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "simsd.h"
+
+#define SIMSD_API extern "C" __attribute__((visibility("default")))
+
+namespace simsd {
+
+constexpr int kMaxB = 32;          // block size limit (labels hold tau in 7 bits; warp scans)
+constexpr uint8_t kSegMask = 0x80; // label bit: mask slot D~
+constexpr uint8_t kLabelInvalid = 0xFF;
+
+static inline simsd_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+}
+
+static inline simsd_status last_launch_status() {
+  return cuda_status(cudaGetLastError());
+}
+
+static inline int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------------------ Philox
+// Philox4x32-10 as defined by Salmon, Moraes, Dror, Shaw (SC'11): each round forms the
+// 64-bit products of counter words 0 and 2 with two odd multipliers, and the new counter
+// is (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1), hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)); the key is advanced
+// by two Weyl increments between rounds.
+struct Philox4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(Philox4 c, uint32_t k0, uint32_t k1) {
+  const uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  const uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint32_t hi0 = __umulhi(kM0, c.x), lo0 = kM0 * c.x;
+    const uint32_t hi1 = __umulhi(kM1, c.z), lo1 = kM1 * c.z;
+    Philox4 n;
+    n.x = hi1 ^ c.y ^ k0;
+    n.y = lo1;
+    n.z = hi0 ^ c.w ^ k1;
+    n.w = lo0;
+    c = n;
+  }
+  return c;
+}
+
+// Odd multiple of 2^-24 in (0, 1): exact in fp32.
+__device__ __forceinline__ float word_to_uniform(uint32_t w) {
+  return (float)(((w >> 9) << 1) | 1u) * 5.9604644775390625e-8f;  // * 2^-24
+}
+
+__device__ __forceinline__ uint32_t philox_word(const Philox4& r, int i) {
+  return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
+}
+
+constexpr uint32_t kResampleTag = 0x80000000u;
+
+}  // namespace simsd

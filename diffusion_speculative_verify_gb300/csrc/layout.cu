@@ -1,0 +1,61 @@
+// simsd_build_layout: paired data/mask layout, copied RoPE ids, packed step labels.
+//
+// SimSD notes (papernotes.org), "关键设计" items 1-3: the response part of the input is
+// [D_1..D_B | D~_1..D~_B]; D_k holds the draft token, D~_k is the [MASK] prediction slot
+// bound to it; every response slot carries a step label tau in 1..B (a permutation, per
+// the gist.science summary, section 2), and D~_k reuses the position id of D_k.
+// No mask is materialised: labels are enough to evaluate A_ij on the fly.
+#include "common.cuh"
+
+namespace simsd {
+
+// One warp per request; lane k handles slot k (B <= 32).
+__global__ void __launch_bounds__(128) build_layout_kernel(
+    const int32_t* __restrict__ tau, const int32_t* __restrict__ prompt_len, int batch, int B,
+    int32_t* __restrict__ pos_ids, uint8_t* __restrict__ labels, uint32_t* __restrict__ dev_err) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= batch) return;
+  const bool active = lane < B;
+  const int t = active ? tau[(size_t)r * B + lane] : 0;
+  const int P = prompt_len[r];
+  // tau is a permutation of 1..B  <=>  every value lies in 1..B and the B values cover
+  // all of 1..B (B values, B distinct bits set).
+  const bool in_range = !active || (t >= 1 && t <= B);
+  const unsigned bit = (active && t >= 1 && t <= B) ? (1u << (t - 1)) : 0u;
+  const unsigned covered = __reduce_or_sync(0xffffffffu, bit);
+  const unsigned full = (B == 32) ? 0xffffffffu : ((1u << B) - 1u);
+  const bool perm_ok = __all_sync(0xffffffffu, in_range) && covered == full;
+  uint32_t bad = 0;
+  if (!perm_ok) bad |= SIMSD_DEVERR_TAU;
+  if (P < 0) bad |= SIMSD_DEVERR_PROMPT_LEN;
+  if (!active) return;
+  const size_t row = (size_t)r * 2 * B;
+  if (bad) {
+    pos_ids[row + lane] = -1;
+    pos_ids[row + B + lane] = -1;
+    labels[row + lane] = kLabelInvalid;
+    labels[row + B + lane] = kLabelInvalid;
+    if (lane == 0) atomicOr(dev_err, bad);
+    return;
+  }
+  pos_ids[row + lane] = P + lane;      // D_k: next response position
+  pos_ids[row + B + lane] = P + lane;  // D~_k: copy of D_k's id
+  labels[row + lane] = (uint8_t)t;
+  labels[row + B + lane] = (uint8_t)(kSegMask | t);
+}
+
+}  // namespace simsd
+
+SIMSD_API simsd_status simsd_build_layout(const int32_t* tau, const int32_t* prompt_len,
+                                          int batch, int B, int32_t* pos_ids, uint8_t* labels,
+                                          uint32_t* dev_err, simsd_stream_t stream) {
+  if (batch < 0 || B < 1 || B > simsd::kMaxB) return SIMSD_ERR_INVALID_ARG;
+  if (batch == 0) return SIMSD_OK;
+  if (!tau || !prompt_len || !pos_ids || !labels || !dev_err) return SIMSD_ERR_INVALID_ARG;
+  const int warps = 4;
+  const int grid = (batch + warps - 1) / warps;
+  simsd::build_layout_kernel<<<grid, warps * 32, 0, (cudaStream_t)stream>>>(
+      tau, prompt_len, batch, B, pos_ids, labels, dev_err);
+  return simsd::last_launch_status();
+}

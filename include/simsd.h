@@ -1,0 +1,200 @@
+/*
+ * simsd.h -- C interface of the GB300 (sm_103a) SimSD single-forward verification step.
+ *
+ * The step has three calls, run in this order on one CUDA stream:
+ *
+ *   simsd_build_layout      paired layout [prompt | D_1..D_B | D~_1..D~_B]: copied RoPE
+ *                           position ids and packed step labels (no mask is stored).
+ *   simsd_verify_attention  one attention layer of the verify forward over that layout
+ *                           under the temporal-causal mask A_ij, evaluated on the fly.
+ *   simsd_accept            min(1, p/q) prefix acceptance along the step order, then
+ *                           residual resampling at the first rejected slot.
+ *
+ * Conventions shared by every call
+ *   - All array pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     reference after the call returns. Every call is asynchronous on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream), never synchronises and never
+ *     allocates memory. Scratch memory is a caller-provided `workspace`, sized by the
+ *     matching *_workspace() query.
+ *   - Errors the host can see (null pointers, unsupported sizes, a workspace that is too
+ *     small) are returned synchronously as a simsd_status and nothing is launched.
+ *   - Errors that depend on device data are OR-ed into the caller's 32-bit device error
+ *     word `dev_err` (SIMSD_DEVERR_* bits) and the affected request gets the documented
+ *     sentinel outputs. Kernels never trap, assert or print.
+ *   - Shapes: b = batch (requests), B = block size (1..32), Hq / Hkv query / key-value
+ *     heads (Hq % Hkv == 0, G = Hq / Hkv), D = head dim (64 or 128), V = vocabulary.
+ *     Response slot index s in [0, 2B): s < B is the data slot D_{s+1}, s >= B the mask
+ *     slot D~_{s-B+1}.
+ *
+ * Passages cited (pages on SimSD / S2D2 / SPOT):
+ *   [SimSD-1] SimSD notes (papernotes.org), "关键设计" item 1: paired data/mask layout.
+ *   [SimSD-2] same page, item 2: step labels tau in 1..B (prompt tau = 0) and the
+ *             four-case mask equation A_ij.
+ *   [SimSD-3] same page, item 3: the mask slot D~_k reuses the RoPE position id of D_k.
+ *   [SimSD-4] same page, item 4: alpha_r = min(1, p_theta / p_phi) in the draft's time
+ *             order, longest accepted prefix, in-place resampling of the rejected slot.
+ *   [SimSD-P] gist.science SimSD summary, sections 1-4 (same method; tau is a permutation).
+ *   [S2D2-5]  S2D2 page, "方法步骤详情" step (5): residual distribution (P_ver - P)^+.
+ *   [SPOT-G]  SPOT page, "Gumbel-Max 技巧与随机耦合": argmax(log p + G) samples p.
+ */
+#ifndef SIMSD_H
+#define SIMSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* simsd_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  SIMSD_OK = 0,
+  SIMSD_ERR_INVALID_ARG = 1, /* null pointer, bad size or combination of sizes        */
+  SIMSD_ERR_UNSUPPORTED = 2, /* valid request this build does not implement           */
+  SIMSD_ERR_WORKSPACE = 3,   /* workspace pointer null / misaligned / too small        */
+  SIMSD_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed (launch, encode)  */
+  SIMSD_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait ran out           */
+} simsd_status;
+
+/* Bits of the device error word. */
+#define SIMSD_DEVERR_TAU 1u        /* tau of a request is not a permutation of 1..B     */
+#define SIMSD_DEVERR_PROMPT_LEN 2u /* prompt length < 0                                 */
+#define SIMSD_DEVERR_TOKEN 4u      /* a verified draft token id is outside [0, V)       */
+#define SIMSD_DEVERR_TIMEOUT 8u    /* a bounded wait inside a kernel gave up            */
+
+/* Label byte of a response slot: (segment << 7) | tau, segment 0 = D, 1 = D~.
+ * 0xFF marks every slot of a request the layout call rejected. */
+#define SIMSD_LABEL_INVALID 0xFFu
+
+typedef enum { SIMSD_DTYPE_FP32 = 0, SIMSD_DTYPE_BF16 = 1 } simsd_dtype;
+
+/* Cache layouts of the packed prompt K/V (keys stored already rotated at positions
+ * 0..P-1 of their request):
+ *   NHD: [cache_tokens, Hkv, D]      HND: [Hkv, cache_tokens, D]   (both contiguous) */
+typedef enum { SIMSD_CACHE_NHD = 0, SIMSD_CACHE_HND = 1 } simsd_cache_layout;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* simsd_status_str(simsd_status s);
+
+/* Library interface version (major * 10000 + minor * 100 + patch). */
+int simsd_version(void);
+
+/* ---------------------------------------------------------------------------------
+ * simsd_build_layout  [SimSD-1], [SimSD-2], [SimSD-3], [SimSD-P] sections 1-3.
+ *
+ * Lays out the response part of [prompt | D_1..D_B | D~_1..D~_B] for each request:
+ *   pos_ids[r][k]     = P_r + k   for the data slot D_{k+1}         (k = 0..B-1)
+ *   pos_ids[r][B + k] = P_r + k   for the mask slot D~_{k+1} (copied id)
+ *   labels[r][k]      = tau[r][k]            (segment 0, data)
+ *   labels[r][B + k]  = 0x80 | tau[r][k]     (segment 1, mask)
+ * Prompt tokens have tau = 0 and positions 0..P_r-1 implicitly; no mask is stored.
+ *
+ *   tau        int32 [batch, B]   step label of each slot; must be a permutation of 1..B
+ *   prompt_len int32 [batch]      prompt length P_r >= 0
+ *   pos_ids    int32 [batch, 2B]  output
+ *   labels     uint8 [batch, 2B]  output
+ *   dev_err    uint32 [1]         error word, bits OR-ed in (never cleared here)
+ * Data errors: a request whose tau is not a permutation of 1..B (SIMSD_DEVERR_TAU) or
+ * whose P_r < 0 (SIMSD_DEVERR_PROMPT_LEN) gets pos_ids = -1 and labels = 0xFF.
+ * Returns SIMSD_ERR_INVALID_ARG for null pointers, batch < 0, B < 1 or B > 32.
+ * --------------------------------------------------------------------------------- */
+simsd_status simsd_build_layout(const int32_t* tau, const int32_t* prompt_len, int batch,
+                                int B, int32_t* pos_ids, uint8_t* labels, uint32_t* dev_err,
+                                simsd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * simsd_verify_attention  [SimSD-2], [SimSD-3], [SimSD-P] sections 2-4.
+ *
+ * One softmax-attention layer of the single verify forward. Response row s of request r
+ * and query head h (kv head h / G) attends to
+ *   - every prompt key of the request (tau = 0 is earlier than every step), and
+ *   - the response keys allowed by A_ij: with t = tau(s) + [s is a data slot], a data
+ *     key D_j is visible iff tau(j) < t and a mask key D~_j iff tau(j) >= t
+ *     (equivalent to the four cases of A_ij; every row sees exactly B response keys).
+ * Response queries and keys are rotated here (RoPE, pairs (d, d + D/2), angle
+ * pos * theta^(-2d/D)) with the copied ids from simsd_build_layout; V is not rotated.
+ * Output row = softmax(scale * q k^T) v over the visible keys; lse = natural-log
+ * sum-exp of the scaled scores (optional).
+ *
+ * BF16 path: tcgen05 tensor-core kernel (fp32 accumulation), split over the prompt keys
+ * and merged; FP32 path: CUDA-core kernel in fp32 throughout.
+ * --------------------------------------------------------------------------------- */
+typedef struct {
+  simsd_dtype dtype;        /* element type of q, k_resp, v_resp, k_cache, v_cache, out */
+  int batch, B, Hq, Hkv, D;
+  const void* q;            /* [batch, 2B, Hq, D]   pre-RoPE                            */
+  const void* k_resp;       /* [batch, 2B, Hkv, D]  pre-RoPE                            */
+  const void* v_resp;       /* [batch, 2B, Hkv, D]                                      */
+  const void* k_cache;      /* packed prompt keys (already rotated), see cache_layout   */
+  const void* v_cache;      /* packed prompt values, same layout                        */
+  simsd_cache_layout cache_layout;
+  int64_t cache_tokens;     /* number of token rows in the packed cache                 */
+  const int64_t* cache_start; /* int64 [batch]: first cache row of each request         */
+  const int32_t* prompt_len;  /* int32 [batch]: P_r; rows cache_start[r] .. + P_r - 1  */
+  const int32_t* pos_ids;   /* int32 [batch, 2B] from simsd_build_layout                */
+  const uint8_t* labels;    /* uint8 [batch, 2B] from simsd_build_layout                */
+  float rope_theta;         /* RoPE base theta (> 0)                                    */
+  float softmax_scale;      /* <= 0 selects 1/sqrt(D)                                   */
+  void* out;                /* [batch, 2B, Hq, D] output, dtype as the inputs           */
+  float* lse;               /* fp32 [batch, 2B, Hq] output, or NULL                     */
+  uint32_t* dev_err;        /* device error word                                        */
+} simsd_attn_params;
+/* Data errors: a request with labels 0xFF or P_r < 0 (bit SIMSD_DEVERR_PROMPT_LEN for
+ * the latter) gets zero output rows and lse = -inf. Host errors: SIMSD_ERR_INVALID_ARG
+ * (null pointer, Hq % Hkv != 0, B outside 1..32, negative sizes),
+ * SIMSD_ERR_UNSUPPORTED (D not 64/128; BF16 needs D = 128 and 2B*G <= 256 on this
+ * build; cache rows or pointers not 16-byte aligned), SIMSD_ERR_WORKSPACE. */
+
+/* Bytes of workspace simsd_verify_attention needs for these sizes (on the current
+ * device). The workspace must be 256-byte aligned; its contents need no initialisation
+ * and are scratch after the call. */
+size_t simsd_verify_attention_workspace(const simsd_attn_params* p);
+
+simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
+                                    size_t workspace_bytes, simsd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * simsd_accept  [SimSD-4], [SimSD-P] section 4, [S2D2-5], [SPOT-G].
+ *
+ * For each request r, with o_t = the slot whose step label is t (from labels' data
+ * half) and x_t = draft_tokens[r][o_t], for t = 1..gamma:
+ *   p = softmax(target_logits[r][o_t] / T), q = softmax(draft_logits[r][o_t] / T)
+ *   accept step t iff p[x_t] >= q[x_t] or u_t * q[x_t] < p[x_t]; stop at the first
+ *   rejection. accepted_len = a (number of leading accepted steps).
+ * If a < gamma, slot o_{a+1} is resampled from the normalised residual max(0, p - q)
+ * by the exponential race y = argmax_v r_v / E_v, E_v = -ln(u_v) (ties -> smallest v;
+ * if the residual is zero everywhere the race runs on p). No extra token is drawn when
+ * all gamma steps are accepted.
+ * Uniforms: Philox4x32-10 (Salmon et al., SC'11), key = (seed lo, seed hi);
+ *   step t (0-based)  counter (r, offset lo, offset hi, t / 4), word t % 4;
+ *   token v           counter (r, offset lo, offset hi, 0x80000000 | v / 4), word v % 4;
+ *   u = (2 * (word >> 9) + 1) * 2^-24.
+ *
+ *   target_logits, draft_logits  fp32 [batch, B, V], row k = block slot k
+ *   draft_tokens                 int32 [batch, B], token of data slot k
+ *   labels                       uint8 [batch, 2B] from simsd_build_layout
+ *   accepted_len                 int32 [batch]     a, or -1 for a rejected request
+ *   n_commit                     int32 [batch]     a + (a < gamma), or 0
+ *   out_tokens                   int32 [batch, B]  committed tokens in step order, -1 after
+ *   out_pos                      int32 [batch, B]  their slot indices, -1 after
+ * Requires 1 <= gamma <= B <= 32, V >= 1, temperature > 0 (T = 0 is
+ * SIMSD_ERR_UNSUPPORTED). Data errors: labels not a permutation (SIMSD_DEVERR_TAU) or a
+ * verified token outside [0, V) (SIMSD_DEVERR_TOKEN) -> accepted_len = -1, n_commit = 0,
+ * out_tokens = out_pos = -1 for that request.
+ * --------------------------------------------------------------------------------- */
+size_t simsd_accept_workspace(int batch, int B, int gamma, int V);
+
+simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
+                          const int32_t* draft_tokens, const uint8_t* labels, int batch,
+                          int B, int gamma, int V, float temperature, uint64_t seed,
+                          uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
+                          int32_t* out_pos, int32_t* n_commit, void* workspace,
+                          size_t workspace_bytes, uint32_t* dev_err, simsd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SIMSD_H */

@@ -201,7 +201,7 @@ def _order_from_labels(labels_row, B):
 
 
 def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
-           seed, offset, requests=None):
+           seed, offset, requests=None, request_ids=None):
     """Speculative acceptance along the draft's time order, then residual resampling.
 
     For steps r = 1..gamma: slot k = o_r, x = draft token at k, p = softmax(target
@@ -211,7 +211,8 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
     argmax_v r_v / E_v, E_v = -ln(u_v) (ties: smallest v; if the residual is all zero,
     race on p instead). Returns dict with accepted_len [b], n_commit [b], out_tokens
     [b, B], out_pos [b, B] (slot index, step order, -1 past n_commit), err, and
-    per-request diagnostics (decision margins, race top-2 keys).
+    per-request diagnostics (decision margins, race top-2 keys). ``request_ids`` maps
+    batch rows to the request index used in the Philox counters (default: the row).
     """
     tl = np.asarray(target_logits)
     dl = np.asarray(draft_logits)
@@ -234,7 +235,8 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
         if any(not (0 <= int(toks[r, k]) < V) for k in steps):
             err |= ERR_TOKEN
             continue
-        u = philox.accept_uniforms(seed, offset, r, gamma)
+        rid = r if request_ids is None else int(request_ids[r])
+        u = philox.accept_uniforms(seed, offset, rid, gamma)
         a = 0
         margins = []
         p = q = None
@@ -259,7 +261,7 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
             res = np.maximum(p - q, 0.0)
             if not np.any(res > 0):
                 res = p
-            uv = philox.resample_uniforms(seed, offset, r, V)
+            uv = philox.resample_uniforms(seed, offset, rid, V)
             keys = res / (-np.log(uv))
             y = int(np.argmax(keys))          # first maximum = smallest v on ties
             top2 = np.sort(keys)[-2:] if V > 1 else np.array([0.0, keys[0]])

@@ -1,0 +1,315 @@
+"""Parity of the CUDA path (called through the C interface) with the fp64 oracle.
+
+Integer work (layout, accept lengths, committed tokens and slots) must match bit for
+bit (accept mismatches are tolerated only at oracle-reported near-ties, which are
+counted); attention outputs must match within rel-L2 <= 1e-2 and max-abs <= 3e-2 for
+bf16 and 1e-5 for fp32.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    H.ensure_library()
+    import diffusion_speculative_verify_gb300 as pkg
+    pkg.load_library()
+    yield
+
+
+def _pkg():
+    import diffusion_speculative_verify_gb300 as pkg
+    return pkg
+
+
+def _step(w, inputs, meta, with_lse=True):
+    pkg = _pkg()
+    st = pkg.VerifyStep(inputs, gamma=w.gamma, rope_theta=w.rope_theta,
+                        temperature=w.temperature, cache_layout=meta["cache_layout"],
+                        with_lse=with_lse, philox_seed=meta["philox_seed"],
+                        philox_offset=meta["philox_offset"])
+    st.run()
+    torch.cuda.synchronize()
+    return st
+
+
+# ----------------------------------------------------------------------------- layout
+@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
+def test_layout_bit_exact(name):
+    w = W[name]
+    lay = workloads.make_layout_inputs(w)
+    tau, plen = lay["tau"].cuda(), lay["prompt_len"].cuda()
+    b, B = tau.shape
+    pos = torch.empty(b, 2 * B, dtype=torch.int32, device="cuda")
+    lab = torch.empty(b, 2 * B, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _pkg().simsd_build_layout(tau, plen, pos, lab, err)
+    rp, rl, re_ = oracle.build_layout(lay["tau"].numpy(), lay["prompt_len"].numpy())
+    assert np.array_equal(pos.cpu().numpy(), rp)
+    assert np.array_equal(lab.cpu().numpy(), rl)
+    assert int(err.item()) == re_ == 0
+
+
+def test_layout_invalid_requests_and_block_32():
+    B = 32
+    rng = np.random.default_rng(0)
+    tau = np.stack([rng.permutation(B) + 1 for _ in range(5)])
+    tau[1, 3] = tau[1, 4]          # duplicate
+    tau[2, 0] = 0                  # out of range
+    tau[3, 7] = 33
+    plen = np.array([10, 20, 30, 40, -5])
+    pos = torch.empty(5, 2 * B, dtype=torch.int32, device="cuda")
+    lab = torch.empty(5, 2 * B, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _pkg().simsd_build_layout(torch.tensor(tau, dtype=torch.int32).cuda(),
+                              torch.tensor(plen, dtype=torch.int32).cuda(), pos, lab, err)
+    rp, rl, re_ = oracle.build_layout(tau, plen)
+    assert np.array_equal(pos.cpu().numpy(), rp)
+    assert np.array_equal(lab.cpu().numpy(), rl)
+    assert int(err.item()) == re_ == (oracle.ERR_TAU | oracle.ERR_PROMPT_LEN)
+
+
+# -------------------------------------------------------------------------- attention
+def _attention_parity(w, inputs, meta, st, requests=None, kv_heads=None):
+    ref, ref_lse = H.oracle_attention(inputs, st.pos_ids, st.labels, w.rope_theta,
+                                      meta["cache_layout"], requests, kv_heads)
+    got = H.to_np(st.out)
+    got_lse = st.lse.cpu().numpy()
+    reqs = list(range(w.batch)) if requests is None else list(requests)
+    heads = list(range(w.Hkv)) if kv_heads is None else list(kv_heads)
+    g = H.select_heads(got[reqs], w.G, heads)
+    r = H.select_heads(ref[reqs], w.G, heads)
+    rel, mx = H.compare_attention(g, r, w.torch_dtype)
+    gl = H.select_heads(got_lse[reqs], w.G, heads)
+    rl = H.select_heads(ref_lse[reqs], w.G, heads)
+    tol = H.FP32_TOL if w.torch_dtype == torch.float32 else H.BF16_LSE_ABS
+    assert np.abs(gl - rl).max() <= tol
+    return rel, mx
+
+
+def test_attention_tiny_fp32_full():
+    w = W["tiny_fp32"]
+    inputs, meta = H.make_case(w)
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+
+
+SAMPLES = {
+    "gqa8b_bf16": ([0, 7, 15], [0, 5]),
+    "large_block_bf16": ([0, 31], [2, 7]),
+    "long_context_bf16": ([0, 5], [1, 6]),
+    "ragged_bf16": ([0, 1, 77, 200, 255], [0, 7]),
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_attention_bf16_full_size_sampled(name):
+    w = W[name]
+    inputs, meta = H.make_case(w)
+    st = _step(w, inputs, meta)
+    reqs, heads = SAMPLES[name]
+    _attention_parity(w, inputs, meta, st, reqs, heads)
+    assert int(st.dev_err.item()) == 0
+    # every output row is finite and every lse finite at full size
+    assert torch.isfinite(st.out.float()).all()
+    assert torch.isfinite(st.lse).all()
+
+
+MEDIUM = workloads.Workload(
+    name="medium_bf16", dtype="bf16", batch=4, Hq=8, Hkv=2, D=128, B=8, prompt_len=None,
+    prompt_len_range=(0, 1), rope_theta=1e6, gamma=8, V=4096)
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("B", [1, 4, 8, 16, 32])
+def test_attention_bf16_ragged_tiles_full_compare(layout, B):
+    w = MEDIUM.with_(B=B, gamma=B)
+    plen = [0, 61, 128, 1000 + 37][: w.batch]
+    inputs, meta = H.make_case(w, seed=B, cache_layout=layout, prompt_len=plen)
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+
+
+def test_attention_bf16_identity_tau_and_d64():
+    w = MEDIUM.with_(D=64, B=4, gamma=4)
+    tau = [[1, 2, 3, 4]] * w.batch
+    inputs, meta = H.make_case(w, seed=3, prompt_len=[5, 300, 0, 64], tau=tau)
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+
+
+def test_attention_fp32_ragged_and_long_positions():
+    w = W["tiny_fp32"].with_(batch=3, Hq=4, Hkv=2, D=128, B=8, gamma=8, rope_theta=1e6)
+    inputs, meta = H.make_case(w, seed=9, prompt_len=[0, 33, 777])
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+    # large absolute positions (RoPE angle accuracy): shift the prompt start
+    w2 = W["tiny_fp32"].with_(batch=1, B=4, gamma=4)
+    inputs, meta = H.make_case(w2, seed=10, prompt_len=[40000])
+    st = _step(w2, inputs, meta)
+    _attention_parity(w2, inputs, meta, st)
+
+
+def test_attention_invalid_request_rows_are_zero():
+    w = MEDIUM.with_(B=4, gamma=4)
+    tau = [[1, 2, 3, 4], [1, 1, 3, 4], [2, 1, 4, 3], [4, 3, 2, 1]]
+    inputs, meta = H.make_case(w, seed=4, prompt_len=[10, 20, 30, 40], tau=tau)
+    st = _step(w, inputs, meta)
+    assert int(st.dev_err.item()) & oracle.ERR_TAU
+    assert torch.count_nonzero(st.out[1].float()) == 0
+    assert torch.isneginf(st.lse[1]).all()
+    _attention_parity(w, inputs, meta, st, requests=[0, 2, 3])
+
+
+def test_masked_slots_do_not_influence_prediction_rows():
+    w = MEDIUM.with_(batch=1, B=8, gamma=8)
+    tau = [[3, 8, 1, 6, 2, 7, 4, 5]]
+    inputs, meta = H.make_case(w, seed=5, prompt_len=[300], tau=tau)
+    st = _step(w, inputs, meta)
+    base = st.out.clone()
+    t = tau[0]
+    i = 3                                   # prediction slot D~_3, tau = 6
+    for j in range(8):
+        for seg in (0, 1):
+            invisible = (t[j] >= t[i]) if seg == 0 else (t[j] < t[i])
+            if not invisible:
+                continue
+            inputs["k_resp"][0, seg * 8 + j] += 1.0
+            inputs["v_resp"][0, seg * 8 + j] -= 1.0
+    st.run()
+    torch.cuda.synchronize()
+    assert torch.equal(st.out[0, 8 + i], base[0, 8 + i])
+    # a visible response slot (the data slot decided at step 1) does change it
+    j = t.index(1)
+    inputs["v_resp"][0, j] += 1.0
+    st.run()
+    torch.cuda.synchronize()
+    assert not torch.equal(st.out[0, 8 + i], base[0, 8 + i])
+
+
+# ----------------------------------------------------------------------------- accept
+ACC_SAMPLE = {"tiny_fp32": None, "gqa8b_bf16": None, "large_block_bf16": None,
+              "long_context_bf16": None, "ragged_bf16": list(range(0, 256, 4))}
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
+def test_accept_bit_exact(name):
+    w = W[name]
+    inputs, meta = H.make_case(w)
+    st = _step(w, inputs, meta, with_lse=False)
+    reqs = ACC_SAMPLE[name] or list(range(w.batch))
+    res = H.oracle_accept(inputs, st.labels, w.gamma, w.temperature, meta["philox_seed"],
+                          meta["philox_offset"], requests=reqs)
+    got = {k: getattr(st, k).cpu().numpy() for k in
+           ("accepted_len", "n_commit", "out_tokens", "out_pos")}
+    ties = H.check_accept(res, got, reqs)
+    assert ties <= max(1, len(reqs) // 100)
+    assert int(st.dev_err.item()) == 0
+
+
+def test_accept_equal_logits_accept_everything():
+    w = W["gqa8b_bf16"].with_(batch=8, V=5000)
+    inputs, meta = H.make_case(w, seed=2)
+    inputs["draft_logits"].copy_(inputs["target_logits"])
+    st = _step(w, inputs, meta, with_lse=False)
+    assert st.accepted_len.tolist() == [w.gamma] * 8
+    assert st.n_commit.tolist() == [w.gamma] * 8
+
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 1.5])
+def test_accept_temperatures_and_odd_vocab(T):
+    w = W["tiny_fp32"].with_(batch=64, B=8, gamma=6, V=1001, temperature=T)
+    inputs, meta = H.make_case(w, seed=11)
+    st = _step(w, inputs, meta, with_lse=False)
+    reqs = list(range(w.batch))
+    res = H.oracle_accept(inputs, st.labels, w.gamma, T, meta["philox_seed"],
+                          meta["philox_offset"])
+    got = {k: getattr(st, k).cpu().numpy() for k in
+           ("accepted_len", "n_commit", "out_tokens", "out_pos")}
+    H.check_accept(res, got, reqs)
+    assert (st.accepted_len.cpu().numpy() < w.gamma).any()
+
+
+def test_accept_invalid_labels_and_tokens():
+    pkg = _pkg()
+    B, V = 4, 100
+    tl = torch.randn(3, B, V, device="cuda")
+    toks = torch.tensor([[1, 2, 3, 4], [1, 2, 300, 4], [0, 0, 0, 0]], dtype=torch.int32,
+                        device="cuda")
+    labels = torch.tensor([[1, 2, 3, 4, 129, 130, 131, 132],
+                           [1, 2, 3, 4, 129, 130, 131, 132],
+                           [1, 1, 3, 4, 129, 129, 131, 132]], dtype=torch.uint8, device="cuda")
+    out = {k: torch.full((3,), 7, dtype=torch.int32, device="cuda")
+           for k in ("accepted_len", "n_commit")}
+    ot = torch.zeros(3, B, dtype=torch.int32, device="cuda")
+    op = torch.zeros(3, B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkg.simsd_accept_workspace(3, B, B, V), dtype=torch.uint8, device="cuda")
+    pkg.simsd_accept(tl, tl, toks, labels, B, 1.0, 1, 0, out["accepted_len"], ot, op,
+                     out["n_commit"], ws, err)
+    torch.cuda.synchronize()
+    res = oracle.accept(tl.cpu().numpy(), tl.cpu().numpy(), toks.cpu().numpy(),
+                        labels.cpu().numpy(), B, 1.0, 1, 0)
+    assert out["accepted_len"].tolist() == res["accepted_len"].tolist() == [4, -1, -1]
+    assert out["n_commit"].tolist() == res["n_commit"].tolist()
+    assert np.array_equal(ot.cpu().numpy(), res["out_tokens"])
+    assert np.array_equal(op.cpu().numpy(), res["out_pos"])
+    assert int(err.item()) == res["err"] == (oracle.ERR_TAU | oracle.ERR_TOKEN)
+
+
+def test_accept_monte_carlo_commits_follow_target():
+    """2^16 requests with identical logits and draft tokens drawn from q: the committed
+    token of step 1 follows p (chi-square), E[accepted] matches the 1 - TV closed form."""
+    from scipy import stats
+    pkg = _pkg()
+    N, B, V = 1 << 16, 4, 16
+    g = torch.Generator(device="cpu").manual_seed(77)
+    tl1 = torch.randn(B, V, generator=g) * 1.5
+    dl1 = tl1 + torch.randn(B, V, generator=g)
+    p = torch.softmax(tl1.double(), -1).numpy()
+    q = torch.softmax(dl1.double(), -1).numpy()
+    tau = torch.tensor([2, 4, 1, 3], dtype=torch.int32)
+    order = [int((tau == t).nonzero()) for t in range(1, B + 1)]
+    toks = torch.stack([torch.multinomial(torch.tensor(q[k]), N, replacement=True, generator=g)
+                        for k in range(B)], 1).to(torch.int32)
+    labels = torch.cat([tau, tau + 128]).to(torch.uint8).repeat(N, 1)
+    tl = tl1.repeat(N, 1, 1).cuda()
+    dl = dl1.repeat(N, 1, 1).cuda()
+    al = torch.empty(N, dtype=torch.int32, device="cuda")
+    nc = torch.empty_like(al)
+    ot = torch.empty(N, B, dtype=torch.int32, device="cuda")
+    op = torch.empty_like(ot)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkg.simsd_accept_workspace(N, B, B, V), dtype=torch.uint8, device="cuda")
+    pkg.simsd_accept(tl, dl, toks.cuda(), labels.cuda(), B, 1.0, 99, 0, al, ot, op, nc, ws, err)
+    torch.cuda.synchronize()
+    a = al.cpu().numpy()
+    ot = ot.cpu().numpy()
+    beta = 1 - 0.5 * np.abs(p - q).sum(1)
+    bs = [beta[k] for k in order]
+    expected = sum(np.prod(bs[:k + 1]) for k in range(B))
+    assert abs(a.mean() - expected) < 4 * a.std() / math.sqrt(N) + 1e-3
+    for step, sel in ((0, np.ones(N, bool)), (1, a >= 1)):
+        counts = np.bincount(ot[sel, step], minlength=V)
+        e = p[order[step]] * sel.sum()
+        keep = e > 5
+        chi2 = ((counts[keep] - e[keep]) ** 2 / e[keep]).sum()
+        assert stats.chi2.sf(chi2, keep.sum() - 1) > 1e-4
+    # and bit-exact against the oracle on a slice of the same requests
+    reqs = list(range(0, N, 512))
+    res = oracle.accept(tl1.numpy()[None].repeat(N, 0), dl1.numpy()[None].repeat(N, 0),
+                        toks.numpy(), labels.numpy(), B, 1.0, 99, 0, requests=reqs)
+    got = {"accepted_len": a, "n_commit": nc.cpu().numpy(), "out_tokens": ot,
+           "out_pos": op.cpu().numpy()}
+    H.check_accept(res, got, reqs)

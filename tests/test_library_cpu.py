@@ -1,0 +1,89 @@
+"""CPU checks of the C library: it builds, loads, exports every function the header
+declares, and rejects bad host-side arguments synchronously (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.helpers import ensure_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(simsd_\w+)\s*\(", text, re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_library()
+    import diffusion_speculative_verify_gb300 as pkg
+    return pkg.load_library()
+
+
+def test_header_declares_the_three_calls():
+    names = _declared_functions()
+    for n in ("simsd_build_layout", "simsd_verify_attention", "simsd_accept",
+              "simsd_verify_attention_workspace", "simsd_accept_workspace"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+    import diffusion_speculative_verify_gb300 as pkg
+    assert set(pkg.EXPORTED) == set(names)
+
+
+def test_status_strings_and_version(lib):
+    import diffusion_speculative_verify_gb300 as pkg
+    assert pkg.simsd_status_str(0) == "SIMSD_OK"
+    assert pkg.simsd_status_str(3) == "SIMSD_ERR_WORKSPACE"
+    assert pkg.simsd_status_str(99) == "SIMSD_ERR_UNKNOWN"
+    assert pkg.simsd_version() >= 100
+
+
+def test_host_argument_errors_return_status(lib):
+    # nothing below reaches a kernel launch
+    assert lib.simsd_build_layout(None, None, 4, 0, None, None, None, None) == 1
+    assert lib.simsd_build_layout(None, None, 4, 33, None, None, None, None) == 1
+    assert lib.simsd_build_layout(None, None, 4, 4, None, None, None, None) == 1
+    assert lib.simsd_build_layout(None, None, 0, 4, None, None, None, None) == 0
+    # temperature 0 (greedy) is not implemented; gamma > B is invalid
+    args = [None] * 4 + [2, 4, 4, 100, 0.0, 0, 0] + [None] * 4 + [None, 0, None, None]
+    assert lib.simsd_accept(*args) == 2
+    args[8] = 1.0
+    args[6] = 5
+    assert lib.simsd_accept(*args) == 1
+    args[6] = 4
+    assert lib.simsd_accept(*args) == 1          # null pointers
+    assert lib.simsd_accept_workspace(2, 4, 4, 100) > 0
+    assert lib.simsd_accept_workspace(2, 4, 5, 100) == 0
+
+
+def test_attention_parameter_checks(lib):
+    import diffusion_speculative_verify_gb300 as pkg
+    p = pkg.AttnParams()
+    p.dtype, p.batch, p.B, p.Hq, p.Hkv, p.D = 0, 1, 4, 4, 1, 64
+    p.rope_theta = 1e4
+    assert lib.simsd_verify_attention_workspace(ctypes.byref(p)) > 0
+    assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1  # null pointers
+    p.Hq = 3
+    assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1
+    p.Hq, p.D = 4, 96
+    assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 2
+    p.D, p.B = 64, 40
+    assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1
+    p.B, p.rope_theta = 4, 0.0
+    assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1
