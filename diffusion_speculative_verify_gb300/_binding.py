@@ -22,14 +22,15 @@ DEVERR_TAU, DEVERR_PROMPT_LEN, DEVERR_TOKEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 CACHE_NHD, CACHE_HND = 0, 1
 
-EXPORTED = ["simsd_status_str", "simsd_version", "simsd_build_layout",
+EXPORTED = ["simsd_status_str", "simsd_version", "simsd_last_cuda_error", "simsd_build_layout",
             "simsd_verify_attention_workspace", "simsd_verify_attention",
             "simsd_accept_workspace", "simsd_accept"]
 
 
 class SimsdError(RuntimeError):
-    def __init__(self, status: int, what: str):
-        super().__init__(f"{what} failed: {STATUS_NAMES.get(status, status)}")
+    def __init__(self, status: int, what: str, detail: str = ""):
+        msg = f"{what} failed: {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.status = status
 
 
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.simsd_status_str.restype = ctypes.c_char_p
     lib.simsd_version.argtypes = []
     lib.simsd_version.restype = i32
+    lib.simsd_last_cuda_error.argtypes = []
+    lib.simsd_last_cuda_error.restype = ctypes.c_char_p
     lib.simsd_build_layout.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
     lib.simsd_build_layout.restype = i32
     lib.simsd_verify_attention_workspace.argtypes = [ctypes.POINTER(AttnParams)]
@@ -101,7 +104,8 @@ def _check(t, name, dtype=None, device=None):
 
 def _raise(st, what):
     if st != SIMSD_OK:
-        raise SimsdError(st, what)
+        detail = load_library().simsd_last_cuda_error().decode() if st == 4 else ""
+        raise SimsdError(st, what, detail)
 
 
 def simsd_status_str(status: int) -> str:
@@ -110,6 +114,10 @@ def simsd_status_str(status: int) -> str:
 
 def simsd_version() -> int:
     return load_library().simsd_version()
+
+
+def simsd_last_cuda_error() -> str:
+    return load_library().simsd_last_cuda_error().decode()
 
 
 def simsd_build_layout(tau, prompt_len, pos_ids, labels, dev_err, stream=None):

@@ -1,5 +1,7 @@
 // Status strings, version, and the verify-attention entry points (dispatch between the
 // tcgen05 bf16 kernel and the CUDA-core kernel).
+#include <stdio.h>
+
 #include "attn_common.cuh"
 
 namespace simsd {
@@ -23,6 +25,16 @@ SIMSD_API const char* simsd_status_str(simsd_status s) {
 }
 
 SIMSD_API int simsd_version(void) { return 100; }
+
+namespace simsd {
+static thread_local char g_last_error[256];
+void record_cuda_error(const char* what, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s%s%s (%d)", what, what[0] ? ": " : "",
+           cudaGetErrorString(e), (int)e);
+}
+}  // namespace simsd
+
+SIMSD_API const char* simsd_last_cuda_error(void) { return simsd::g_last_error; }
 
 SIMSD_API size_t simsd_verify_attention_workspace(const simsd_attn_params* p) {
   if (simsd::check_attn_sizes(p) != SIMSD_OK) return 0;

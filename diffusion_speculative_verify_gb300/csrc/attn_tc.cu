@@ -31,6 +31,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdio.h>
+
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -48,28 +50,50 @@ constexpr uint32_t kStageBytes = 2 * kKVTile;         // K + V
 constexpr uint32_t kQBlock = 2 * kBlockRows * 128;    // 32 KB: 128 rows x 128 dims
 constexpr uint32_t kPBlock = kBlockRows * 128;        // 16 KB: 128 rows x 64 keys
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
+#ifndef SIMSD_L2_PREFETCH_TILES
+#define SIMSD_L2_PREFETCH_TILES 0
+#endif
+constexpr uint32_t kPrefetchTiles = SIMSD_L2_PREFETCH_TILES;  // L2 prefetch distance beyond the ring
+constexpr int kMaxStages = 8;                         // stage barriers reserved in shared memory
 
+// NRB = 1: up to 128 query rows per pair; the two softmax warpgroups split each row's 64
+//          key columns (32 each) and keep separate O accumulators, merged at the end.
+// NRB = 2: up to 256 rows; warpgroup w owns row block w and all 64 columns.
 template <int NRB>
 struct Cfg {
-  static constexpr int kStages = NRB == 1 ? 4 : 2;
-  static constexpr int kSoftmaxThreads = 128 * NRB;
-  static constexpr int kProducerWarp = 4 * NRB;
-  static constexpr int kMmaWarp = 4 * NRB + 1;
+  static constexpr bool kSplitCols = NRB == 1;
+  // NRB = 1 keeps the rotated Q in TMEM and issues S = Q K^T with A from TMEM (a
+  // shared-memory A operand costs a fixed ~70 cycles per M=128 K=16 instruction, TMEM ~45)
+  static constexpr bool kQInTmem = NRB == 1;
+  static constexpr int kCols = kSplitCols ? 32 : 64;  // S columns per softmax thread
+  static constexpr int kStages = NRB == 1 ? 5 : 2;
+  // S is issued this many tiles ahead of P V; tiles jj .. jj + kSAhead hold stages until
+  // P V of tile jj completes, so kSAhead <= kStages - 1 keeps the producer able to refill
+  static constexpr int kSAhead = kStages - 1;
+  static_assert(kSAhead >= 1 && kSAhead <= kStages - 1, "lookahead vs stages");
+  static constexpr int kSoftmaxThreads = 256;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
   static constexpr int kThreads = kSoftmaxThreads + 64;
-  static constexpr uint32_t kTmemCols = 256 * NRB;
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffP = kOffQ + NRB * kQBlock;            // [rb][buf]
+  static constexpr uint32_t kOffP = kOffQ + (kQInTmem ? 0 : NRB * kQBlock);  // [rb][buf]
   static constexpr uint32_t kOffStages = kOffP + NRB * 2 * kPBlock;
   static constexpr uint32_t kOffTail = kOffStages + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffTail + kStageBytes;
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + base alignment
+  // TMEM columns: S buffers [rb][buf] x 64, two 128-column O accumulators, then (NRB = 1)
+  // the rotated Q as bf16 pairs (64 columns)
   static constexpr uint32_t tmem_s(int rb, int buf) { return (uint32_t)(rb * 2 + buf) * 64u; }
-  static constexpr uint32_t tmem_o(int rb) { return (uint32_t)NRB * 128u + (uint32_t)rb * 128u; }
+  static constexpr uint32_t tmem_o(int idx) { return (uint32_t)NRB * 128u + (uint32_t)idx * 128u; }
+  static constexpr uint32_t kTmemQ = 384;
+  static_assert(kStages <= kMaxStages, "stage barriers");
 };
 
 struct TcArgs {
   int batch, B, Hq, Hkv, G, R, nrb, ctas;  // R = 2B*G real rows per pair
+  int tile_keys;                           // prompt keys per tile (64 or 128)
   int layout;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_resp;
@@ -78,13 +102,21 @@ struct TcArgs {
   const int32_t* prompt_len;
   const int32_t* pos_ids;
   const uint8_t* labels;
-  float scale_log2;
+  float scale_log2;  // softmax scale * log2(e), folded into the rotated queries
   __nv_bfloat16* out;
   float* lse;
   uint32_t* dev_err;
   float* ws_o;     // [2 * ctas][nrb * 128][128] partial numerators
   float2* ws_ml;   // [2 * ctas][nrb * 128] partial (max, sum), log2 domain
+  struct MergeDesc* ws_desc;  // [ctas] split pair starting in each CTA (or none)
   RopeTable rope;
+};
+
+// Written by every CTA for the pair its range ends in, when that pair started inside the
+// range and continues past it; the merge kernel combines that pair's pieces.
+struct MergeDesc {
+  int b, h, c_last, slot0;  // b < 0: no split pair starts here
+  long long T;
 };
 
 // ----------------------------------------------------------------------- scheduling
@@ -93,7 +125,7 @@ __device__ __forceinline__ bool request_invalid(const TcArgs& a, int b) {
 }
 __device__ __forceinline__ int tiles_per_pair(const TcArgs& a, int b) {
   if (request_invalid(a, b)) return 1;
-  return 1 + (a.prompt_len[b] + kTileKeys - 1) / kTileKeys;
+  return 1 + (a.prompt_len[b] + a.tile_keys - 1) / a.tile_keys;
 }
 
 // CTA c covers global tiles [c*T/C, (c+1)*T/C).
@@ -191,17 +223,50 @@ struct SegIter {
   }
 };
 
+// Yields the prompt tiles (kv head, first cache row) of one CTA's range, in order.
+struct PromptTiles {
+  SegIter it;
+  int i;
+  bool have;
+  __device__ void init(const TcArgs& a, const SchedStart& s) {
+    it.init(a, s);
+    have = false;
+  }
+  __device__ bool next(const TcArgs& a, int& h, int& tok) {
+    while (true) {
+      if (!have) {
+        if (!it.next(a)) return false;
+        have = true;
+        i = it.i0;
+      }
+      if (!it.invalid) {
+        while (i < it.i0 + it.n) {
+          const int ii = i++;
+          if (ii == 0) continue;
+          h = it.h;
+          tok = (int)(a.cache_start[it.b] + (int64_t)(ii - 1) * a.tile_keys);
+          return true;
+        }
+      }
+      it.advance(a);
+      have = false;
+    }
+  }
+};
+
 // --------------------------------------------------------------------- small helpers
+enum BarIdx { kFull0 = 0, kEmpty0 = kMaxStages, kSFull0 = 2 * kMaxStages, kSFree0 = kSFull0 + 2,
+              kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kQFull = kPFree0 + 2, kDrain = kQFull + 1,
+              kNumBars = kDrain + 1 };
+
 struct Shared {
-  uint64_t bars[20];
+  uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort;
   int64_t T, t0, t1, Tb;
   int b;
 };
 
-enum BarIdx { kFull0 = 0, kEmpty0 = 4, kSFull0 = 8, kSFree0 = 10, kPFull0 = 12, kPFree0 = 14,
-              kQFull = 16, kDrain = 17 };
 
 __device__ __forceinline__ bool wait_bar(Shared* sh, uint32_t bar, uint32_t parity,
                                          uint32_t* dev_err) {
@@ -234,8 +299,9 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 }
 
 // Rotates the 16 chunks (8 bf16 each) of one 128-element row held in `v` (chunk c pairs
-// with chunk c + 8: elements d and d + 64) at position `pos`.
-__device__ __forceinline__ void rope_row(uint4 (&v)[16], int pos, const RopeTable& rt) {
+// with chunk c + 8: elements d and d + 64) with the (cos, sin) table `cs` of its position
+// (64 float2 entries, one per pair), and multiplies by `scale`.
+__device__ __forceinline__ void rope_row(uint4 (&v)[16], const float2* cs, float scale) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint32_t* lo = reinterpret_cast<uint32_t*>(&v[c]);
@@ -243,13 +309,11 @@ __device__ __forceinline__ void rope_row(uint4 (&v)[16], int pos, const RopeTabl
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int d0 = 8 * c + 2 * e;
-      float s0, c0, s1, c1;
-      rope_sincos(pos, rt.c_hi[d0], rt.c_lo[d0], &s0, &c0);
-      rope_sincos(pos, rt.c_hi[d0 + 1], rt.c_lo[d0 + 1], &s1, &c1);
+      const float4 t = *reinterpret_cast<const float4*>(cs + d0);  // cos0, sin0, cos1, sin1
       const float x0 = bf16_lo(lo[e]), x1 = bf16_hi(lo[e]);
       const float y0 = bf16_lo(hi[e]), y1 = bf16_hi(hi[e]);
-      lo[e] = pack_bf16(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-      hi[e] = pack_bf16(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
+      lo[e] = pack_bf16((x0 * t.x - y0 * t.y) * scale, (x1 * t.z - y1 * t.w) * scale);
+      hi[e] = pack_bf16((x0 * t.y + y0 * t.x) * scale, (x1 * t.w + y1 * t.z) * scale);
     }
   }
 }
@@ -274,6 +338,7 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ TcArgs a) {
   using C = Cfg<NRB>;
+  static_assert(sizeof(Shared) <= C::kBarBytes, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Shared* sh = reinterpret_cast<Shared*>(smem + C::kOffBar);
@@ -327,36 +392,48 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      SegIter it;
-      it.init(a, st);
-      uint32_t m = 0;
+      PromptTiles tiles, ahead;
+      tiles.init(a, st);
+      ahead.init(a, st);
+      uint32_t m = 0, prefetched = 0;
       bool ok = true;
-      while (ok && it.next(a)) {
-        if (!it.invalid) {
-          const int64_t start = a.cache_start[it.b];
-          for (int i = it.i0; i < it.i0 + it.n && ok; ++i) {
-            if (i == 0) continue;  // response tail: staged by the softmax warps
-            const int s = m % C::kStages;
-            ok = wait_bar(sh, bar(kEmpty0 + s), ((m / C::kStages) & 1) ^ 1, a.dev_err);
-            if (!ok) break;
-            ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStageBytes);
-            const int tok = (int)(start + (int64_t)(i - 1) * kTileKeys);
-            const uint32_t kdst = sbase + C::kOffStages + s * kStageBytes;
-            const uint32_t vdst = kdst + kKVTile;
+      int h, tok;
+      while (ok && tiles.next(a, h, tok)) {
+        // keep the L2 warm kPrefetchTiles tiles beyond the shared-memory ring
+        int hp, tp;
+        while (kPrefetchTiles > 0 && prefetched <= m + C::kStages + kPrefetchTiles &&
+               ahead.next(a, hp, tp)) {
+          if (prefetched >= (uint32_t)C::kStages) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               if (a.layout == SIMSD_CACHE_NHD) {
-                ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, it.h, tok, bar(kFull0 + s));
-                ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, it.h, tok, bar(kFull0 + s));
+                ptx::tma_prefetch_l2_3d(&tmk, half * 64, hp, tp);
+                ptx::tma_prefetch_l2_3d(&tmv, half * 64, hp, tp);
               } else {
-                ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, tok, it.h, bar(kFull0 + s));
-                ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, tok, it.h, bar(kFull0 + s));
+                ptx::tma_prefetch_l2_3d(&tmk, half * 64, tp, hp);
+                ptx::tma_prefetch_l2_3d(&tmv, half * 64, tp, hp);
               }
             }
-            ++m;
+          }
+          ++prefetched;
+        }
+        const int s = m % C::kStages;
+        ok = wait_bar(sh, bar(kEmpty0 + s), ((m / C::kStages) & 1) ^ 1, a.dev_err);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStageBytes);
+        const uint32_t kdst = sbase + C::kOffStages + s * kStageBytes;
+        const uint32_t vdst = kdst + kKVTile;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (a.layout == SIMSD_CACHE_NHD) {
+            ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, h, tok, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, h, tok, bar(kFull0 + s));
+          } else {
+            ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, tok, h, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, tok, h, bar(kFull0 + s));
           }
         }
-        it.advance(a);
+        ++m;
       }
       if (!ok) {  // let the loads already issued land before shared memory goes away
         const uint32_t issued = m;
@@ -377,55 +454,36 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
       it.init(a, st);
       uint32_t j = 0, m = 0, nseg = 0;
       bool ok = true;
-      // per S/P buffer: where the tile's V lives and which stage to release
-      uint32_t vaddr_of[2] = {0, 0};
-      int stage_of[2] = {-1, -1};
-      auto issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
+      // per tile (ring of 8 >= kSAhead + 1 tiles between the oldest pending P V and the
+      // newest S): where its V lives and which stage its P V releases
+      uint32_t vaddr_of[8];
+      int stage_of[8];
+      static_assert(C::kSAhead + 1 <= 8, "tile ring");
+      // S_jj = Q K_jj^T into S buffer jj % 2 (free once the softmax has read S_{jj-2}).
+      // Non-blocking: returns false (and issues nothing) while K_jj or the buffer is busy.
+      auto try_issue_s = [&](uint32_t jj, int i) -> bool {
         const int buf = jj & 1;
-        if (!wait_bar(sh, bar(kPFull0 + buf), (jj >> 1) & 1, a.dev_err)) return false;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int rb = 0; rb < NRB; ++rb) {
-          const uint32_t pbase = sbase + C::kOffP + (rb * 2 + buf) * kPBlock;
-#pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(pbase + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(vaddr_of[buf] + kk * 16 * 128, kHalfTile, 1024);
-            ptx::mma_f16_ss(tmem + C::tmem_o(rb), ad, bd, idPV, (first_in_seg && kk == 0) ? 0u : 1u);
-          }
+        const int s = m % C::kStages;
+        if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / C::kStages) & 1)) return false;
+        if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj >> 1) & 1) ^ 1)) return false;
+        uint32_t kaddr;
+        if (i == 0) {
+          kaddr = sbase + C::kOffTail;
+          stage_of[jj & 7] = -1;
+        } else {
+          kaddr = sbase + C::kOffStages + s * kStageBytes;
+          stage_of[jj & 7] = s;
+          ++m;
         }
-        ptx::mma_commit(bar(kPFree0 + buf));
-        if (stage_of[buf] >= 0) ptx::mma_commit(bar(kEmpty0 + stage_of[buf]));
-        return true;
-      };
-      while (ok && it.next(a)) {
-        if (it.invalid) {
-          it.advance(a);
-          continue;
-        }
-        ok = wait_bar(sh, bar(kQFull), nseg & 1, a.dev_err);
-        if (!ok) break;
+        vaddr_of[jj & 7] = kaddr + kKVTile;
         ptx::tc_fence_after();
-        const uint32_t jfirst = j;
-        for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
-          const int buf = j & 1;
-          uint32_t kaddr;
-          if (i == 0) {
-            kaddr = sbase + C::kOffTail;
-            vaddr_of[buf] = kaddr + kKVTile;
-            stage_of[buf] = -1;
-          } else {
-            const int s = m % C::kStages;
-            ok = wait_bar(sh, bar(kFull0 + s), (m / C::kStages) & 1, a.dev_err);
-            if (!ok) break;
-            kaddr = sbase + C::kOffStages + s * kStageBytes;
-            vaddr_of[buf] = kaddr + kKVTile;
-            stage_of[buf] = s;
-            ++m;
+        if constexpr (C::kQInTmem) {
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
+            ptx::mma_f16_ts(tmem + C::tmem_s(0, buf), tmem + C::kTmemQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
           }
-          ok = wait_bar(sh, bar(kSFree0 + buf), ((j >> 1) & 1) ^ 1, a.dev_err);
-          if (!ok) break;
-          ptx::tc_fence_after();
+        } else {
 #pragma unroll
           for (int rb = 0; rb < NRB; ++rb) {
             const uint32_t qbase = sbase + C::kOffQ + rb * kQBlock;
@@ -437,14 +495,78 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
               ptx::mma_f16_ss(tmem + C::tmem_s(rb, buf), ad, bd, idS, kk > 0 ? 1u : 0u);
             }
           }
-          ptx::mma_commit(bar(kSFull0 + buf));
-          if (j > jfirst) {
-            ok = issue_pv(j - 1, j - 1 == jfirst);
-            if (!ok) break;
+        }
+        ptx::mma_commit(bar(kSFull0 + buf));
+        return true;
+      };
+      // O (+)= P_jj V_jj once the softmax has written P_jj. Non-blocking like try_issue_s.
+      auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
+        const int buf = jj & 1;
+        if (!ptx::mbar_test(bar(kPFull0 + buf), (jj >> 1) & 1)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int rb = 0; rb < NRB; ++rb) {
+          const uint32_t pbase = sbase + C::kOffP + (rb * 2 + buf) * kPBlock;
+#pragma unroll
+          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+            // key slice kk (16 keys) of P and V; with split columns, keys 0-31 feed O[0]
+            // and keys 32-63 feed O[1]
+            const int oidx = C::kSplitCols ? (kk >> 1) : rb;
+            const bool first_k = C::kSplitCols ? ((kk & 1) == 0) : (kk == 0);
+            const uint64_t ad = ptx::sdesc_sw128(pbase + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(vaddr_of[jj & 7] + kk * 16 * 128, kHalfTile, 1024);
+            ptx::mma_f16_ss(tmem + C::tmem_o(oidx), ad, bd, idPV, (first_in_seg && first_k) ? 0u : 1u);
+          }
+        }
+        ptx::mma_commit(bar(kPFree0 + buf));
+        if (stage_of[jj & 7] >= 0) ptx::mma_commit(bar(kEmpty0 + stage_of[jj & 7]));
+        return true;
+      };
+      while (ok && it.next(a)) {
+        if (it.invalid) {
+          it.advance(a);
+          continue;
+        }
+        ok = wait_bar(sh, bar(kQFull), nseg & 1, a.dev_err);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        // Event loop over the segment's tiles: P V of the oldest tile is issued as soon as
+        // its P is ready (it frees a stage), S of the next tile as soon as its K has landed
+        // and its S buffer is free; S may run up to kSAhead tiles ahead of P V.
+        constexpr uint32_t A = C::kSAhead;
+        const uint32_t jfirst = j, jend = j + (uint32_t)it.n;
+        uint32_t ns = jfirst, npv = jfirst;
+        uint64_t t_idle = 0;
+        uint32_t spins = 0;
+        while (npv < jend) {
+          bool progressed = false;
+          if (npv < ns && try_issue_pv(npv, npv == jfirst)) {
+            ++npv;
+            progressed = true;
+          }
+          if (ns < jend && ns <= npv + A && try_issue_s(ns, it.i0 + (int)(ns - jfirst))) {
+            ++ns;
+            progressed = true;
+          }
+          if (progressed) {
+            spins = 0;
+            continue;
+          }
+          if ((++spins & 63) == 0) {  // bounded: give up after kWaitLimitNs without progress
+            const uint64_t now = ptx::globaltimer_ns();
+            if (spins == 64) t_idle = now;
+            if (*(volatile int*)&sh->abort || now - t_idle > kWaitLimitNs) {
+              if (!*(volatile int*)&sh->abort) {
+                *(volatile int*)&sh->abort = 1;
+                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
+              }
+              ok = false;
+              break;
+            }
           }
         }
         if (!ok) break;
-        ok = issue_pv(j - 1, j - 1 == jfirst);
+        j = jend;
         ++nseg;
         it.advance(a);
       }
@@ -457,9 +579,13 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax warps
-    const int rb = warp >> 2;                // row block of this warpgroup
-    const int lrow = (warp & 3) * 32 + lane;  // TMEM lane = row within the block
-    const int row = rb * kBlockRows + lrow;   // row within the pair
+    constexpr int NC = C::kCols;
+    const int wg = warp >> 2;                       // softmax warpgroup 0 / 1
+    const int rb = C::kSplitCols ? 0 : wg;          // row block
+    const int col0 = C::kSplitCols ? 32 * wg : 0;   // first S column of this thread
+    const int oidx = C::kSplitCols ? wg : rb;       // O accumulator
+    const int lrow = (warp & 3) * 32 + lane;        // TMEM lane = row within the block
+    const int row = rb * kBlockRows + lrow;         // row within the pair
     const bool real = row < a.R;
     const int s_slot = real ? row / a.G : 0;
     const int g = real ? row % a.G : 0;
@@ -467,12 +593,544 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
     uint8_t* qtile = smem + C::kOffQ + rb * kQBlock;
     uint8_t* tailk = smem + C::kOffTail;
     uint8_t* tailv = tailk + kKVTile;
+    const bool q_writer = !C::kSplitCols || wg == 0;
+    const bool tail_writer = C::kSplitCols ? (wg == 1) : (wg == 0);
     SegIter it;
     it.init(a, st);
     uint32_t j = 0;
     bool ok = true;
+    MergeDesc desc;
+    desc.b = -1;
+    desc.T = st.T;
     while (ok && it.next(a)) {
       const int b = it.b, h = it.h;
+      if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
+        const int64_t pe = it.t + it.nt;
+        desc.b = b;
+        desc.h = h;
+        desc.c_last = (int)((pe * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
+        desc.slot0 = 2 * blockIdx.x + (it.first ? 0 : 1);
+      }
+      const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
+      if (it.invalid) {
+        if (real && q_writer) {
+          uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
+          if (a.lse) a.lse[orow] = -INFINITY;
+        }
+        if (tid == 0 && h == 0 && a.prompt_len[b] < 0) atomicOr(a.dev_err, SIMSD_DEVERR_PROMPT_LEN);
+        it.advance(a);
+        continue;
+      }
+      const int P = a.prompt_len[b];
+      // ---- segment prologue: rotated Q rows (and the response tail tile)
+      // (cos, sin) of the 2B response positions, computed once per segment into the P
+      // area (idle here: the previous segment's last P V has completed)
+      float2* rtab = reinterpret_cast<float2*>(smem + C::kOffP);
+      for (int e = tid; e < twoB * 64; e += C::kSoftmaxThreads) {
+        const int sidx = e >> 6, d = e & 63;
+        float sn, cs;
+        rope_sincos(a.pos_ids[(size_t)b * twoB + sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
+        rtab[e] = make_float2(cs, sn);
+      }
+      ptx::named_bar_sync(1, C::kSoftmaxThreads);
+      {
+        uint4 v[16];
+        if (q_writer) {
+          if (real) {
+            load_row(v, a.q + orow * kD);
+            rope_row(v, rtab + s_slot * 64, a.scale_log2);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+          }
+          if constexpr (C::kQInTmem) {
+            // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
+            uint32_t w[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                w[4 * c] = v[8 * half + c].x;
+                w[4 * c + 1] = v[8 * half + c].y;
+                w[4 * c + 2] = v[8 * half + c].z;
+                w[4 * c + 3] = v[8 * half + c].w;
+              }
+              ptx::tmem_st32(tmem + lane_off + C::kTmemQ + 32 * half, w);
+            }
+            ptx::tmem_st_wait();
+          } else {
+            store_row_sw(qtile, kBlockRows * 128, lrow, v);
+          }
+        }
+        if (it.has_tail && tail_writer) {
+          const int key = lrow & 63;
+          const bool is_v = lrow >= 64;
+          if (key < twoB) {
+            const size_t krow = (((size_t)b * twoB + key) * a.Hkv + h) * kD;
+            load_row(v, (is_v ? a.v_resp : a.k_resp) + krow);
+            if (!is_v) rope_row(v, rtab + key * 64, 1.f);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+          }
+          store_row_sw(is_v ? tailv : tailk, kHalfTile, key, v);
+        }
+      }
+      ptx::named_bar_sync(1, C::kSoftmaxThreads);  // table reads done before P reuses the area
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kQFull));
+      // visibility of this thread's response-key columns (bit c = column col0 + c visible)
+      uint64_t vis = 0;
+      if (it.has_tail) {
+        const uint8_t* lab = a.labels + (size_t)b * twoB;
+        if (real) {
+          const int t = row_threshold(lab[s_slot]);
+          for (int k = 0; k < twoB; ++k)
+            if (response_key_visible(lab[k], t)) vis |= 1ull << k;
+        } else {
+          vis = twoB == 64 ? ~0ull : ((1ull << twoB) - 1);
+        }
+        vis >>= col0;
+      }
+      float m_used = -INFINITY, l = 0.f;
+      const uint32_t jfirst = j;
+      for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
+        const int buf = j & 1;
+        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        float x[NC];
+        {
+          uint32_t sa[32];
+          const uint32_t ts = tmem + lane_off + C::tmem_s(rb, buf) + col0;
+          if constexpr (NC == 32) {
+            ptx::tmem_ld32(ts, sa);
+            ptx::tmem_ld_wait(sa);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sa[c]);
+          } else {
+            uint32_t sb[32];
+            ptx::tmem_ld32(ts, sa);
+            ptx::tmem_ld32(ts + 32, sb);
+            ptx::tmem_ld_wait(sa);
+            ptx::tmem_ld_wait(sb);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              x[c] = __uint_as_float(sa[c]);
+              x[c + 32] = __uint_as_float(sb[c]);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kSFree0 + buf));
+        if (i == 0) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) x[c] = ((vis >> c) & 1ull) ? x[c] : -INFINITY;
+        } else {
+          const int nvalid = P - (i - 1) * kTileKeys - col0;
+          if (nvalid < NC) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
+          }
+        }
+        float mt;
+        {
+          float mx[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = x[u];
+#pragma unroll
+          for (int c = 8; c < NC; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+          mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        }
+        // lazy rescale: only when some row's max grew by more than 2^8; warp-uniform because
+        // TMEM loads/stores are warp-collective
+        if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
+          const float m_new = fmaxf(m_used, mt);
+          if (j != jfirst) {  // rescale O: the previous P V must have landed
+            const uint32_t jp = j - 1;
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(sh, bar(kPFree0 + (jp & 1)), (jp >> 1) & 1, a.dev_err));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const float alpha = ptx::ex2(m_used - m_new);
+            l *= alpha;
+            const uint32_t to = tmem + lane_off + C::tmem_o(oidx);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t o[32];
+              ptx::tmem_ld32(to + 32 * k, o);
+              ptx::tmem_ld_wait(o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              ptx::tmem_st32(to + 32 * k, o);
+            }
+            ptx::tmem_st_wait();
+          }
+          m_used = m_new;
+        }
+        // a thread whose columns have all been masked so far (possible with split columns:
+        // the tail tile's 2B keys, or a ragged last tile) keeps p = 0, l = 0
+        const float msafe = m_used == -INFINITY ? 0.f : m_used;
+        uint32_t pk[NC / 2];
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; c += 2) {
+          const float p0 = ptx::ex2(x[c] - msafe);
+          const float p1 = ptx::ex2(x[c + 1] - msafe);
+          ls0 += p0;
+          ls1 += p1;
+          pk[c >> 1] = pack_bf16(p0, p1);
+        }
+        l += ls0 + ls1;
+        // P buffer `buf` is free once the P V that last read it (tile j - 2) completed
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(sh, bar(kPFree0 + buf), ((j >> 1) & 1) ^ 1, a.dev_err));
+        if (!ok) break;
+        uint8_t* pt = smem + C::kOffP + (rb * 2 + buf) * kPBlock;
+#pragma unroll
+        for (int c = 0; c < NC / 8; ++c)
+          *reinterpret_cast<uint4*>(pt + sw128(lrow, c + col0 / 8)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kPFull0 + buf));
+      }
+      if (!ok) break;
+      // ---- epilogue: wait for the last P V, then O / l (or the partial)
+      const uint32_t jl = j - 1;
+      ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kPFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      // combine the two column halves (split mode): exchange (max, sum) through the tail
+      // K/V area, which no MMA reads any more in this segment and which the next prologue
+      // rewrites only after its first softmax-wide barrier
+      float wA = 1.f, wB = 0.f, m_all = m_used, l_all = l;
+      int dcol0 = 0, ncols = kD;
+      if constexpr (C::kSplitCols) {
+        float2* xch = reinterpret_cast<float2*>(smem + C::kOffTail);
+        xch[wg * kBlockRows + lrow] = make_float2(m_used, l);
+        ptx::named_bar_sync(1, C::kSoftmaxThreads);
+        const float2 mlA = xch[lrow], mlB = xch[kBlockRows + lrow];
+        m_all = fmaxf(mlA.x, mlB.x);  // finite: every row sees at least B keys
+        wA = mlA.x == -INFINITY ? 0.f : ptx::ex2(mlA.x - m_all);
+        wB = mlB.x == -INFINITY ? 0.f : ptx::ex2(mlB.x - m_all);
+        l_all = wA * mlA.y + wB * mlB.y;
+        dcol0 = 64 * wg;
+        ncols = 64;
+      }
+      const uint32_t toA = tmem + lane_off + C::tmem_o(C::kSplitCols ? 0 : oidx);
+      const uint32_t toB = tmem + lane_off + C::tmem_o(1);
+      const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
+      const float inv = it.full ? 1.f / l_all : 1.f;
+      for (int k = 0; k < ncols / 32; ++k) {
+        const int dc = dcol0 + 32 * k;
+        uint32_t o[32];
+        ptx::tmem_ld32(toA + dc, o);
+        ptx::tmem_ld_wait(o);
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * wA;
+        if constexpr (C::kSplitCols) {
+          uint32_t o2[32];
+          ptx::tmem_ld32(toB + dc, o2);
+          ptx::tmem_ld_wait(o2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = fmaf(__uint_as_float(o2[e]), wB, f[e]);
+        }
+        if (!real) continue;
+        if (it.full) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + dc);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pack_bf16(f[8 * c] * inv, f[8 * c + 1] * inv),
+                                pack_bf16(f[8 * c + 2] * inv, f[8 * c + 3] * inv),
+                                pack_bf16(f[8 * c + 4] * inv, f[8 * c + 5] * inv),
+                                pack_bf16(f[8 * c + 6] * inv, f[8 * c + 7] * inv));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(
+              a.ws_o + ((size_t)slot * (NRB * kBlockRows) + row) * kD + dc);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+        }
+      }
+      if (real && q_writer) {
+        if (it.full) {
+          if (a.lse) a.lse[orow] = (m_all + __log2f(l_all)) * 0.69314718055994530942f;
+        } else {
+          a.ws_ml[(size_t)slot * (NRB * kBlockRows) + row] = make_float2(m_all, l_all);
+        }
+      }
+      ptx::tc_fence_before();
+      it.advance(a);
+    }
+    if (tid == 0) a.ws_desc[blockIdx.x] = desc;
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == C::kMmaWarp) ptx::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// =========================================================================================
+// Pairs of up to 128 query rows (2B*G <= 128): 128-key prompt tiles, and every operand that
+// an MMA reads as A lives in TMEM, which lets each tcgen05.mma run at full rate (an A
+// operand from shared memory, or N < 128, caps an M = 128 instruction well below it):
+//   S_j = Q K_j^T   A = rotated Q (TMEM), B = K tile (smem, K-major), N = 128 keys
+//   O  += P_j V_j   A = P_j (TMEM, bf16),  B = V tile (smem, MN-major), N = 128 = D
+// TMEM columns: S buffers [0,128) and [128,256), O [256,384), Q [384,448), P [448,512).
+// Warps 0-3: softmax (thread = row = TMEM lane; warps whose 32 rows are all padding skip
+// their work), warp 4: TMA producer, warp 5: MMA issuer (non-blocking event loop).
+namespace r128 {
+constexpr int kKeys = 128;                       // prompt keys per tile
+constexpr uint32_t kHalf = kKeys * 128;          // 16 KB: one 64-element half of a K or V tile
+constexpr uint32_t kKV = 2 * kHalf;              // 32 KB
+constexpr uint32_t kStage = 2 * kKV;             // 64 KB: K + V
+constexpr int kStages = 3;
+constexpr int kAhead = kStages - 1;              // S runs up to 2 tiles ahead of P V
+constexpr uint32_t kTailHalf = 64 * 128;         // tail tile: 2B <= 64 keys, 64-key layout
+constexpr uint32_t kTailKV = 2 * kTailHalf;      // 16 KB
+constexpr uint32_t kOffStages = 0;
+constexpr uint32_t kOffTail = kOffStages + kStages * kStage;  // tail K (16 KB) then V (16 KB)
+constexpr uint32_t kOffBar = kOffTail + 2 * kTailKV;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemQ = 384, kTmemP = 448, kTmemCols = 512;
+static_assert(kStages <= kMaxStages, "stage barriers");
+}  // namespace r128
+
+__global__ void __launch_bounds__(r128::kThreads, 1)
+    attn_tc128_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ TcArgs a) {
+  using namespace r128;
+  static_assert(sizeof(Shared) <= 256, "barrier area");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = ptx::smem_u32(smem);
+  auto bar = [&](int i) { return ptx::smem_u32(&sh->bars[i]); };
+  // single-buffer P: kPFull0 = P_j written, kPFree0 = P_j V_j completed
+  const uint32_t bar_pfull = ptx::smem_u32(&sh->bars[kPFull0]);
+  const uint32_t bar_pvdone = ptx::smem_u32(&sh->bars[kPFree0]);
+
+  if (warp == kProducerWarp) {
+    const SchedStart s = warp_schedule(a, blockIdx.x, a.ctas, lane);
+    if (lane == 0) {
+      sh->T = s.T;
+      sh->t0 = s.t0;
+      sh->t1 = s.t1;
+      sh->Tb = s.Tb;
+      sh->b = s.b;
+      sh->abort = 0;
+      for (int i = 0; i < kStages; ++i) {
+        ptx::mbar_init(bar(kFull0 + i), 1);
+        ptx::mbar_init(bar(kEmpty0 + i), 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(bar(kSFull0 + i), 1);
+        ptx::mbar_init(bar(kSFree0 + i), 128);
+      }
+      ptx::mbar_init(bar_pfull, 128);
+      ptx::mbar_init(bar_pvdone, 1);
+      ptx::mbar_init(bar(kQFull), 128);
+      ptx::mbar_init(bar(kDrain), 1);
+      ptx::fence_mbar_init();
+      ptx::prefetch_tensormap(&tmk);
+      ptx::prefetch_tensormap(&tmv);
+    }
+  } else if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  SchedStart st;
+  st.T = sh->T;
+  st.t0 = sh->t0;
+  st.t1 = sh->t1;
+  st.Tb = sh->Tb;
+  st.b = sh->b;
+  const uint32_t tmem = sh->tmem_base;
+  const int twoB = 2 * a.B;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      PromptTiles tiles;
+      tiles.init(a, st);
+      uint32_t m = 0;
+      bool ok = true;
+      int h, tok;
+      while (tiles.next(a, h, tok)) {
+        const int s = m % kStages;
+        ok = wait_bar(sh, bar(kEmpty0 + s), ((m / kStages) & 1) ^ 1, a.dev_err);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
+        const uint32_t kdst = sbase + kOffStages + s * kStage;
+        const uint32_t vdst = kdst + kKV;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (a.layout == SIMSD_CACHE_NHD) {
+            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
+          } else {
+            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
+          }
+        }
+        ++m;
+      }
+      if (!ok) {  // let the loads already issued land before shared memory goes away
+        for (uint32_t k = m > (uint32_t)kStages ? m - kStages : 0; k < m; ++k) {
+          const uint64_t t_start = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(bar(kFull0 + k % kStages), (k / kStages) & 1) &&
+                 ptx::globaltimer_ns() - t_start < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::idesc_bf16(128, kKeys, 0, 0);
+      constexpr uint32_t idS_tail = ptx::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idPV = ptx::idesc_bf16(128, kD, 0, 1);
+      SegIter it;
+      it.init(a, st);
+      uint32_t j = 0, m = 0, nseg = 0;
+      bool ok = true;
+      int stage_of[8];  // per tile (ring): stage to release after its P V, -1 = tail tile
+      static_assert(kAhead + 1 <= 8, "tile ring");
+      auto try_issue_s = [&](uint32_t jj, int i) -> bool {
+        const int buf = jj & 1;
+        const int s = m % kStages;
+        if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / kStages) & 1)) return false;
+        if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj >> 1) & 1) ^ 1)) return false;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + kTmemS0 + buf * 128;
+        if (i == 0) {
+          const uint32_t kaddr = sbase + kOffTail;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            ptx::mma_f16_ts(d, tmem + kTmemQ + kk * 8,
+                            ptx::sdesc_sw128(kaddr + (kk >> 2) * kTailHalf + (kk & 3) * 32, 16, 1024),
+                            idS_tail, kk > 0 ? 1u : 0u);
+          stage_of[jj & 7] = -1;
+        } else {
+          const uint32_t kaddr = sbase + kOffStages + s * kStage;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            ptx::mma_f16_ts(d, tmem + kTmemQ + kk * 8,
+                            ptx::sdesc_sw128(kaddr + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+                            idS, kk > 0 ? 1u : 0u);
+          stage_of[jj & 7] = s;
+          ++m;
+        }
+        ptx::mma_commit(bar(kSFull0 + buf));
+        return true;
+      };
+      auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
+        if (!ptx::mbar_test(bar_pfull, jj & 1)) return false;
+        ptx::tc_fence_after();
+        const int s = stage_of[jj & 7];
+        const uint32_t vaddr = s < 0 ? sbase + kOffTail + kTailKV : sbase + kOffStages + s * kStage + kKV;
+        const uint32_t lbo = s < 0 ? kTailHalf : kHalf;
+        const int nk = s < 0 ? 4 : kKeys / 16;
+        for (int kk = 0; kk < nk; ++kk)
+          ptx::mma_f16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                          ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV,
+                          (first_in_seg && kk == 0) ? 0u : 1u);
+        ptx::mma_commit(bar_pvdone);
+        if (s >= 0) ptx::mma_commit(bar(kEmpty0 + s));
+        return true;
+      };
+      while (ok && it.next(a)) {
+        if (it.invalid) {
+          it.advance(a);
+          continue;
+        }
+        ok = wait_bar(sh, bar(kQFull), nseg & 1, a.dev_err);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t jfirst = j, jend = j + (uint32_t)it.n;
+        uint32_t ns = jfirst, npv = jfirst, spins = 0;
+        uint64_t t_idle = 0;
+        while (npv < jend) {
+          bool progressed = false;
+          if (npv < ns && try_issue_pv(npv, npv == jfirst)) {
+            ++npv;
+            progressed = true;
+          }
+          if (ns < jend && ns <= npv + kAhead && try_issue_s(ns, it.i0 + (int)(ns - jfirst))) {
+            ++ns;
+            progressed = true;
+          }
+          if (progressed) {
+            spins = 0;
+            continue;
+          }
+          if ((++spins & 63) == 0) {  // bounded: give up after kWaitLimitNs without progress
+            const uint64_t now = ptx::globaltimer_ns();
+            if (spins == 64) t_idle = now;
+            if (*(volatile int*)&sh->abort || now - t_idle > kWaitLimitNs) {
+              if (!*(volatile int*)&sh->abort) {
+                *(volatile int*)&sh->abort = 1;
+                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
+              }
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) break;
+        j = jend;
+        ++nseg;
+        it.advance(a);
+      }
+      ptx::mma_commit(bar(kDrain));
+      const uint64_t t_start = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar(kDrain), 0) && ptx::globaltimer_ns() - t_start < 100000000ull) {
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax warps
+    const int row = warp * 32 + lane;  // TMEM lane = row within the pair
+    const bool real = row < a.R;
+    const bool warp_active = warp * 32 < a.R;  // warp-uniform: some row of this warp is real
+    const int s_slot = real ? row / a.G : 0;
+    const int g = real ? row % a.G : 0;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint8_t* tailk = smem + kOffTail;
+    uint8_t* tailv = tailk + kTailKV;
+    // (cos, sin) table of the 2B response positions lives in the tail V area during the
+    // prologue when it fits (2B * 64 * 8 bytes <= 16 KB), else each thread evaluates its own
+    const bool use_table = twoB * 64 * 8 <= (int)kTailKV;
+    SegIter it;
+    it.init(a, st);
+    uint32_t j = 0;
+    bool ok = true;
+    MergeDesc desc;
+    desc.b = -1;
+    desc.T = st.T;
+    while (ok && it.next(a)) {
+      const int b = it.b, h = it.h;
+      if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
+        const int64_t pe = it.t + it.nt;
+        desc.b = b;
+        desc.h = h;
+        desc.c_last = (int)((pe * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
+        desc.slot0 = 2 * blockIdx.x + (it.first ? 0 : 1);
+      }
       const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
       if (it.invalid) {
         if (real) {
@@ -486,36 +1144,85 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
         continue;
       }
       const int P = a.prompt_len[b];
-      // ---- segment prologue: rotated Q rows (and the response tail tile)
-      {
-        uint4 v[16];
+      const int* pos = a.pos_ids + (size_t)b * twoB;
+      // ---- prologue: rotation table, rotated + scaled Q rows into TMEM, tail K/V tiles
+      float2* rtab = reinterpret_cast<float2*>(tailv);
+      if (use_table) {
+        for (int e = tid; e < twoB * 64; e += 128) {
+          const int sidx = e >> 6, d = e & 63;
+          float sn, cs;
+          rope_sincos(pos[sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
+          rtab[e] = make_float2(cs, sn);
+        }
+      }
+      ptx::named_bar_sync(1, 128);
+      uint4 v[16];
+      if (warp_active) {
         if (real) {
           load_row(v, a.q + orow * kD);
-          rope_row(v, a.pos_ids[(size_t)b * twoB + s_slot], a.rope);
+          if (use_table) {
+            rope_row(v, rtab + s_slot * 64, a.scale_log2);
+          } else {
+            float2 cs[64];
+#pragma unroll
+            for (int d = 0; d < 64; ++d) rope_sincos(pos[s_slot], a.rope.c_hi[d], a.rope.c_lo[d], &cs[d].y, &cs[d].x);
+            rope_row(v, cs, a.scale_log2);
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
-        store_row_sw(qtile, kBlockRows * 128, lrow, v);
-        if (it.has_tail && rb == 0) {
-          const int key = lrow & 63;
-          const bool is_v = lrow >= 64;
-          if (key < twoB) {
-            const size_t krow = (((size_t)b * twoB + key) * a.Hkv + h) * kD;
-            load_row(v, (is_v ? a.v_resp : a.k_resp) + krow);
-            if (!is_v) rope_row(v, a.pos_ids[(size_t)b * twoB + key], a.rope);
-          } else {
+        // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
+        uint32_t w[32];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            w[4 * c] = v[8 * half + c].x;
+            w[4 * c + 1] = v[8 * half + c].y;
+            w[4 * c + 2] = v[8 * half + c].z;
+            w[4 * c + 3] = v[8 * half + c].w;
           }
-          store_row_sw(is_v ? tailv : tailk, kHalfTile, key, v);
+          ptx::tmem_st32(tmem + lane_off + kTmemQ + 32 * half, w);
         }
+        ptx::tmem_st_wait();
+      }
+      const bool has_tail = it.has_tail;
+      const int key = tid & 63;
+      if (has_tail && tid < 64) {  // tail K rows (rotated) into the 64-key K layout
+        if (key < twoB) {
+          const size_t krow = (((size_t)b * twoB + key) * a.Hkv + h) * kD;
+          load_row(v, a.k_resp + krow);
+          if (use_table) {
+            rope_row(v, rtab + key * 64, 1.f);
+          } else {
+            float2 cs[64];
+#pragma unroll
+            for (int d = 0; d < 64; ++d) rope_sincos(pos[key], a.rope.c_hi[d], a.rope.c_lo[d], &cs[d].y, &cs[d].x);
+            rope_row(v, cs, 1.f);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+        }
+        store_row_sw(tailk, kTailHalf, key, v);
+      }
+      ptx::named_bar_sync(1, 128);  // every table read is done: the V tail may overwrite it
+      if (has_tail && tid >= 64) {
+        if (key < twoB) {
+          load_row(v, a.v_resp + (((size_t)b * twoB + key) * a.Hkv + h) * kD);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+        }
+        store_row_sw(tailv, kTailHalf, key, v);
       }
       ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kQFull));
-      // visibility of the 2B response keys for this row (bit j = key j visible)
+      // visibility of the 2B response keys for this row (bit k = key k visible)
       uint64_t vis = 0;
-      if (it.has_tail) {
+      if (has_tail) {
         const uint8_t* lab = a.labels + (size_t)b * twoB;
         if (real) {
           const int t = row_threshold(lab[s_slot]);
@@ -531,46 +1238,80 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
         const int buf = j & 1;
         ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
         if (!ok) break;
-        ptx::tc_fence_after();
-        uint32_t sa[32], sb[32];
-        const uint32_t ts = tmem + lane_off + C::tmem_s(rb, buf);
-        ptx::tmem_ld32(ts, sa);
-        ptx::tmem_ld32(ts + 32, sb);
-        ptx::tmem_ld_wait(sa);
-        ptx::tmem_ld_wait(sb);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kSFree0 + buf));
-        float x[64];
-        if (i == 0) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * a.scale_log2;
-            x[c] = ((vis >> c) & 1ull) ? sv : -INFINITY;
+        if (!warp_active) {  // padding rows only: keep the barriers' counts, skip the work
+          ptx::mbar_arrive(bar(kSFree0 + buf));
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, (j - 1) & 1, a.dev_err));
+            if (!ok) break;
           }
-        } else {
-          const int nvalid = P - (i - 1) * kTileKeys;
+          ptx::mbar_arrive(bar_pfull);
+          continue;
+        }
+        ptx::tc_fence_after();
+        const int ncols = (i == 0) ? 64 : kKeys;  // warp-uniform
+        float x[kKeys];
+        {
+          const uint32_t ts = tmem + lane_off + kTmemS0 + buf * 128;
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld32(ts, r0);
+          ptx::tmem_ld32(ts + 32, r1);
+          ptx::tmem_ld_wait(r0);
+          ptx::tmem_ld_wait(r1);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]) * a.scale_log2;
-            x[c] = c < nvalid ? sv : -INFINITY;
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(r0[c]);
+            x[c + 32] = __uint_as_float(r1[c]);
+          }
+          if (ncols == kKeys) {
+            ptx::tmem_ld32(ts + 64, r0);
+            ptx::tmem_ld32(ts + 96, r1);
+            ptx::tmem_ld_wait(r0);
+            ptx::tmem_ld_wait(r1);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              x[c + 64] = __uint_as_float(r0[c]);
+              x[c + 96] = __uint_as_float(r1[c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 64; c < kKeys; ++c) x[c] = -INFINITY;
           }
         }
-        float mt = x[0];
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kSFree0 + buf));
+        if (i == 0) {
 #pragma unroll
-        for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
-        // lazy rescale: only when some row's max grew by more than 2^8; warp-uniform because
-        // TMEM loads/stores are warp-collective
+          for (int c = 0; c < 64; ++c) x[c] = ((vis >> c) & 1ull) ? x[c] : -INFINITY;
+        } else {
+          const int nvalid = P - (i - 1) * kKeys;
+          if (nvalid < kKeys) {
+#pragma unroll
+            for (int c = 0; c < kKeys; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
+          }
+        }
+        float mt;
+        {
+          float mx[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = x[u];
+#pragma unroll
+          for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+          mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        }
+        // P_{j-1} V_{j-1} must have completed before O is rescaled or P is overwritten
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, (j - 1) & 1, a.dev_err));
+          if (!ok) break;
+          ptx::tc_fence_after();
+        }
+        // lazy rescale (warp-uniform: TMEM accesses are warp-collective)
         if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
           const float m_new = fmaxf(m_used, mt);
-          if (j != jfirst) {  // rescale O: the previous P V must have landed
-            const uint32_t jp = j - 1;
-            ok = __all_sync(0xffffffffu,
-                            wait_bar(sh, bar(kPFree0 + (jp & 1)), (jp >> 1) & 1, a.dev_err));
-            if (!ok) break;
-            ptx::tc_fence_after();
+          if (j != jfirst) {
             const float alpha = ptx::ex2(m_used - m_new);
             l *= alpha;
-            const uint32_t to = tmem + lane_off + C::tmem_o(rb);
+            const uint32_t to = tmem + lane_off + kTmemO;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               uint32_t o[32];
@@ -580,48 +1321,51 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
               ptx::tmem_st32(to + 32 * k, o);
             }
-            ptx::tmem_st_wait();
           }
           m_used = m_new;
         }
-        uint32_t pk[32];
-        float lsum = 0.f;
+        const float msafe = m_used == -INFINITY ? 0.f : m_used;
+        uint32_t pk[kKeys / 2];
+        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ptx::ex2(x[c] - m_used);
-          const float p1 = ptx::ex2(x[c + 1] - m_used);
-          lsum += p0 + p1;
+        for (int c = 0; c < kKeys; c += 2) {
+          const float p0 = ptx::ex2(x[c] - msafe);
+          const float p1 = ptx::ex2(x[c + 1] - msafe);
+          ls0 += p0;
+          ls1 += p1;
           pk[c >> 1] = pack_bf16(p0, p1);
         }
-        l += lsum;
-        // P buffer `buf` is free once the P V that last read it (tile j - 2) completed
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(sh, bar(kPFree0 + buf), ((j >> 1) & 1) ^ 1, a.dev_err));
-        if (!ok) break;
-        uint8_t* pt = smem + C::kOffP + (rb * 2 + buf) * kPBlock;
+        l += ls0 + ls1;
+        {
+          uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(pt + sw128(lrow, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        ptx::fence_proxy_async_smem();
+          for (int c = 0; c < 32; ++c) w[c] = pk[c];
+          ptx::tmem_st32(tmem + lane_off + kTmemP, w);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) w[c] = pk[32 + c];
+          ptx::tmem_st32(tmem + lane_off + kTmemP + 32, w);
+        }
+        ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kPFull0 + buf));
+        ptx::mbar_arrive(bar_pfull);
       }
       if (!ok) break;
       // ---- epilogue: wait for the last P V, then O / l (or the partial)
       const uint32_t jl = j - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kPFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err));
+      ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, jl & 1, a.dev_err));
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t to = tmem + lane_off + C::tmem_o(rb);
-      if (it.full) {
-        const float inv = 1.f / l;
+      if (warp_active) {
+        const uint32_t to = tmem + lane_off + kTmemO;
+        const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
+        const float inv = it.full ? 1.f / l : 1.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t o[32];
           ptx::tmem_ld32(to + 32 * k, o);
           ptx::tmem_ld_wait(o);
-          if (real) {
+          if (!real) continue;
+          if (it.full) {
             uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + 32 * k);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -629,120 +1373,79 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
                                   pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
                                   pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
                                   pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
-          }
-        }
-        if (real && a.lse) a.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994530942f;
-      } else {
-        const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
-        float* wo = a.ws_o + ((size_t)slot * (NRB * kBlockRows) + row) * kD;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t o[32];
-          ptx::tmem_ld32(to + 32 * k, o);
-          ptx::tmem_ld_wait(o);
-          if (real) {
-            float4* dst = reinterpret_cast<float4*>(wo + 32 * k);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + ((size_t)slot * kBlockRows + row) * kD + 32 * k);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
                                    __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
           }
         }
-        if (real) a.ws_ml[(size_t)slot * (NRB * kBlockRows) + row] = make_float2(m_used, l);
+        if (real) {
+          if (it.full) {
+            if (a.lse) a.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994530942f;
+          } else {
+            a.ws_ml[(size_t)slot * kBlockRows + row] = make_float2(m_used, l);
+          }
+        }
       }
       ptx::tc_fence_before();
       it.advance(a);
     }
+    if (tid == 0) a.ws_desc[blockIdx.x] = desc;
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == C::kMmaWarp) ptx::tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merges the partial segments of every pair that was split between CTAs. Block c handles
-// the pair containing the last tile of CTA c's range when that pair started inside CTA c's
-// range and continues past it (so every split pair is merged exactly once).
+// Merges the pieces of every pair split between CTAs. Block (c, y) reads CTA c's merge
+// descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that pair:
+// one thread per (row, 4 output elements), so every load is independent.
 template <int NRB>
-__global__ void __launch_bounds__(128) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
-  __shared__ SchedStart s_end;
-  __shared__ int64_t s_pair_start, s_pair_end;
-  __shared__ int s_b, s_h, s_go;
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
   const int c = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0) {
-    // locate the tile t1(c) - 1 with the same scan the attention kernel uses
-    SchedStart s = warp_schedule(a, c + 1, a.ctas, lane);  // s.t0 = t1(c)
-    const int64_t T = s.T;
-    const int64_t t0c = cta_begin(T, a.ctas, c);
-    const int64_t t1c = s.t0;
-    int go = 0;
-    if (lane == 0 && t1c > t0c && t1c < T) {
-      // request containing tile t1c - 1: rescan from s (which contains tile t1c)
-      int b = s.b;
-      int64_t Tb = s.Tb;
-      const int64_t last = t1c - 1;
-      while (last < Tb) {  // step back one request at a time (rarely more than one)
-        --b;
-        Tb -= (int64_t)a.Hkv * tiles_per_pair(a, b);
-      }
-      const int nt = tiles_per_pair(a, b);
-      const int q = (int)((last - Tb) / nt);
-      const int64_t ps = Tb + (int64_t)q * nt, pe = ps + nt;
-      if (pe > t1c && ps >= t0c) {
-        go = 1;
-        s_pair_start = ps;
-        s_pair_end = pe;
-        s_b = b;
-        s_h = q;
-      }
-      s_end.T = T;
-    }
-    go = __shfl_sync(0xffffffffu, go, 0);
-    if (lane == 0) s_go = go;
-  }
-  __syncthreads();
-  if (!s_go) return;
-  const int64_t T = s_end.T;
-  const int64_t ps = s_pair_start, pe = s_pair_end;
-  const int b = s_b, h = s_h;
+  const MergeDesc d = a.ws_desc[c];
+  if (d.b < 0) return;
+  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int quad = threadIdx.x & 31;
+  if (row >= a.R) return;
+  const int64_t T = d.T;
   const int C = a.ctas;
-  // CTAs covering [ps, pe): c .. cta_of(pe - 1)
-  const int c_last = (int)(((pe - 1 + 1) * (int64_t)C + T - 1) / T) - 1;
-  const int twoB = 2 * a.B;
-  const int rows = a.R;
-  for (int row = warp; row < rows; row += 4) {
-    float mmax = -INFINITY;
-    for (int cc = c; cc <= c_last; ++cc) {
-      if (cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;  // empty range: no partial
-      const int slot = 2 * cc + ((cc == c && cta_begin(T, C, cc) < ps) ? 1 : 0);
-      mmax = fmaxf(mmax, a.ws_ml[(size_t)slot * (NRB * kBlockRows) + row].x);
-    }
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cc = c; cc <= c_last; ++cc) {
-      if (cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;
-      const int slot = 2 * cc + ((cc == c && cta_begin(T, C, cc) < ps) ? 1 : 0);
-      const float2 ml = a.ws_ml[(size_t)slot * (NRB * kBlockRows) + row];
-      const float w = exp2f(ml.x - mmax);
-      L += w * ml.y;
-      const float4 o = reinterpret_cast<const float4*>(
-          a.ws_o + ((size_t)slot * (NRB * kBlockRows) + row) * kD)[lane];
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
-    }
-    const float inv = 1.f / L;
-    const int s_slot = row / a.G, g = row % a.G;
-    const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
-    uint2 pk;
-    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(a.out + orow * kD)[lane] = pk;
-    if (lane == 0 && a.lse) a.lse[orow] = (mmax + log2f(L)) * 0.69314718055994530942f;
+  const size_t stride = (size_t)NRB * kBlockRows;
+  // pieces: CTA c (slot0) and every later non-empty CTA up to c_last (its first slot)
+  float mmax = -INFINITY;
+#pragma unroll 4
+  for (int cc = c; cc <= d.c_last; ++cc) {
+    if (cc > c && cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;
+    const int slot = (cc == c) ? d.slot0 : 2 * cc;
+    mmax = fmaxf(mmax, a.ws_ml[(size_t)slot * stride + row].x);
   }
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int cc = c; cc <= d.c_last; ++cc) {
+    if (cc > c && cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;
+    const int slot = (cc == c) ? d.slot0 : 2 * cc;
+    const float2 ml = a.ws_ml[(size_t)slot * stride + row];
+    const float4 o = reinterpret_cast<const float4*>(a.ws_o + ((size_t)slot * stride + row) * kD)[quad];
+    const float w = exp2f(ml.x - mmax);
+    L += w * ml.y;
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = 1.f / L;
+  const int s_slot = row / a.G, g = row % a.G;
+  const size_t orow = ((size_t)d.b * 2 * a.B + s_slot) * a.Hq + (size_t)d.h * a.G + g;
+  uint2 pk;
+  pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(a.out + orow * kD)[quad] = pk;
+  if (quad == 0 && a.lse) a.lse[orow] = (mmax + log2f(L)) * 0.69314718055994530942f;
 }
 
 // ------------------------------------------------------------------------------- host
@@ -761,7 +1464,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 static bool encode_cache_map(CUtensorMap* map, const void* base, int layout, int64_t tokens,
-                             int Hkv) {
+                             int Hkv, int box_keys) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3];
@@ -776,7 +1479,7 @@ static bool encode_cache_map(CUtensorMap* map, const void* base, int layout, int
     strides[1] = (cuuint64_t)Hkv * kD * 2;
     box[0] = 64;
     box[1] = 1;
-    box[2] = kTileKeys;
+    box[2] = (cuuint32_t)box_keys;
   } else {  // [Hkv][tokens][D]: dims (D, tokens, Hkv)
     dims[0] = kD;
     dims[1] = (cuuint64_t)(tokens > 0 ? tokens : 1);
@@ -784,7 +1487,7 @@ static bool encode_cache_map(CUtensorMap* map, const void* base, int layout, int
     strides[0] = (cuuint64_t)kD * 2;
     strides[1] = (cuuint64_t)(tokens > 0 ? tokens : 1) * kD * 2;
     box[0] = 64;
-    box[1] = kTileKeys;
+    box[1] = (cuuint32_t)box_keys;
     box[2] = 1;
   }
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
@@ -796,9 +1499,27 @@ static bool encode_cache_map(CUtensorMap* map, const void* base, int layout, int
 
 static int rows_per_pair(const simsd_attn_params* p) { return 2 * p->B * (p->Hq / p->Hkv); }
 
+// Persistent grid: one CTA per SM; when every (request, kv head) pair fits on the SMs and
+// prompts are short, one CTA per pair instead (no pair is split, nothing to merge).
 static int grid_ctas(const simsd_attn_params* p) {
-  const int sms = device_sm_count();
-  return sms > 0 ? sms : 148;
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  const int64_t pairs = (int64_t)p->batch * p->Hkv;
+  const int64_t avg_tiles = 1 + (p->batch > 0 ? (p->cache_tokens / p->batch + kTileKeys - 1) / kTileKeys : 0);
+  if (pairs > 0 && pairs <= sms && avg_tiles <= 64) return (int)pairs;
+  return sms;
+}
+
+struct WsLayout {
+  size_t o, ml, desc, bytes;
+};
+static WsLayout ws_layout(int ctas, int nrb) {
+  WsLayout w;
+  w.o = 0;
+  w.ml = align_up(w.o + (size_t)2 * ctas * nrb * kBlockRows * kD * sizeof(float), 256);
+  w.desc = align_up(w.ml + (size_t)2 * ctas * nrb * kBlockRows * sizeof(float2), 256);
+  w.bytes = align_up(w.desc + (size_t)ctas * sizeof(MergeDesc), 256);
+  return w;
 }
 
 template <int NRB>
@@ -812,6 +1533,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.G = p->Hq / p->Hkv;
   a.R = rows_per_pair(p);
   a.nrb = NRB;
+  a.tile_keys = NRB == 1 ? r128::kKeys : kTileKeys;
   a.ctas = grid_ctas(p);
   a.layout = (int)p->cache_layout;
   a.q = (const __nv_bfloat16*)p->q;
@@ -826,33 +1548,57 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.out = (__nv_bfloat16*)p->out;
   a.lse = p->lse;
   a.dev_err = p->dev_err;
-  const size_t o_bytes = align_up((size_t)2 * a.ctas * NRB * kBlockRows * kD * sizeof(float), 256);
-  const size_t ml_bytes = align_up((size_t)2 * a.ctas * NRB * kBlockRows * sizeof(float2), 256);
-  if (!ws || ws_bytes < o_bytes + ml_bytes || (((uintptr_t)ws) & 255)) return SIMSD_ERR_WORKSPACE;
-  a.ws_o = (float*)ws;
-  a.ws_ml = (float2*)((char*)ws + o_bytes);
+  const WsLayout wl = ws_layout(a.ctas, NRB);
+  if (!ws || ws_bytes < wl.bytes || (((uintptr_t)ws) & 255)) return SIMSD_ERR_WORKSPACE;
+  a.ws_o = (float*)((char*)ws + wl.o);
+  a.ws_ml = (float2*)((char*)ws + wl.ml);
+  a.ws_desc = (MergeDesc*)((char*)ws + wl.desc);
   make_rope_table(&a.rope, (double)p->rope_theta, kD);
 
   CUtensorMap tmk, tmv;
   const void* kbase = p->cache_tokens > 0 ? p->k_cache : p->k_resp;  // any valid address
   const void* vbase = p->cache_tokens > 0 ? p->v_cache : p->v_resp;
-  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv) ||
-      !encode_cache_map(&tmv, vbase, a.layout, p->cache_tokens, p->Hkv))
+  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv, a.tile_keys) ||
+      !encode_cache_map(&tmv, vbase, a.layout, p->cache_tokens, p->Hkv, a.tile_keys)) {
+    record_cuda_error("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     return SIMSD_ERR_CUDA;
+  }
 
+  // pairs of <= 128 rows: the all-TMEM 128-key kernel; 129..256 rows: two row blocks
+  const void* kfn = NRB == 1 ? (const void*)attn_tc128_kernel : (const void*)attn_tc_kernel<NRB>;
+  const int threads = NRB == 1 ? r128::kThreads : C::kThreads;
+  const uint32_t smem_bytes = NRB == 1 ? r128::kSmemBytes : C::kSmemBytes;
   static int attr_done[64][3];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev][NRB]) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<NRB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes) != cudaSuccess)
+    const cudaError_t e =
+        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) {
+      record_cuda_error("cudaFuncSetAttribute", e);
       return SIMSD_ERR_CUDA;
+    }
     attr_done[dev][NRB] = 1;
   }
-  attn_tc_kernel<NRB><<<a.ctas, C::kThreads, C::kSmemBytes, stream>>>(tmk, tmv, a);
-  simsd_status st = last_launch_status();
-  if (st != SIMSD_OK) return st;
-  attn_tc_merge_kernel<NRB><<<a.ctas, 128, 0, stream>>>(a);
+  if (NRB == 1)
+    attn_tc128_kernel<<<a.ctas, threads, smem_bytes, stream>>>(tmk, tmv, a);
+  else
+    attn_tc_kernel<NRB><<<a.ctas, threads, smem_bytes, stream>>>(tmk, tmv, a);
+  const cudaError_t le = cudaGetLastError();
+  if (le != cudaSuccess) {
+    cudaFuncAttributes fa;
+    char what[200] = "attention kernel launch";
+    if (cudaFuncGetAttributes(&fa, kfn) == cudaSuccess)
+      snprintf(what, sizeof(what),
+               "attention kernel launch (threads %d, regs %d, max threads %d, dyn smem %u, "
+               "max dyn smem %d, static smem %zu, local %zu)",
+               threads, fa.numRegs, fa.maxThreadsPerBlock, smem_bytes,
+               fa.maxDynamicSharedSizeBytes, fa.sharedSizeBytes, fa.localSizeBytes);
+    record_cuda_error(what, le);
+    return SIMSD_ERR_CUDA;
+  }
+  const dim3 mgrid(a.ctas, (a.R + 7) / 8);  // blocks without a split pair exit at once
+  attn_tc_merge_kernel<NRB><<<mgrid, 256, 0, stream>>>(a);
   return last_launch_status();
 }
 
@@ -868,9 +1614,7 @@ bool attn_tc_supported(const simsd_attn_params* p) {
 
 size_t attn_tc_workspace(const simsd_attn_params* p) {
   const int nrb = tc::rows_per_pair(p) > 128 ? 2 : 1;
-  const int ctas = tc::grid_ctas(p);
-  return align_up((size_t)2 * ctas * nrb * tc::kBlockRows * tc::kD * sizeof(float), 256) +
-         align_up((size_t)2 * ctas * nrb * tc::kBlockRows * sizeof(float2), 256);
+  return tc::ws_layout(tc::grid_ctas(p), nrb).bytes;
 }
 
 simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_bytes,

@@ -15,8 +15,13 @@ constexpr int kMaxB = 32;          // block size limit (labels hold tau in 7 bit
 constexpr uint8_t kSegMask = 0x80; // label bit: mask slot D~
 constexpr uint8_t kLabelInvalid = 0xFF;
 
+// Records the text of the last CUDA failure seen on this host thread.
+void record_cuda_error(const char* what, cudaError_t e);
+
 static inline simsd_status cuda_status(cudaError_t e) {
-  return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+  if (e == cudaSuccess) return SIMSD_OK;
+  record_cuda_error("", e);
+  return SIMSD_ERR_CUDA;
 }
 
 static inline simsd_status last_launch_status() {

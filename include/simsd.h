@@ -81,6 +81,10 @@ const char* simsd_status_str(simsd_status s);
 /* Library interface version (major * 10000 + minor * 100 + patch). */
 int simsd_version(void);
 
+/* Text of the CUDA runtime/driver error behind the most recent SIMSD_ERR_CUDA returned
+ * on the calling host thread ("" if none). Static/thread-local storage, never NULL. */
+const char* simsd_last_cuda_error(void);
+
 /* ---------------------------------------------------------------------------------
  * simsd_build_layout  [SimSD-1], [SimSD-2], [SimSD-3], [SimSD-P] sections 1-3.
  *
