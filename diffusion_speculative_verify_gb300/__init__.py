@@ -12,6 +12,7 @@ import torch
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
                        DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, LIB_PATH, AttnParams,
                        SimsdError, load_library, make_attn_params, simsd_accept,
+                       simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
                        simsd_accept_workspace, simsd_build_layout, simsd_last_cuda_error, simsd_status_str,
                        simsd_verify_attention, simsd_verify_attention_workspace,
                        simsd_version)

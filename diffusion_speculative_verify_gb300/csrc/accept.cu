@@ -18,6 +18,8 @@
 //                         request's scratch.
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace simsd {
@@ -434,4 +436,68 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
       (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), (uint32_t)(offset & 0xffffffffu),
       (uint32_t)(offset >> 32), plan, ws, accepted_len, out_tokens, out_pos, n_commit, dev_err);
   return last_launch_status();
+}
+
+// ------------------------------------------------------------------------------------
+// Allocation-free variant. Its scratch lives in a fixed device array of this file, so the
+// caller passes only inputs and outputs. Every device that loads the library holds the
+// array (kNoAllocScratchBytes) until the process exits.
+namespace simsd {
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)1 << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices];
+
+// Device address of g_accept_scratch on the current device. Resolved on the first call
+// per device (with that device current) and cached; the host-side symbol itself is not a
+// device address and is never passed to a kernel.
+simsd_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    record_cuda_error("cudaGetDevice", e);
+    return SIMSD_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SIMSD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
+    if (e != cudaSuccess || !ptr) {
+      record_cuda_error("cudaGetSymbolAddress", e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+      return SIMSD_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return SIMSD_OK;
+}
+}  // namespace
+}  // namespace simsd
+
+SIMSD_API size_t simsd_accept_noalloc_max_scratch(void) { return simsd::kNoAllocScratchBytes; }
+
+SIMSD_API simsd_status simsd_accept_noalloc(const float* target_logits, const float* draft_logits,
+                                            const int32_t* draft_tokens, const uint8_t* labels,
+                                            int batch, int B, int gamma, int V, float temperature,
+                                            uint64_t seed, uint64_t offset, int32_t* accepted_len,
+                                            int32_t* out_tokens, int32_t* out_pos,
+                                            int32_t* n_commit, uint32_t* dev_err,
+                                            simsd_stream_t stream) {
+  using namespace simsd;
+  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
+    return SIMSD_ERR_INVALID_ARG;
+  if (batch > 0 && make_plan(batch, gamma, V).bytes > kNoAllocScratchBytes)
+    return SIMSD_ERR_WORKSPACE;  // these sizes need more scratch than the fixed array holds
+  void* scratch = nullptr;
+  if (batch > 0) {
+    const simsd_status st = noalloc_scratch(&scratch);
+    if (st != SIMSD_OK) return st;
+  }
+  return simsd_accept(target_logits, draft_logits, draft_tokens, labels, batch, B, gamma, V,
+                      temperature, seed, offset, accepted_len, out_tokens, out_pos, n_commit,
+                      scratch, kNoAllocScratchBytes, dev_err, stream);
 }

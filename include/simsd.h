@@ -197,6 +197,38 @@ simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
                           int32_t* out_pos, int32_t* n_commit, void* workspace,
                           size_t workspace_bytes, uint32_t* dev_err, simsd_stream_t stream);
 
+/* ---------------------------------------------------------------------------------
+ * simsd_accept_noalloc -- the same operation as simsd_accept, for callers that cannot
+ * allocate device memory. (Library addition: the pages have no counterpart to this call.)
+ *
+ * Some callers have no way to provide scratch memory: plugin hosts that hand the library
+ * only its input and output buffers and expose no allocator, or runtimes that forbid
+ * device allocation once serving has started (an allocation can synchronise the device
+ * and has unbounded latency). This entry point takes no workspace and allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine): its scratch is a fixed
+ * 1 MiB device array inside the library, present on every device that loads the library
+ * until the process exits.
+ *   - Arguments, outputs, error bits and sentinels: exactly as simsd_accept.
+ *   - The first call on each device looks up that array's device address (a runtime
+ *     query, with that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Sizes whose scratch would exceed the array (see simsd_accept_noalloc_max_scratch;
+ *     simsd_accept_workspace(batch, B, gamma, V) must not exceed it) return
+ *     SIMSD_ERR_WORKSPACE and launch nothing.
+ *   - Every call shares the one array: calls that may overlap on the GPU (different
+ *     streams without ordering between them) race and must not be issued; calls ordered
+ *     on one stream are safe. The kernels reset the parts that must start at zero.
+ * --------------------------------------------------------------------------------- */
+simsd_status simsd_accept_noalloc(const float* target_logits, const float* draft_logits,
+                                  const int32_t* draft_tokens, const uint8_t* labels,
+                                  int batch, int B, int gamma, int V, float temperature,
+                                  uint64_t seed, uint64_t offset, int32_t* accepted_len,
+                                  int32_t* out_tokens, int32_t* out_pos, int32_t* n_commit,
+                                  uint32_t* dev_err, simsd_stream_t stream);
+
+/* Size in bytes of the fixed scratch array behind simsd_accept_noalloc. */
+size_t simsd_accept_noalloc_max_scratch(void);
+
 #ifdef __cplusplus
 }
 #endif
