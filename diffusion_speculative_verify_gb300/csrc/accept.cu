@@ -18,6 +18,7 @@
 //                         request's scratch.
 #include <float.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -26,7 +27,7 @@ namespace simsd {
 
 namespace {
 
-constexpr int kStatThreads = 512;
+constexpr int kStatThreads = 256;
 constexpr int kFinishThreads = 256;
 
 struct AcceptWs {
@@ -42,16 +43,12 @@ struct AcceptPlan {
   size_t off_stats, off_winners, off_anypos, off_ticket, bytes;
 };
 
+constexpr int kStatChunk = 2048;  // vocabulary entries per (row, chunk) work item: 8 KB
+
 AcceptPlan make_plan(int batch, int gamma, int V) {
   AcceptPlan p;
-  const long rows = (long)batch * gamma * 2;
-  const long target_ctas = 1216;  // keeps every SM busy several times over
-  long na = rows > 0 ? (target_ctas + rows - 1) / rows : 1;
-  const long max_na = (V + 4095) / 4096;
-  if (na > max_na) na = max_na;
-  if (na < 1) na = 1;
-  p.nchunk_a = (int)na;
-  p.chunk_a = (int)(((V + na - 1) / na + 3) / 4 * 4);
+  p.nchunk_a = (V + kStatChunk - 1) / kStatChunk;
+  p.chunk_a = kStatChunk;
   long nb = batch > 0 ? (608 + batch - 1) / batch : 1;
   const long max_nb = (V + 1023) / 1024;
   if (nb > max_nb) nb = max_nb;
@@ -99,27 +96,27 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   }
 }
 
-// Slot whose data label carries step `step1` (1-based), or -1.
-__device__ __forceinline__ int slot_of_step(const uint8_t* lab, int B, int step1) {
-  for (int k = 0; k < B; ++k)
-    if ((lab[k] & 0x7F) == step1 && !(lab[k] & kSegMask)) return k;
-  return -1;
+// ----------------------------------------------------------------------------- K3a
+// One warp per (row, chunk) work item of kStatChunk vocabulary entries; a persistent grid of
+// warps strides over the items, so there is no block-level synchronisation and every lane
+// keeps kStatChunk / 32 / 4 float4 loads in flight at once. exp is evaluated as
+// 2^((x - m) * log2 e) with the ex2 instruction (about 2 ulp; the acceptance decisions use
+// the accurate exp on single values).
+__device__ __forceinline__ float exp_shifted(float x, float m) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"((x - m) * 1.4426950408889634f));
+  return y;
 }
 
-// ----------------------------------------------------------------------------- K3a
 __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     const float* __restrict__ target, const float* __restrict__ draft,
     const uint8_t* __restrict__ labels, int batch, int B, int gamma, int V, float T,
     AcceptPlan plan, AcceptWs ws) {
+  const int lane = threadIdx.x & 31;
+  const long warp_global = (long)blockIdx.x * (kStatThreads / 32) + (threadIdx.x >> 5);
+  const long nwarps = (long)gridDim.x * (kStatThreads / 32);
   const int nchunk = plan.nchunk_a;
-  int idx = blockIdx.x;
-  const int chunk = idx % nchunk;
-  idx /= nchunk;
-  const int model = idx & 1;
-  idx >>= 1;
-  const int step = idx % gamma;
-  const int r = idx / gamma;
-
+  const long items = (long)batch * gamma * 2 * nchunk;
   if (blockIdx.x == 0) {  // scratch of K3b starts at zero on every call
     for (int i = threadIdx.x; i < batch; i += blockDim.x) {
       ws.winners[2 * i] = 0ull;
@@ -128,85 +125,70 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
       ws.ticket[i] = 0u;
     }
   }
-
-  __shared__ int s_slot;
-  if (threadIdx.x == 0) s_slot = slot_of_step(labels + (size_t)r * 2 * B, B, step + 1);
-  __syncthreads();
-  const int k = s_slot;
-  float m = -INFINITY, s = 0.f;
-  if (k >= 0) {
-    const float* row = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
-    const int c0 = chunk * plan.chunk_a;
-    const int c1 = min(V, c0 + plan.chunk_a);
-    const bool unit_T = (T == 1.f);
-    const bool vec = ((V & 3) == 0) && ((((uintptr_t)row) & 15) == 0);
-    if (vec) {
-      const int n4 = (c1 - c0) >> 2;  // c0 is a multiple of 4; V too
-      const float* base = row + c0;
-      int i = threadIdx.x;
-      for (; i + 3 * kStatThreads < n4; i += 4 * kStatThreads) {
-        float4 x[4];
+  const bool unit_T = (T == 1.f);
+  const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+  constexpr int kPer = kStatChunk / 32 / 4;  // float4 per lane
+  for (long item = warp_global; item < items; item += nwarps) {
+    const int chunk = (int)(item % nchunk);
+    const long row = item / nchunk;
+    const int model = (int)(row & 1);
+    const int step = (int)((row >> 1) % gamma);
+    const int r = (int)((row >> 1) / gamma);
+    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
+    float m = -INFINITY, sum = 0.f;
+    if (hit) {
+      const int k = __ffs(hit) - 1;
+      const float* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
+      const int c0 = chunk * kStatChunk;
+      const int len = min(kStatChunk, V - c0);
+      if (vec_ok) {
+        const float4* src = reinterpret_cast<const float4*>(rowp + c0);
+        const int n4 = len >> 2;
+        float4 x[kPer];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = ld_stream4(base + 4 * (i + u * kStatThreads));
+        for (int u = 0; u < kPer; ++u) {
+          const int i4 = lane + 32 * u;
+          x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
+                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float z0 = scale_logit(x[u].x, T, unit_T), z1 = scale_logit(x[u].y, T, unit_T);
-          const float z2 = scale_logit(x[u].z, T, unit_T), z3 = scale_logit(x[u].w, T, unit_T);
-          const float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
-          if (mx > m) {
-            s *= expf(m - mx);
-            m = mx;
+        for (int u = 0; u < kPer; ++u) {
+          if (!unit_T) {
+            x[u].x = scale_logit(x[u].x, T, false);
+            x[u].y = scale_logit(x[u].y, T, false);
+            x[u].z = scale_logit(x[u].z, T, false);
+            x[u].w = scale_logit(x[u].w, T, false);
           }
-          s += expf(z0 - m) + expf(z1 - m) + expf(z2 - m) + expf(z3 - m);
+          m = fmaxf(m, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
         }
-      }
-      for (; i < n4; i += kStatThreads) {
-        const float4 x = ld_stream4(base + 4 * i);
-        const float z0 = scale_logit(x.x, T, unit_T), z1 = scale_logit(x.y, T, unit_T);
-        const float z2 = scale_logit(x.z, T, unit_T), z3 = scale_logit(x.w, T, unit_T);
-        const float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
-        if (mx > m) {
-          s *= expf(m - mx);
-          m = mx;
+        if (m != -INFINITY) {
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            s0 += exp_shifted(x[u].x, m) + exp_shifted(x[u].y, m);
+            s1 += exp_shifted(x[u].z, m) + exp_shifted(x[u].w, m);
+          }
+          sum = s0 + s1;
         }
-        s += expf(z0 - m) + expf(z1 - m) + expf(z2 - m) + expf(z3 - m);
-      }
-    } else {
-      for (int v = c0 + threadIdx.x; v < c1; v += kStatThreads) {
-        const float z = scale_logit(row[v], T, unit_T);
-        if (z > m) {
-          s *= expf(m - z);
-          m = z;
+      } else {
+        for (int v = lane; v < len; v += 32) {
+          const float z = scale_logit(rowp[c0 + v], T, unit_T);
+          if (z > m) {
+            sum = (m == -INFINITY) ? 0.f : sum * exp_shifted(m, z);
+            m = z;
+          }
+          sum += exp_shifted(z, m);
         }
-        s += expf(z - m);
       }
     }
-  }
-  // block reduction of (m, s)
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
-  }
-  __shared__ float sm[kStatThreads / 32], ss[kStatThreads / 32];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sm[w] = m;
-    ss[w] = s;
-  }
-  __syncthreads();
-  if (w == 0) {
-    m = lane < kStatThreads / 32 ? sm[lane] : -INFINITY;
-    s = lane < kStatThreads / 32 ? ss[lane] : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      lse_merge(m, s, m2, s2);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      lse_merge(m, sum, m2, s2);
     }
-    if (lane == 0)
-      ws.stats[(((size_t)r * gamma + step) * 2 + model) * nchunk + chunk] = make_float2(m, s);
+    if (lane == 0) ws.stats[item] = make_float2(m, sum);  // items enumerate [row][chunk]
   }
 }
 
@@ -237,6 +219,26 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __shared__ int s_order[kMaxB];
   __shared__ int s_a, s_bad;
   __shared__ float s_mt, s_st, s_md, s_sd;
+  __shared__ float2 s_rowstat[2 * kMaxB];  // merged (max, sum exp) per (step, model)
+
+  // merge the chunk partials of every verified (step, model) row: warp w takes rows
+  // w, w + 8, ...; its lanes stride over the chunks
+  for (int row = w; row < 2 * gamma; row += kFinishThreads / 32) {
+    const float2* src = ws.stats + ((size_t)r * gamma * 2 + row) * plan.nchunk_a;
+    float m = -INFINITY, sum = 0.f;
+    for (int c = lane; c < plan.nchunk_a; c += 32) {
+      const float2 v = src[c];
+      lse_merge(m, sum, v.x, v.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      lse_merge(m, sum, m2, s2);
+    }
+    if (lane == 0) s_rowstat[row] = make_float2(m, sum);
+  }
+  __syncthreads();
 
   if (w == 0) {
     // step labels of the data half -> order o_t; validity of the permutation
@@ -262,18 +264,11 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
       bool acc = true;
       float mt = 0.f, st = 0.f, md = 0.f, sd = 0.f;
       if (lane < gamma) {
-        float m1 = -INFINITY, s1 = 0.f, m2 = -INFINITY, s2 = 0.f;
-        const float2* st_t = ws.stats + (((size_t)r * gamma + lane) * 2 + 0) * plan.nchunk_a;
-        const float2* st_d = ws.stats + (((size_t)r * gamma + lane) * 2 + 1) * plan.nchunk_a;
-        for (int c = 0; c < plan.nchunk_a; ++c) {
-          const float2 a2 = st_t[c], b2 = st_d[c];
-          lse_merge(m1, s1, a2.x, a2.y);
-          lse_merge(m2, s2, b2.x, b2.y);
-        }
-        mt = m1;
-        st = s1;
-        md = m2;
-        sd = s2;
+        const float2 rt = s_rowstat[2 * lane], rd = s_rowstat[2 * lane + 1];
+        mt = rt.x;
+        st = rt.y;
+        md = rd.x;
+        sd = rd.y;
         const size_t rowoff = ((size_t)r * B + k) * (size_t)V + x;
         const float px = __fdiv_rn(expf(scale_logit(target[rowoff], T, unit_T) - mt), st);
         const float qx = __fdiv_rn(expf(scale_logit(draft[rowoff], T, unit_T) - md), sd);
@@ -322,8 +317,9 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     const float* drow = draft + ((size_t)r * B + k) * (size_t)V;
     const int c0 = chunk * plan.chunk_b;
     const int c1 = min(V, c0 + plan.chunk_b);
-    unsigned long long best_res = 0ull, best_p = 0ull;
+    unsigned long long best_res = 0ull;
     bool anyp = false;
+    const float inv_st = 1.f / st, inv_sd = 1.f / sd;
     for (int g = c0 / 4 + tid; g * 4 < c1; g += blockDim.x) {
       Philox4 c4 = {(uint32_t)r, off_lo, off_hi, kResampleTag | (uint32_t)g};
       const Philox4 rnd = philox4x32_10(c4, key0, key1);
@@ -331,28 +327,25 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
       for (int j = 0; j < 4; ++j) {
         const int v = 4 * g + j;
         if (v >= c1) break;
-        const float p = __fdiv_rn(expf(scale_logit(trow[v], T, unit_T) - mt), st);
-        const float q = __fdiv_rn(expf(scale_logit(drow[v], T, unit_T) - md), sd);
-        const float res = fmaxf(p - q, 0.f);
-        const float E = -logf(word_to_uniform(philox_word(rnd, j)));
-        anyp |= res > 0.f;
-        const unsigned long long kr = pack_key(__fdiv_rn(res, E), v);
-        const unsigned long long kp = pack_key(__fdiv_rn(p, E), v);
-        best_res = kr > best_res ? kr : best_res;
-        best_p = kp > best_p ? kp : best_p;
+        const float p = expf(scale_logit(trow[v], T, unit_T) - mt) * inv_st;
+        const float q = expf(scale_logit(drow[v], T, unit_T) - md) * inv_sd;
+        const float res = p - q;
+        if (res > 0.f) {
+          anyp = true;
+          const float E = -logf(word_to_uniform(philox_word(rnd, j)));
+          const unsigned long long kr = pack_key(__fdividef(res, E), v);
+          best_res = kr > best_res ? kr : best_res;
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
-      const unsigned long long b2 = __shfl_xor_sync(0xffffffffu, best_p, o);
       best_res = b1 > best_res ? b1 : best_res;
-      best_p = b2 > best_p ? b2 : best_p;
     }
     anyp = __any_sync(0xffffffffu, anyp);
     if (lane == 0) {
       atomicMax(&ws.winners[2 * r], best_res);
-      atomicMax(&ws.winners[2 * r + 1], best_p);
       if (anyp) atomicOr(&ws.any_pos[r], 1u);
     }
   }
@@ -367,6 +360,35 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  __shared__ unsigned long long s_win;
+  if (tid == 0) s_win = atomicAdd(&ws.winners[2 * r], 0ull);
+  __syncthreads();
+  if (a < gamma && atomicAdd(&ws.any_pos[r], 0u) == 0u) {
+    // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
+    // over the whole row, done here by the last CTA (never on typical inputs)
+    const int k = s_order[a];
+    const float* trow = target + ((size_t)r * B + k) * (size_t)V;
+    const float inv_st = 1.f / s_st;
+    unsigned long long best = 0ull;
+    for (int g = tid; g * 4 < V; g += blockDim.x) {
+      Philox4 c4 = {(uint32_t)r, off_lo, off_hi, kResampleTag | (uint32_t)g};
+      const Philox4 rnd = philox4x32_10(c4, key0, key1);
+      for (int j = 0; j < 4 && 4 * g + j < V; ++j) {
+        const int v = 4 * g + j;
+        const float p = expf(scale_logit(trow[v], T, unit_T) - s_mt) * inv_st;
+        const float E = -logf(word_to_uniform(philox_word(rnd, j)));
+        const unsigned long long kp = pack_key(__fdividef(p, E), v);
+        best = kp > best ? kp : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
+      best = b1 > best ? b1 : best;
+    }
+    if (lane == 0) atomicMax(&s_win, best);
+    __syncthreads();
+  }
   if (tid < B) {
     int tok = -1, pos = -1;
     if (tid < a) {
@@ -374,10 +396,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
       tok = tokens[(size_t)r * B + pos];
     } else if (tid == a && a < gamma) {
       pos = s_order[a];
-      const unsigned long long wr = atomicAdd(&ws.winners[2 * r], 0ull);
-      const unsigned long long wp = atomicAdd(&ws.winners[2 * r + 1], 0ull);
-      const unsigned ap = atomicAdd(&ws.any_pos[r], 0u);
-      tok = unpack_token(ap ? wr : wp);
+      tok = unpack_token(s_win);
     }
     out_tokens[(size_t)r * B + tid] = tok;
     out_pos[(size_t)r * B + tid] = pos;
@@ -427,7 +446,22 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   const long grid_b = (long)batch * plan.nchunk_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
-  accept_stats_kernel<<<(unsigned)grid_a, kStatThreads, 0, s>>>(
+  // persistent grid: as many stats CTAs as can be resident at once
+  static int resident[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && resident[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_stats_kernel, kStatThreads, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 2;
+    const int sms = device_sm_count();
+    resident[dev] = per_sm * (sms > 0 ? sms : 148);
+  }
+  const long max_ctas = dev < 64 ? resident[dev] : 296;
+  const long warps_needed = (long)batch * gamma * 2 * plan.nchunk_a;
+  const long grid_stats = std::max<long>(1, std::min<long>((warps_needed + kStatThreads / 32 - 1) / (kStatThreads / 32),
+                                                           max_ctas));
+  accept_stats_kernel<<<(unsigned)grid_stats, kStatThreads, 0, s>>>(
       target_logits, draft_logits, labels, batch, B, gamma, V, temperature, plan, ws);
   simsd_status st = last_launch_status();
   if (st != SIMSD_OK) return st;
