@@ -229,6 +229,29 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def _traffic(workload, call):
+    """DRAM bytes per launch of `call` on `workload` from profiles/traffic.txt, if the
+    recorded source hash still matches the kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        parts = line.split()
+        if len(parts) != 5 or line.startswith("#"):
+            continue
+        wl, c, nbytes, src, sha = parts
+        if wl == workload and c == call:
+            try:
+                cur = hashlib.sha1(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:12]
+            except OSError:
+                return None
+            return int(nbytes) if cur == sha else None
+    return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -382,7 +405,7 @@ def run_ours(args):
         roofline = {"bound": "hbm", "kernel": "simsd_accept (accept_stats + accept_finish)"
                     if dom == "accept" else "simsd_verify_attention",
                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": None,
+                    "frac": achieved / peak, "traffic": _traffic(w.name, dom),
                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                     "algorithmic_bytes_per_launch": call_bytes[dom],
                     "avg_launch_us": per_call[dom] * 1e6,
