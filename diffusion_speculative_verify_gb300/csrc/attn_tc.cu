@@ -81,7 +81,7 @@ struct Cfg {
   static constexpr uint32_t kOffStages = kOffP + NRB * 2 * kPBlock;
   static constexpr uint32_t kOffTail = kOffStages + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffTail + kStageBytes;
-  static constexpr uint32_t kBarBytes = 256;
+  static constexpr uint32_t kBarBytes = 1024;
   static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + base alignment
   // TMEM columns: S buffers [rb][buf] x 64, two 128-column O accumulators, then (NRB = 1)
   // the rotated Q as bf16 pairs (64 columns)
@@ -265,6 +265,8 @@ struct Shared {
   int abort;
   int64_t T, t0, t1, Tb;
   int b;
+  int pos[2 * kMaxB];       // position ids of the current pair's response slots
+  uint8_t lab[2 * kMaxB];   // their labels
 };
 
 
@@ -318,6 +320,47 @@ __device__ __forceinline__ void rope_row(uint4 (&v)[16], const float2* cs, float
   }
 }
 
+// Max over the valid entries (bit c of vm) of a 32-column chunk of fp32 scores.
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], uint32_t vm) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (vm == 0xffffffffu) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if ((vm >> c) & 1u) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// p = 2^(s - m) on the valid entries (0 elsewhere) of a 32-column chunk, packed as bf16
+// pairs (lower column in the low half); returns the sum of the fp32 p.
+__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[32], uint32_t vm, float m,
+                                           uint32_t (&pk)[16]) {
+  float s0 = 0.f, s1 = 0.f;
+  if (vm == 0xffffffffu) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const float p0 = ptx::ex2(__uint_as_float(r[c]) - m);
+      const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - m);
+      s0 += p0;
+      s1 += p1;
+      pk[c >> 1] = pack_bf16(p0, p1);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const float p0 = ((vm >> c) & 1u) ? ptx::ex2(__uint_as_float(r[c]) - m) : 0.f;
+      const float p1 = ((vm >> (c + 1)) & 1u) ? ptx::ex2(__uint_as_float(r[c + 1]) - m) : 0.f;
+      s0 += p0;
+      s1 += p1;
+      pk[c >> 1] = pack_bf16(p0, p1);
+    }
+  }
+  return s0 + s1;
+}
+
 __device__ __forceinline__ void load_row(uint4 (&v)[16], const __nv_bfloat16* src) {
   const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -330,6 +373,23 @@ __device__ __forceinline__ void store_row_sw(uint8_t* tile, uint32_t half_bytes,
 #pragma unroll
   for (int c = 0; c < 16; ++c)
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half_bytes + sw128(r, c & 7)) = v[c];
+}
+
+// A 128-element bf16 row (16 chunks) into 64 TMEM columns of this thread's lane:
+// elements (2c, 2c + 1) in column c, the lower index in the low half.
+__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      w[4 * c] = v[8 * half + c].x;
+      w[4 * c + 1] = v[8 * half + c].y;
+      w[4 * c + 2] = v[8 * half + c].z;
+      w[4 * c + 3] = v[8 * half + c].w;
+    }
+    ptx::tmem_st32(taddr + 32 * half, w);
+  }
 }
 
 // ------------------------------------------------------------------------- the kernel
@@ -883,7 +943,10 @@ __global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
 // operand from shared memory, or N < 128, caps an M = 128 instruction well below it):
 //   S_j = Q K_j^T   A = rotated Q (TMEM), B = K tile (smem, K-major), N = 128 keys
 //   O  += P_j V_j   A = P_j (TMEM, bf16),  B = V tile (smem, MN-major), N = 128 = D
-// TMEM columns: S buffers [0,128) and [128,256), O [256,384), Q [384,448), P [448,512).
+// TMEM columns: S buffers [0,128) and [128,256), O [256,384), Q [384,448). P_j (bf16 pairs,
+// 64 columns) is written in place over the first columns of S_j, which the softmax has
+// already read, so P double-buffers with S; an S buffer is released by the commit of the
+// P V that read its P.
 // Warps 0-3: softmax (thread = row = TMEM lane; warps whose 32 rows are all padding skip
 // their work), warp 4: TMA producer, warp 5: MMA issuer (non-blocking event loop).
 namespace r128 {
@@ -898,10 +961,10 @@ constexpr uint32_t kTailKV = 2 * kTailHalf;      // 16 KB
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffTail = kOffStages + kStages * kStage;  // tail K (16 KB) then V (16 KB)
 constexpr uint32_t kOffBar = kOffTail + 2 * kTailKV;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemQ = 384, kTmemP = 448, kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemQ = 384, kTmemCols = 512;
 static_assert(kStages <= kMaxStages, "stage barriers");
 }  // namespace r128
 
@@ -909,7 +972,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     attn_tc128_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ TcArgs a) {
   using namespace r128;
-  static_assert(sizeof(Shared) <= 256, "barrier area");
+  static_assert(sizeof(Shared) <= 1024, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
@@ -917,9 +980,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = ptx::smem_u32(smem);
   auto bar = [&](int i) { return ptx::smem_u32(&sh->bars[i]); };
-  // single-buffer P: kPFull0 = P_j written, kPFree0 = P_j V_j completed
-  const uint32_t bar_pfull = ptx::smem_u32(&sh->bars[kPFull0]);
-  const uint32_t bar_pvdone = ptx::smem_u32(&sh->bars[kPFree0]);
+  // kPFull0 + b: P of the tile in S buffer b written. kSFree0 + b: the P V that read S
+  // buffer b completed; its phase for tile j is j / 2, and the previous phase (tile j - 2) is
+  // always complete by the time anyone waits for tile j, so a parity wait is unambiguous.
 
   if (warp == kProducerWarp) {
     const SchedStart s = warp_schedule(a, blockIdx.x, a.ctas, lane);
@@ -936,10 +999,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(bar(kSFull0 + i), 1);
-        ptx::mbar_init(bar(kSFree0 + i), 128);
+        ptx::mbar_init(bar(kSFree0 + i), 1);
+        ptx::mbar_init(bar(kPFull0 + i), 128);
       }
-      ptx::mbar_init(bar_pfull, 128);
-      ptx::mbar_init(bar_pvdone, 1);
       ptx::mbar_init(bar(kQFull), 128);
       ptx::mbar_init(bar(kDrain), 1);
       ptx::fence_mbar_init();
@@ -1040,17 +1102,18 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         return true;
       };
       auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
-        if (!ptx::mbar_test(bar_pfull, jj & 1)) return false;
+        const int buf = jj & 1;
+        if (!ptx::mbar_test(bar(kPFull0 + buf), (jj >> 1) & 1)) return false;
         ptx::tc_fence_after();
         const int s = stage_of[jj & 7];
         const uint32_t vaddr = s < 0 ? sbase + kOffTail + kTailKV : sbase + kOffStages + s * kStage + kKV;
         const uint32_t lbo = s < 0 ? kTailHalf : kHalf;
         const int nk = s < 0 ? 4 : kKeys / 16;
         for (int kk = 0; kk < nk; ++kk)
-          ptx::mma_f16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8,
+          ptx::mma_f16_ts(tmem + kTmemO, tmem + kTmemS0 + buf * 128 + kk * 8,
                           ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV,
                           (first_in_seg && kk == 0) ? 0u : 1u);
-        ptx::mma_commit(bar_pvdone);
+        ptx::mma_commit(bar(kSFree0 + buf));
         if (s >= 0) ptx::mma_commit(bar(kEmpty0 + s));
         return true;
       };
@@ -1059,7 +1122,21 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           it.advance(a);
           continue;
         }
-        ok = wait_bar(sh, bar(kQFull), nseg & 1, a.dev_err);
+        {  // poll (no suspend): the segment cannot start before Q is in TMEM
+          const uint64_t t_start = ptx::globaltimer_ns();
+          uint32_t spin = 0;
+          while (!ptx::mbar_test(bar(kQFull), nseg & 1)) {
+            if ((++spin & 255) == 0 &&
+                (*(volatile int*)&sh->abort || ptx::globaltimer_ns() - t_start > kWaitLimitNs)) {
+              if (!*(volatile int*)&sh->abort) {
+                *(volatile int*)&sh->abort = 1;
+                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
+              }
+              ok = false;
+              break;
+            }
+          }
+        }
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t jfirst = j, jend = j + (uint32_t)it.n;
@@ -1112,9 +1189,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint8_t* tailk = smem + kOffTail;
     uint8_t* tailv = tailk + kTailKV;
-    // (cos, sin) table of the 2B response positions lives in the tail V area during the
-    // prologue when it fits (2B * 64 * 8 bytes <= 16 KB), else each thread evaluates its own
-    const bool use_table = twoB * 64 * 8 <= (int)kTailKV;
     SegIter it;
     it.init(a, st);
     uint32_t j = 0;
@@ -1144,92 +1218,75 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         continue;
       }
       const int P = a.prompt_len[b];
-      const int* pos = a.pos_ids + (size_t)b * twoB;
-      // ---- prologue: rotation table, rotated + scaled Q rows into TMEM, tail K/V tiles
-      float2* rtab = reinterpret_cast<float2*>(tailv);
-      if (use_table) {
-        for (int e = tid; e < twoB * 64; e += 128) {
-          const int sidx = e >> 6, d = e & 63;
-          float sn, cs;
-          rope_sincos(pos[sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
-          rtab[e] = make_float2(cs, sn);
-        }
+      const bool has_tail = it.has_tail;
+      // ---- prologue: rotated + scaled Q rows into TMEM, rotated tail K and plain tail V
+      // tiles. The Q row, labels and positions are loaded together and the tail rows are
+      // prefetched into L2 at the same time, so only one wait goes to DRAM.
+      const int key = tid & 63;
+      const bool tail_row = has_tail && key < twoB;
+      uint4 v[16];
+      const __nv_bfloat16* trow =
+          (tid < 64 ? a.k_resp : a.v_resp) + (((size_t)b * twoB + key) * a.Hkv + h) * kD;
+      if (tail_row) {  // into L2 now, into registers once Q is in TMEM
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
+      }
+      if (warp_active && real) load_row(v, a.q + orow * kD);
+      if (tid < twoB) {
+        sh->lab[tid] = a.labels[(size_t)b * twoB + tid];
+        sh->pos[tid] = a.pos_ids[(size_t)b * twoB + tid];
       }
       ptx::named_bar_sync(1, 128);
-      uint4 v[16];
+      // (cos, sin) of the 2B response positions, over the tail K and V area (2B <= 64:
+      // at most 32 KB); the tail rows are stored once every read of the table is done
+      float2* rtab = reinterpret_cast<float2*>(tailk);
+      for (int e = tid; e < twoB * 64; e += 128) {
+        const int sidx = e >> 6, d = e & 63;
+        float sn, cs;
+        rope_sincos(sh->pos[sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
+        rtab[e] = make_float2(cs, sn);
+      }
+      ptx::named_bar_sync(1, 128);
       if (warp_active) {
         if (real) {
-          load_row(v, a.q + orow * kD);
-          if (use_table) {
-            rope_row(v, rtab + s_slot * 64, a.scale_log2);
-          } else {
-            float2 cs[64];
-#pragma unroll
-            for (int d = 0; d < 64; ++d) rope_sincos(pos[s_slot], a.rope.c_hi[d], a.rope.c_lo[d], &cs[d].y, &cs[d].x);
-            rope_row(v, cs, a.scale_log2);
-          }
+          rope_row(v, rtab + s_slot * 64, a.scale_log2);
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
         // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
-        uint32_t w[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            w[4 * c] = v[8 * half + c].x;
-            w[4 * c + 1] = v[8 * half + c].y;
-            w[4 * c + 2] = v[8 * half + c].z;
-            w[4 * c + 3] = v[8 * half + c].w;
-          }
-          ptx::tmem_st32(tmem + lane_off + kTmemQ + 32 * half, w);
-        }
-        ptx::tmem_st_wait();
+        tmem_st_row(tmem + lane_off + kTmemQ, v);
       }
-      const bool has_tail = it.has_tail;
-      const int key = tid & 63;
-      if (has_tail && tid < 64) {  // tail K rows (rotated) into the 64-key K layout
-        if (key < twoB) {
-          const size_t krow = (((size_t)b * twoB + key) * a.Hkv + h) * kD;
-          load_row(v, a.k_resp + krow);
-          if (use_table) {
-            rope_row(v, rtab + key * 64, 1.f);
-          } else {
-            float2 cs[64];
-#pragma unroll
-            for (int d = 0; d < 64; ++d) rope_sincos(pos[key], a.rope.c_hi[d], a.rope.c_lo[d], &cs[d].y, &cs[d].x);
-            rope_row(v, cs, 1.f);
-          }
+      ptx::tmem_st_wait();
+      if (has_tail) {
+        if (tail_row) {
+          load_row(v, trow);
+          if (tid < 64) rope_row(v, rtab + key * 64, 1.f);  // K rotated, V as is
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
-        store_row_sw(tailk, kTailHalf, key, v);
       }
-      ptx::named_bar_sync(1, 128);  // every table read is done: the V tail may overwrite it
-      if (has_tail && tid >= 64) {
-        if (key < twoB) {
-          load_row(v, a.v_resp + (((size_t)b * twoB + key) * a.Hkv + h) * kD);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
-        }
-        store_row_sw(tailv, kTailHalf, key, v);
-      }
+      ptx::named_bar_sync(1, 128);  // table reads done
+      if (has_tail) store_row_sw(tid < 64 ? tailk : tailv, kTailHalf, key, v);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kQFull));
-      // visibility of the 2B response keys for this row (bit k = key k visible)
-      uint64_t vis = 0;
+      // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
+      uint32_t vis0 = 0, vis1 = 0;
       if (has_tail) {
-        const uint8_t* lab = a.labels + (size_t)b * twoB;
         if (real) {
-          const int t = row_threshold(lab[s_slot]);
+          const int th = row_threshold(sh->lab[s_slot]);
           for (int k = 0; k < twoB; ++k)
-            if (response_key_visible(lab[k], t)) vis |= 1ull << k;
+            if (response_key_visible(sh->lab[k], th)) {
+              if (k < 32)
+                vis0 |= 1u << k;
+              else
+                vis1 |= 1u << (k - 32);
+            }
         } else {
-          vis = twoB == 64 ? ~0ull : ((1ull << twoB) - 1);
+          vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
+          vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
         }
       }
       float m_used = -INFINITY, l = 0.f;
@@ -1238,128 +1295,106 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         const int buf = j & 1;
         ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
         if (!ok) break;
-        if (!warp_active) {  // padding rows only: keep the barriers' counts, skip the work
-          ptx::mbar_arrive(bar(kSFree0 + buf));
-          if (j > 0) {
-            ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, (j - 1) & 1, a.dev_err));
-            if (!ok) break;
-          }
-          ptx::mbar_arrive(bar_pfull);
+        if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
+          ptx::mbar_arrive(bar(kPFull0 + buf));
           continue;
         }
         ptx::tc_fence_after();
-        const int ncols = (i == 0) ? 64 : kKeys;  // warp-uniform
-        float x[kKeys];
-        {
-          const uint32_t ts = tmem + lane_off + kTmemS0 + buf * 128;
-          uint32_t r0[32], r1[32];
-          ptx::tmem_ld32(ts, r0);
-          ptx::tmem_ld32(ts + 32, r1);
-          ptx::tmem_ld_wait(r0);
-          ptx::tmem_ld_wait(r1);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x[c] = __uint_as_float(r0[c]);
-            x[c + 32] = __uint_as_float(r1[c]);
+        const uint32_t ts = tmem + lane_off + kTmemS0 + buf * 128;
+        const int nchunks = (i == 0) ? 2 : kKeys / 32;  // warp-uniform
+        const int nvalid = (i == 0) ? 0 : P - (i - 1) * kKeys;
+        // valid-column bits of 32-column chunk k
+        auto chunk_mask = [&](int k) -> uint32_t {
+          if (i == 0) return k == 0 ? vis0 : vis1;
+          const int n = nvalid - 32 * k;
+          return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+        };
+        // One pass in the common case: chunk k's P = 2^(s - m) goes in place over S columns
+        // [16k, 16k + 16), which this thread has already read. If some row's max grows by
+        // more than 2^8 (always on the first tile of a segment), finish the tile's max over
+        // the remaining chunks, rescale O and the P chunks already written, and go on.
+        float lsum = 0.f;
+        int k = 0;
+        bool grew = false;
+#pragma unroll 1
+        for (; k < nchunks; ++k) {
+          uint32_t r[32];
+          ptx::tmem_ld32(ts + 32 * k, r);
+          ptx::tmem_ld_wait(r);
+          const uint32_t vm = chunk_mask(k);
+          if (__any_sync(0xffffffffu, chunk_max(r, vm) > m_used + 8.f)) {
+            grew = true;
+            break;
           }
-          if (ncols == kKeys) {
-            ptx::tmem_ld32(ts + 64, r0);
-            ptx::tmem_ld32(ts + 96, r1);
-            ptx::tmem_ld_wait(r0);
-            ptx::tmem_ld_wait(r1);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              x[c + 64] = __uint_as_float(r0[c]);
-              x[c + 96] = __uint_as_float(r1[c]);
-            }
-          } else {
-#pragma unroll
-            for (int c = 64; c < kKeys; ++c) x[c] = -INFINITY;
+          uint32_t pk[16];
+          lsum += chunk_exp(r, vm, m_used == -INFINITY ? 0.f : m_used, pk);
+          ptx::tmem_st16(ts + 16 * k, pk);
+        }
+        if (grew) {
+          float mt = -INFINITY;
+#pragma unroll 1
+          for (int kk = k; kk < nchunks; ++kk) {
+            uint32_t r[32];
+            ptx::tmem_ld32(ts + 32 * kk, r);
+            ptx::tmem_ld_wait(r);
+            mt = fmaxf(mt, chunk_max(r, chunk_mask(kk)));
           }
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kSFree0 + buf));
-        if (i == 0) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = ((vis >> c) & 1ull) ? x[c] : -INFINITY;
-        } else {
-          const int nvalid = P - (i - 1) * kKeys;
-          if (nvalid < kKeys) {
-#pragma unroll
-            for (int c = 0; c < kKeys; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
-          }
-        }
-        float mt;
-        {
-          float mx[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = x[u];
-#pragma unroll
-          for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-          mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        }
-        // P_{j-1} V_{j-1} must have completed before O is rescaled or P is overwritten
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, (j - 1) & 1, a.dev_err));
-          if (!ok) break;
-          ptx::tc_fence_after();
-        }
-        // lazy rescale (warp-uniform: TMEM accesses are warp-collective)
-        if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
           const float m_new = fmaxf(m_used, mt);
-          if (j != jfirst) {
-            const float alpha = ptx::ex2(m_used - m_new);
+          const float alpha = m_used == -INFINITY ? 0.f : ptx::ex2(m_used - m_new);
+          if (j != jfirst) {  // O holds P V of earlier tiles: rescale once the last P V landed
+            const uint32_t jp = j - 1;
+            ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jp & 1)), (jp >> 1) & 1, a.dev_err));
+            if (!ok) break;
+            ptx::tc_fence_after();
             l *= alpha;
             const uint32_t to = tmem + lane_off + kTmemO;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
+#pragma unroll 1
+            for (int kk = 0; kk < 4; ++kk) {
               uint32_t o[32];
-              ptx::tmem_ld32(to + 32 * k, o);
+              ptx::tmem_ld32(to + 32 * kk, o);
               ptx::tmem_ld_wait(o);
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(to + 32 * k, o);
+              ptx::tmem_st32(to + 32 * kk, o);
             }
           }
+          lsum *= alpha;
+#pragma unroll 1
+          for (int kk = 0; kk < k; ++kk) {  // P chunks already written with the old max
+            uint32_t pk[16];
+            ptx::tmem_ld16(ts + 16 * kk, pk);
+            ptx::tmem_ld16_wait(pk);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(bf16_lo(pk[e]) * alpha, bf16_hi(pk[e]) * alpha);
+            ptx::tmem_st16(ts + 16 * kk, pk);
+          }
           m_used = m_new;
+          const float msafe = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll 1
+          for (; k < nchunks; ++k) {
+            uint32_t r[32], pk[16];
+            ptx::tmem_ld32(ts + 32 * k, r);
+            ptx::tmem_ld_wait(r);
+            lsum += chunk_exp(r, chunk_mask(k), msafe, pk);
+            ptx::tmem_st16(ts + 16 * k, pk);
+          }
         }
-        const float msafe = m_used == -INFINITY ? 0.f : m_used;
-        uint32_t pk[kKeys / 2];
-        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < kKeys; c += 2) {
-          const float p0 = ptx::ex2(x[c] - msafe);
-          const float p1 = ptx::ex2(x[c + 1] - msafe);
-          ls0 += p0;
-          ls1 += p1;
-          pk[c >> 1] = pack_bf16(p0, p1);
-        }
-        l += ls0 + ls1;
-        {
-          uint32_t w[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) w[c] = pk[c];
-          ptx::tmem_st32(tmem + lane_off + kTmemP, w);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) w[c] = pk[32 + c];
-          ptx::tmem_st32(tmem + lane_off + kTmemP + 32, w);
-        }
+        l += lsum;
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_pfull);
+        ptx::mbar_arrive(bar(kPFull0 + buf));
       }
       if (!ok) break;
       // ---- epilogue: wait for the last P V, then O / l (or the partial)
       const uint32_t jl = j - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(sh, bar_pvdone, jl & 1, a.dev_err));
+      ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err));
       if (!ok) break;
       ptx::tc_fence_after();
       if (warp_active) {
         const uint32_t to = tmem + lane_off + kTmemO;
         const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
         const float inv = it.full ? 1.f / l : 1.f;
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           uint32_t o[32];
           ptx::tmem_ld32(to + 32 * k, o);
