@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa8b_bf16")
@@ -229,6 +229,106 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only queries) by a
+    thread that polls about every millisecond while `active` is set, so that even a timed
+    region of a few milliseconds is sampled. Falls back to nvidia-smi when NVML is absent."""
+    # clock-event reason bits (public NVML constants)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = None
+        self.samples = []
+        self.active = threading.Event()
+        self.done = threading.Event()
+        self.thread = None
+        self.index = device.index if device.index is not None else 0
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(device).uuid)
+                ok = lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok:
+                idx = device.index if device.index is not None else 0
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                if vis and vis.split(",")[0].strip().isdigit():
+                    idx = int(vis.split(",")[idx].strip())
+                if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                    return
+            self.h = h
+            mx = ctypes.c_uint()
+            self.max_mhz = (mx.value if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+                            else None)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.lib = lib
+        except Exception:
+            self.lib = None
+
+    def _poll(self):
+        ct, lib, h = self.ct, self.lib, self.h
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self.done.is_set():
+            if not self.active.wait(timeout=0.05):
+                continue
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                p = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+                r = rs.value if self.reasons_fn(h, ct.byref(rs)) == 0 else 0
+                if self.active.is_set():
+                    self.samples.append((mhz.value, p, r))
+            time.sleep(0.001)
+
+    def start(self):
+        import threading
+        if self.lib is None:
+            self.smi = ClockSampler(self.index)
+            return
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+
+    def timed_begin(self):
+        self._switch = sys.getswitchinterval()
+        sys.setswitchinterval(1e-4)   # let the poller run while the launch loop holds the GIL
+        if self.lib is None:
+            self.smi.start()
+        self.active.set()
+
+    def timed_end(self):
+        self.active.clear()
+        sys.setswitchinterval(self._switch)
+        if self.lib is None:
+            self.smi_result = self.smi.stop()
+
+    def stop(self):
+        if self.lib is None:
+            return getattr(self, "smi_result", {"sm_mhz": None, "sm_max_mhz": None,
+                                                "reasons": ["no samples"]})
+        self.done.set()
+        self.thread.join(timeout=2)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "source": "nvml"}
+        reasons = sorted({n for _, _, r in self.samples for bit, n in self.REASONS.items()
+                          if r & bit})
+        power = [p for _, p, _ in self.samples if p is not None]
+        return {"sm_mhz": statistics.median(m for m, _, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "sm_mhz_min": min(m for m, _, _ in self.samples),
+                "power_w_max": max(power) if power else None,
+                "source": "nvml, timed region only"}
+
+
 def _traffic(workload, call):
     """DRAM bytes per launch of `call` on `workload` from profiles/traffic.txt, if the
     recorded source hash still matches the kernel source (else None)."""
@@ -354,7 +454,7 @@ def run_ours(args):
         else:
             steps[k % n_sets].run(stream)
 
-    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks = NvmlSampler(device)
     clocks.start()
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
@@ -367,6 +467,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    clocks.timed_begin()
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         ev0.record(stream)
@@ -375,6 +476,7 @@ def run_ours(args):
         ev1.record(stream)
     ev1.synchronize()
     torch.cuda.synchronize()
+    clocks.timed_end()
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t_wall0

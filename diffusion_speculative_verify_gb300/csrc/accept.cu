@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace simsd {
 
@@ -112,6 +113,8 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     const float* __restrict__ target, const float* __restrict__ draft,
     const uint8_t* __restrict__ labels, int batch, int B, int gamma, int V, float T,
     AcceptPlan plan, AcceptWs ws) {
+  // K3b may be scheduled as SMs free up; it waits for this grid before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long warp_global = (long)blockIdx.x * (kStatThreads / 32) + (threadIdx.x >> 5);
   const long nwarps = (long)gridDim.x * (kStatThreads / 32);
@@ -203,6 +206,111 @@ __device__ __forceinline__ int unpack_token(unsigned long long w) {
   return (int)(0xFFFFFFFFu - (unsigned)(w & 0xFFFFFFFFull));
 }
 
+// -ln(u) for u in (0, 1) to a few ulp relative. The race winners sit where u is close to 1
+// and -ln(u) tiny, where the lg2 instruction's absolute error (about 2^-22) would be a large
+// relative one; there (u >= 1/2) the identity -ln(u) = 2 atanh(s), s = (1 - u) / (1 + u) in
+// (0, 1/3], is summed as an odd series up to s^13 (truncation below 2e-8 relative; 1 - u is
+// exact). Below 1/2 the result is at least ln 2 and lg2's absolute error is harmless.
+__device__ __forceinline__ float neg_log_uniform(float u) {
+  if (u < 0.5f) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(u));
+    return y * -0.6931471805599453f;
+  }
+  const float sv = __fdividef(1.f - u, 1.f + u);
+  const float s2 = sv * sv;
+  float poly = 2.f / 13.f;
+  poly = fmaf(poly, s2, 2.f / 11.f);
+  poly = fmaf(poly, s2, 2.f / 9.f);
+  poly = fmaf(poly, s2, 2.f / 7.f);
+  poly = fmaf(poly, s2, 2.f / 5.f);
+  poly = fmaf(poly, s2, 2.f / 3.f);
+  poly = fmaf(poly, s2, 2.f);
+  return sv * poly;
+}
+
+// Race keys of the 4 entries of counter group g (entries 4g .. 4g + 3 below `end`) on the
+// residual max(0, p - q), or on p when `on_p`. p and q use the ex2 instruction (a few ulp),
+// which moves a key by about 1e-6 relative: only a race whose two best keys are that close
+// can change winner. The group's counter block is drawn only if one of its keys is positive.
+__device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], const float (&d)[4],
+                                           float T, bool unit_T, float mt, float inv_st, float md,
+                                           float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
+                                           uint32_t off_hi, uint32_t key0, uint32_t key1,
+                                           unsigned long long& best, bool& anyp) {
+  float key[4];
+  bool pos = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // p and q rounded on their own (no fused multiply-add into p - q): where the two agree
+    // in fp32 the residual is exactly 0, not the rounding error of q
+    const float p = __fmul_rn(exp_shifted(scale_logit(t[j], T, unit_T), mt), inv_st);
+    if (on_p) {
+      key[j] = p;
+    } else {
+      const float q = __fmul_rn(exp_shifted(scale_logit(d[j], T, unit_T), md), inv_sd);
+      key[j] = __fsub_rn(p, q);
+    }
+    if (4 * g + j >= end) key[j] = on_p ? -1.f : 0.f;
+    pos |= key[j] > 0.f;
+  }
+  anyp |= pos;
+  if (!pos && !on_p) return;
+  Philox4 c4 = {r, off_lo, off_hi, kResampleTag | (uint32_t)g};
+  const Philox4 rnd = philox4x32_10(c4, key0, key1);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (key[j] > 0.f || (on_p && key[j] >= 0.f)) {
+      const float E = neg_log_uniform(word_to_uniform(philox_word(rnd, j)));
+      const unsigned long long kr = pack_key(__fdividef(key[j], E), 4 * g + j);
+      best = kr > best ? kr : best;
+    }
+  }
+}
+
+// Race over entries [c0, c1) (c0 a multiple of 4) of one target row (and draft row unless
+// `on_p`), by `nthreads` threads with thread index `t`: four counter groups' loads in
+// flight per thread at a time.
+__device__ __forceinline__ void race_range(const float* __restrict__ trow, const float* __restrict__ drow,
+                                           int c0, int c1, int t, int nthreads, bool vec_ok,
+                                           float T, bool unit_T, float mt, float inv_st, float md,
+                                           float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
+                                           uint32_t off_hi, uint32_t key0, uint32_t key1,
+                                           unsigned long long& best, bool& anyp) {
+  const int g0 = c0 / 4, g1 = c0 < c1 ? (c1 + 3) / 4 : g0;
+  for (int gb = g0 + t; gb < g1; gb += 4 * nthreads) {
+    float tv[4][4], dv[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = gb + u * nthreads;
+      if (g < g1) {
+        if (vec_ok) {
+          const float4 t4 = __ldg(reinterpret_cast<const float4*>(trow) + g);
+          tv[u][0] = t4.x; tv[u][1] = t4.y; tv[u][2] = t4.z; tv[u][3] = t4.w;
+          if (!on_p) {
+            const float4 d4 = __ldg(reinterpret_cast<const float4*>(drow) + g);
+            dv[u][0] = d4.x; dv[u][1] = d4.y; dv[u][2] = d4.z; dv[u][3] = d4.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int v = 4 * g + j;
+            tv[u][j] = v < c1 ? __ldg(trow + v) : 0.f;
+            dv[u][j] = (v < c1 && !on_p) ? __ldg(drow + v) : 0.f;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = gb + u * nthreads;
+      if (g < g1)
+        race_group(g, c1, tv[u], dv[u], T, unit_T, mt, inv_st, md, inv_sd, on_p, r, off_lo,
+                   off_hi, key0, key1, best, anyp);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     const float* __restrict__ target, const float* __restrict__ draft,
     const int32_t* __restrict__ tokens, const uint8_t* __restrict__ labels, int batch, int B,
@@ -210,6 +318,8 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     AcceptPlan plan, AcceptWs ws, int32_t* __restrict__ accepted_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_pos,
     int32_t* __restrict__ n_commit, uint32_t* __restrict__ dev_err) {
+  // launched as a programmatic dependent of K3a: wait for K3a's results before any read
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int chunk = blockIdx.x % plan.nchunk_b;
   const int r = blockIdx.x / plan.nchunk_b;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -319,25 +429,9 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     const int c1 = min(V, c0 + plan.chunk_b);
     unsigned long long best_res = 0ull;
     bool anyp = false;
-    const float inv_st = 1.f / st, inv_sd = 1.f / sd;
-    for (int g = c0 / 4 + tid; g * 4 < c1; g += blockDim.x) {
-      Philox4 c4 = {(uint32_t)r, off_lo, off_hi, kResampleTag | (uint32_t)g};
-      const Philox4 rnd = philox4x32_10(c4, key0, key1);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int v = 4 * g + j;
-        if (v >= c1) break;
-        const float p = expf(scale_logit(trow[v], T, unit_T) - mt) * inv_st;
-        const float q = expf(scale_logit(drow[v], T, unit_T) - md) * inv_sd;
-        const float res = p - q;
-        if (res > 0.f) {
-          anyp = true;
-          const float E = -logf(word_to_uniform(philox_word(rnd, j)));
-          const unsigned long long kr = pack_key(__fdividef(res, E), v);
-          best_res = kr > best_res ? kr : best_res;
-        }
-      }
-    }
+    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+    race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
+               1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res, anyp);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
@@ -368,19 +462,11 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     // over the whole row, done here by the last CTA (never on typical inputs)
     const int k = s_order[a];
     const float* trow = target + ((size_t)r * B + k) * (size_t)V;
-    const float inv_st = 1.f / s_st;
     unsigned long long best = 0ull;
-    for (int g = tid; g * 4 < V; g += blockDim.x) {
-      Philox4 c4 = {(uint32_t)r, off_lo, off_hi, kResampleTag | (uint32_t)g};
-      const Philox4 rnd = philox4x32_10(c4, key0, key1);
-      for (int j = 0; j < 4 && 4 * g + j < V; ++j) {
-        const int v = 4 * g + j;
-        const float p = expf(scale_logit(trow[v], T, unit_T) - s_mt) * inv_st;
-        const float E = -logf(word_to_uniform(philox_word(rnd, j)));
-        const unsigned long long kp = pack_key(__fdividef(p, E), v);
-        best = kp > best ? kp : best;
-      }
-    }
+    bool anyp = false;
+    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+    race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
+               1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best, anyp);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -465,10 +551,25 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
       target_logits, draft_logits, labels, batch, B, gamma, V, temperature, plan, ws);
   simsd_status st = last_launch_status();
   if (st != SIMSD_OK) return st;
-  accept_finish_kernel<<<(unsigned)grid_b, kFinishThreads, 0, s>>>(
-      target_logits, draft_logits, draft_tokens, labels, batch, B, gamma, V, temperature,
-      (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), (uint32_t)(offset & 0xffffffffu),
-      (uint32_t)(offset >> 32), plan, ws, accepted_len, out_tokens, out_pos, n_commit, dev_err);
+  // K3b as a programmatic dependent of K3a: scheduled while K3a drains
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)grid_b);
+  cfg.blockDim = dim3(kFinishThreads);
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, accept_finish_kernel, target_logits, draft_logits, draft_tokens, labels, batch, B,
+      gamma, V, temperature, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32),
+      (uint32_t)(offset & 0xffffffffu), (uint32_t)(offset >> 32), plan, ws, accepted_len,
+      out_tokens, out_pos, n_commit, dev_err);
+  if (e != cudaSuccess) {
+    record_cuda_error("cudaLaunchKernelEx(accept_finish_kernel)", e);
+    return SIMSD_ERR_CUDA;
+  }
   return last_launch_status();
 }
 

@@ -1,5 +1,6 @@
-// Thin inline-PTX wrappers for sm_100-family features used by the tensor-core attention:
-// mbarriers, TMA tensor loads, tcgen05 (TMEM allocation, MMA, commit, TMEM load/store).
+// Thin inline-PTX wrappers for sm_100-family features used by the tensor-core attention and
+// the acceptance kernel: mbarriers, bulk and TMA tensor loads, tcgen05 (TMEM allocation, MMA,
+// commit, TMEM load/store).
 #pragma once
 
 #include <cuda.h>
@@ -50,6 +51,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// 1-D bulk copy of `bytes` from global memory into this CTA's shared memory, counted on
+// mbarrier `bar` (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

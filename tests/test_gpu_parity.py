@@ -255,7 +255,7 @@ def test_accept_invalid_labels_and_tokens():
     ot = torch.zeros(3, B, dtype=torch.int32, device="cuda")
     op = torch.zeros(3, B, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty(pkg.simsd_accept_workspace(3, B, B, V), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(pkg.simsd_accept_workspace(3, B, B, V), dtype=torch.uint8, device="cuda")
     pkg.simsd_accept(tl, tl, toks, labels, B, 1.0, 1, 0, out["accepted_len"], ot, op,
                      out["n_commit"], ws, err)
     torch.cuda.synchronize()
@@ -266,6 +266,96 @@ def test_accept_invalid_labels_and_tokens():
     assert np.array_equal(ot.cpu().numpy(), res["out_tokens"])
     assert np.array_equal(op.cpu().numpy(), res["out_pos"])
     assert int(err.item()) == res["err"] == (oracle.ERR_TAU | oracle.ERR_TOKEN)
+
+
+def _accept_outputs(path, tl, dl, toks, labels, gamma, T, seed, ws=None):
+    """Runs one acceptance entry point: "workspace" (simsd_accept on a caller workspace,
+    `ws` or a fresh zeroed one) or "fixed" (simsd_accept_noalloc on the library's array)."""
+    pkg = _pkg()
+    b, B, V = tl.shape
+    out = {k: torch.full((b,), -7, dtype=torch.int32, device="cuda")
+           for k in ("accepted_len", "n_commit")}
+    out |= {k: torch.full((b, B), -7, dtype=torch.int32, device="cuda")
+            for k in ("out_tokens", "out_pos")}
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = (tl, dl, toks, labels, gamma, T, seed, 0, out["accepted_len"], out["out_tokens"],
+            out["out_pos"], out["n_commit"])
+    if path == "workspace":
+        if ws is None:
+            ws = torch.zeros(pkg.simsd_accept_workspace(b, B, gamma, V), dtype=torch.uint8,
+                             device="cuda")
+        pkg.simsd_accept(*args, ws, err)
+    else:
+        pkg.simsd_accept_noalloc(*args, err)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}, int(err.item())
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 1.0), ("gqa8b_bf16", 1.0),
+                                    ("gqa8b_bf16", 0.7)])
+def test_accept_fixed_scratch_entry_bit_exact(name, T):
+    """The allocation-free entry point (its scratch a fixed array in the library) against
+    the oracle."""
+    w = W[name].with_(temperature=T)
+    inputs, meta = H.make_case(w, seed=21)
+    st = _step(w, inputs, meta, with_lse=False)
+    reqs = list(range(w.batch))
+    res = H.oracle_accept(inputs, st.labels, w.gamma, T, meta["philox_seed"], 0)
+    got, err = _accept_outputs("fixed", inputs["target_logits"], inputs["draft_logits"],
+                               inputs["draft_tokens"], st.labels, w.gamma, T,
+                               meta["philox_seed"])
+    ties = H.check_accept(res, got, reqs)
+    assert ties <= max(1, len(reqs) // 100)
+    assert err == 0
+
+
+@pytest.mark.parametrize("path", ["workspace", "fixed"])
+def test_accept_residual_vanishing_in_fp32_races_on_p(path):
+    """Target and draft logits equal except at the draft tokens, which sit far below every
+    other logit (-20 in the draft, -30 in the target): step 1 is rejected (p/q = e^-10 at
+    the token) while in fp32 the two softmaxes agree everywhere else, so max(0, p - q) is
+    0 at every entry and the race runs on p. In fp64 the residual is e^(t_v) (1/S_t - 1/S_d)
+    for v != token, i.e. proportional to p there, so the oracle draws the same winner."""
+    b, B, V = 16, 4, 5000
+    g = torch.Generator(device="cpu").manual_seed(31)
+    dl = torch.randn(b, B, V, generator=g)
+    tl = dl.clone()
+    toks = torch.randint(0, V, (b, B), generator=g, dtype=torch.int32)
+    for r in range(b):
+        for k in range(B):
+            dl[r, k, toks[r, k]] = -20.0
+            tl[r, k, toks[r, k]] = -30.0
+    tau = torch.tensor([3, 1, 4, 2], dtype=torch.int32)
+    labels = torch.cat([tau, tau + 128]).to(torch.uint8).repeat(b, 1)
+    res = oracle.accept(tl.numpy(), dl.numpy(), toks.numpy(), labels.numpy(), B, 1.0, 5, 0)
+    got, err = _accept_outputs(path, tl.cuda(), dl.cuda(), toks.cuda(), labels.cuda(), B, 1.0, 5)
+    assert (res["accepted_len"] < B).all()
+    H.check_accept(res, got, list(range(b)))
+    assert err == 0
+
+
+def test_accept_one_workspace_across_shapes():
+    """One workspace, zeroed once, serving calls of different shapes in a row (batch, B,
+    gamma and V all change, so every scratch region moves): each call against the oracle.
+    The per-request state is cleared by every call; only the barrier words at the head of
+    the workspace carry over."""
+    pkg = _pkg()
+    shapes = [(4, 4, 4, 5000), (16, 8, 6, 1000), (2, 32, 32, 30000), (24, 4, 3, 2048)]
+    need = max(pkg.simsd_accept_workspace(b, B, g, V) for b, B, g, V in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    gen = torch.Generator(device="cpu").manual_seed(41)
+    for i, (b, B, gamma, V) in enumerate(shapes):
+        tl = torch.randn(b, B, V, generator=gen)
+        dl = tl + 0.7 * torch.randn(b, B, V, generator=gen)
+        toks = torch.randint(0, V, (b, B), generator=gen, dtype=torch.int32)
+        tau = torch.stack([torch.randperm(B, generator=gen) + 1 for _ in range(b)]).to(torch.int32)
+        labels = torch.cat([tau, tau + 128], 1).to(torch.uint8)
+        res = oracle.accept(tl.numpy(), dl.numpy(), toks.numpy(), labels.numpy(), gamma, 1.0,
+                            100 + i, 0)
+        got, err = _accept_outputs("workspace", tl.cuda(), dl.cuda(), toks.cuda(), labels.cuda(),
+                                   gamma, 1.0, 100 + i, ws=ws)
+        H.check_accept(res, got, list(range(b)))
+        assert err == 0
 
 
 def test_accept_monte_carlo_commits_follow_target():
@@ -291,7 +381,7 @@ def test_accept_monte_carlo_commits_follow_target():
     ot = torch.empty(N, B, dtype=torch.int32, device="cuda")
     op = torch.empty_like(ot)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty(pkg.simsd_accept_workspace(N, B, B, V), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(pkg.simsd_accept_workspace(N, B, B, V), dtype=torch.uint8, device="cuda")
     pkg.simsd_accept(tl, dl, toks.cuda(), labels.cuda(), B, 1.0, 99, 0, al, ot, op, nc, ws, err)
     torch.cuda.synchronize()
     a = al.cpu().numpy()

@@ -2,9 +2,10 @@
 
 simsd_accept_noalloc exists for callers that cannot allocate device memory (plugin hosts
 that only hand over input/output buffers, runtimes that forbid allocation after start-up);
-it uses a fixed scratch array inside the library instead of a caller workspace. Its
-results must be identical to simsd_accept's, and stay so on consecutive calls that reuse
-the shared array. This file sorts last so that a stop-at-first-failure run has already
+it uses a fixed scratch array inside the library instead of a caller workspace, and runs
+the two-launch acceptance (stats, then finish), while simsd_accept runs the one-launch
+cluster kernel: two implementations of the same arithmetic. On random inputs their results
+must be identical, and stay so on consecutive calls that reuse the shared array. This file sorts last so that a stop-at-first-failure run has already
 run every other test when it gets here.
 """
 import numpy as np
@@ -39,7 +40,7 @@ def test_noalloc_accept_matches_workspace_accept_on_consecutive_calls():
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         pkg.simsd_build_layout(lay["tau"].to(dev), lay["prompt_len"].to(dev), pos, labels, err)
         ref = _outputs(b, B, dev)
-        ws = torch.empty(pkg.simsd_accept_workspace(b, B, w.gamma, w.V), dtype=torch.uint8,
+        ws = torch.zeros(pkg.simsd_accept_workspace(b, B, w.gamma, w.V), dtype=torch.uint8,
                          device=dev)
         pkg.simsd_accept(acc["target_logits"], acc["draft_logits"], acc["draft_tokens"], labels,
                          w.gamma, w.temperature, acc["philox_seed"], 0, ref["accepted_len"],
