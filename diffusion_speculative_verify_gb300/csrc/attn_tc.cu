@@ -257,7 +257,7 @@ struct PromptTiles {
 // --------------------------------------------------------------------- small helpers
 enum BarIdx { kFull0 = 0, kEmpty0 = kMaxStages, kSFull0 = 2 * kMaxStages, kSFree0 = kSFull0 + 2,
               kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kQFull = kPFree0 + 2, kDrain = kQFull + 1,
-              kNumBars = kDrain + 1 };
+              kLoads = kDrain + 1, kNumBars = kLoads + 1 };
 
 struct Shared {
   uint64_t bars[kNumBars];
@@ -1004,6 +1004,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       }
       ptx::mbar_init(bar(kQFull), 128);
       ptx::mbar_init(bar(kDrain), 1);
+      ptx::mbar_init(bar(kLoads), 128);
       ptx::fence_mbar_init();
       ptx::prefetch_tensormap(&tmk);
       ptx::prefetch_tensormap(&tmv);
@@ -1035,6 +1036,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       int h, tok;
       while (tiles.next(a, h, tok)) {
         const int s = m % kStages;
+        // the first prologue's global loads are issued before the prompt stream, so that
+        // they are not queued behind it (the first tile the MMA issuer needs is the tail
+        // tile, which the prologue builds in shared memory)
+        if (m == 0) {
+          ok = wait_bar(sh, bar(kLoads), 0, a.dev_err);
+          if (!ok) break;
+        }
         ok = wait_bar(sh, bar(kEmpty0 + s), ((m / kStages) & 1) ^ 1, a.dev_err);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
@@ -1193,6 +1201,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     it.init(a, st);
     uint32_t j = 0;
     bool ok = true;
+    bool loads_signalled = false;  // each thread arrives on kLoads once
     MergeDesc desc;
     desc.b = -1;
     desc.T = st.T;
@@ -1220,55 +1229,98 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       const int P = a.prompt_len[b];
       const bool has_tail = it.has_tail;
       // ---- prologue: rotated + scaled Q rows into TMEM, rotated tail K and plain tail V
-      // tiles. The Q row, labels and positions are loaded together and the tail rows are
-      // prefetched into L2 at the same time, so only one wait goes to DRAM.
-      const int key = tid & 63;
-      const bool tail_row = has_tail && key < twoB;
+      // tiles. Each thread holds at most one row. When the warps beyond the pair's rows can
+      // take the 2 * 2B tail rows ("early"), those load them together with the Q rows, so
+      // the prologue waits on memory once; otherwise the tail rows are prefetched into L2
+      // with the Q loads and loaded once Q is in TMEM.
+      const int rw = (a.R + 31) & ~31;  // threads below rw own the pair's (padded) rows
+      const bool early = has_tail && 128 - rw >= 2 * twoB;
+      int key;
+      bool tail_row, tail_k;
+      if (early) {
+        const int e = tid - rw;
+        tail_row = e >= 0 && e < 2 * twoB;
+        tail_k = e < twoB;
+        key = tail_k ? e : e - twoB;
+      } else {
+        key = tid & 63;
+        tail_row = has_tail && key < twoB;
+        tail_k = tid < 64;
+      }
       uint4 v[16];
       const __nv_bfloat16* trow =
-          (tid < 64 ? a.k_resp : a.v_resp) + (((size_t)b * twoB + key) * a.Hkv + h) * kD;
-      if (tail_row) {  // into L2 now, into registers once Q is in TMEM
+          (tail_k ? a.k_resp : a.v_resp) + (((size_t)b * twoB + (tail_row ? key : 0)) * a.Hkv + h) * kD;
+      if (warp_active) {
+        if (real) load_row(v, a.q + orow * kD);
+      } else if (early && tail_row) {
+        load_row(v, trow);
+      }
+      if (!early && tail_row) {  // into L2 now, into registers once Q is in TMEM
         asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
       }
-      if (warp_active && real) load_row(v, a.q + orow * kD);
+      uint8_t lab_r = 0;
+      int pos_r = 0;
       if (tid < twoB) {
-        sh->lab[tid] = a.labels[(size_t)b * twoB + tid];
-        sh->pos[tid] = a.pos_ids[(size_t)b * twoB + tid];
+        lab_r = a.labels[(size_t)b * twoB + tid];
+        pos_r = a.pos_ids[(size_t)b * twoB + tid];
+      }
+      if (!loads_signalled) {  // the loads above are issued: the prompt stream may follow
+        ptx::mbar_arrive(bar(kLoads));
+        loads_signalled = true;
+      }
+      if (tid < twoB) {
+        sh->lab[tid] = lab_r;
+        sh->pos[tid] = pos_r;
       }
       ptx::named_bar_sync(1, 128);
       // (cos, sin) of the 2B response positions, over the tail K and V area (2B <= 64:
-      // at most 32 KB); the tail rows are stored once every read of the table is done
+      // at most 32 KB); the tail rows are stored once every read of the table is done. Rows
+      // are 66 float2 apart where that fits (16 bytes of padding: threads reading different
+      // positions' rows then hit different banks), else 64.
       float2* rtab = reinterpret_cast<float2*>(tailk);
+      const int tstride = twoB * 66 * 8 <= (int)(2 * kTailKV) ? 66 : 64;
       for (int e = tid; e < twoB * 64; e += 128) {
         const int sidx = e >> 6, d = e & 63;
         float sn, cs;
         rope_sincos(sh->pos[sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
-        rtab[e] = make_float2(cs, sn);
+        rtab[sidx * tstride + d] = make_float2(cs, sn);
       }
       ptx::named_bar_sync(1, 128);
       if (warp_active) {
         if (real) {
-          rope_row(v, rtab + s_slot * 64, a.scale_log2);
+          rope_row(v, rtab + s_slot * tstride, a.scale_log2);
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
         // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
         tmem_st_row(tmem + lane_off + kTmemQ, v);
+        ptx::tmem_st_wait();
+      } else if (early && tail_row && tail_k) {
+        rope_row(v, rtab + key * tstride, 1.f);  // K rotated, V as is
       }
-      ptx::tmem_st_wait();
-      if (has_tail) {
+      if (!early && has_tail) {
         if (tail_row) {
           load_row(v, trow);
-          if (tid < 64) rope_row(v, rtab + key * 64, 1.f);  // K rotated, V as is
+          if (tail_k) rope_row(v, rtab + key * tstride, 1.f);  // K rotated, V as is
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
       }
       ptx::named_bar_sync(1, 128);  // table reads done
-      if (has_tail) store_row_sw(tid < 64 ? tailk : tailv, kTailHalf, key, v);
+      if (early) {
+        if (tail_row) store_row_sw(tail_k ? tailk : tailv, kTailHalf, key, v);
+        // keys 2B .. 63 of both tail tiles are zero (the tail MMAs read 64 keys)
+        const uint4 z[16] = {};
+        for (int e = tid; e < 2 * (64 - twoB); e += 128) {
+          const int zk = twoB + e % (64 - twoB);
+          store_row_sw(e < 64 - twoB ? tailk : tailv, kTailHalf, zk, z);
+        }
+      } else if (has_tail) {
+        store_row_sw(tail_k ? tailk : tailv, kTailHalf, key, v);
+      }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kQFull));
@@ -1428,6 +1480,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       it.advance(a);
     }
     if (tid == 0) a.ws_desc[blockIdx.x] = desc;
+    if (!loads_signalled) ptx::mbar_arrive(bar(kLoads));  // no prologue ran: release the producer
   }
 
   ptx::tc_fence_before();
