@@ -92,7 +92,8 @@ struct Cfg {
 };
 
 struct TcArgs {
-  int batch, B, Hq, Hkv, G, R, nrb, ctas;  // R = 2B*G real rows per pair
+  int batch, B, Hq, Hkv, G, R, nrb, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
+  int cl;                                  // CTAs per schedule unit (a cluster): 1, or 2 when R > 128
   int tile_keys;                           // prompt keys per tile (64 or 128)
   int layout;
   const __nv_bfloat16* q;
@@ -983,9 +984,16 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   // kPFull0 + b: P of the tile in S buffer b written. kSFree0 + b: the P V that read S
   // buffer b completed; its phase for tile j is j / 2, and the previous phase (tile j - 2) is
   // always complete by the time anyone waits for tile j, so a parity wait is unambiguous.
+  // Pairs of more than 128 rows: a cluster of two CTAs takes each schedule unit, CTA `crank`
+  // the rows [128 crank, 128 crank + 128); each prompt tile is loaded once, half by each
+  // CTA, multicast into both, and a stage is refilled once both CTAs have released it.
+  const int cl = a.cl;
+  const int vcta = blockIdx.x / cl, crank = blockIdx.x - vcta * cl;
+  const uint16_t cmask = (uint16_t)((1u << cl) - 1u);
+  const int row0 = crank * 128;  // first pair row of this CTA
 
   if (warp == kProducerWarp) {
-    const SchedStart s = warp_schedule(a, blockIdx.x, a.ctas, lane);
+    const SchedStart s = warp_schedule(a, vcta, a.ctas, lane);
     if (lane == 0) {
       sh->T = s.T;
       sh->t0 = s.t0;
@@ -995,7 +1003,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       sh->abort = 0;
       for (int i = 0; i < kStages; ++i) {
         ptx::mbar_init(bar(kFull0 + i), 1);
-        ptx::mbar_init(bar(kEmpty0 + i), 1);
+        ptx::mbar_init(bar(kEmpty0 + i), (uint32_t)cl);
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(bar(kSFull0 + i), 1);
@@ -1015,6 +1023,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (cl > 1) ptx::cluster_sync_all();  // the peer's barriers are initialised before any use
   ptx::tc_fence_after();
 
   SchedStart st;
@@ -1048,14 +1057,26 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
         const uint32_t kdst = sbase + kOffStages + s * kStage;
         const uint32_t vdst = kdst + kKV;
+        if (cl == 1) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (a.layout == SIMSD_CACHE_NHD) {
-            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
-          } else {
-            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
+          for (int half = 0; half < 2; ++half) {
+            if (a.layout == SIMSD_CACHE_NHD) {
+              ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
+              ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
+            } else {
+              ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
+              ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
+            }
+          }
+        } else {  // this CTA's half of the tile (K for rank 0, V for rank 1), into both CTAs
+          const CUtensorMap* map = crank == 0 ? &tmk : &tmv;
+          const uint32_t dst = crank == 0 ? kdst : vdst;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (a.layout == SIMSD_CACHE_NHD)
+              ptx::tma_load_3d_mc(dst + half * kHalf, map, half * 64, h, tok, bar(kFull0 + s), cmask);
+            else
+              ptx::tma_load_3d_mc(dst + half * kHalf, map, half * 64, tok, h, bar(kFull0 + s), cmask);
           }
         }
         ++m;
@@ -1122,7 +1143,12 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
                           ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV,
                           (first_in_seg && kk == 0) ? 0u : 1u);
         ptx::mma_commit(bar(kSFree0 + buf));
-        if (s >= 0) ptx::mma_commit(bar(kEmpty0 + s));
+        if (s >= 0) {
+          if (cl == 1)
+            ptx::mma_commit(bar(kEmpty0 + s));
+          else
+            ptx::mma_commit_mc(bar(kEmpty0 + s), cmask);  // the stage is free in both CTAs' eyes
+        }
         return true;
       };
       while (ok && it.next(a)) {
@@ -1189,11 +1215,12 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax warps
-    const int row = warp * 32 + lane;  // TMEM lane = row within the pair
-    const bool real = row < a.R;
-    const bool warp_active = warp * 32 < a.R;  // warp-uniform: some row of this warp is real
-    const int s_slot = real ? row / a.G : 0;
-    const int g = real ? row % a.G : 0;
+    const int row = warp * 32 + lane;  // TMEM lane = row within this CTA's block
+    const int prow = row0 + row;       // row within the pair
+    const bool real = prow < a.R;
+    const bool warp_active = row0 + warp * 32 < a.R;  // warp-uniform: some row of this warp is real
+    const int s_slot = real ? prow / a.G : 0;
+    const int g = real ? prow % a.G : 0;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint8_t* tailk = smem + kOffTail;
     uint8_t* tailv = tailk + kTailKV;
@@ -1233,7 +1260,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       // take the 2 * 2B tail rows ("early"), those load them together with the Q rows, so
       // the prologue waits on memory once; otherwise the tail rows are prefetched into L2
       // with the Q loads and loaded once Q is in TMEM.
-      const int rw = (a.R + 31) & ~31;  // threads below rw own the pair's (padded) rows
+      const int rw = (min(128, a.R - row0) + 31) & ~31;  // threads below rw own this block's rows
       const bool early = has_tail && 128 - rw >= 2 * twoB;
       int key;
       bool tail_row, tail_k;
@@ -1487,6 +1514,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (cl > 1) ptx::cluster_sync_all();  // no CTA leaves while its peer may still signal it
 }
 
 // Merges the pieces of every pair split between CTAs. Block (c, y) reads CTA c's merge
@@ -1494,29 +1522,33 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 // one thread per (row, 4 output elements), so every load is independent.
 template <int NRB>
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
-  const int c = blockIdx.x;
+  const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
   const MergeDesc d = a.ws_desc[c];
   if (d.b < 0) return;
-  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int cl = a.cl;
+  const int vc = c / cl, crank = c - vc * cl;
+  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the CTA's block
+  const int prow = crank * 128 + row;                    // row within the pair
   const int quad = threadIdx.x & 31;
-  if (row >= a.R) return;
+  if (row >= NRB * kBlockRows || prow >= a.R) return;
   const int64_t T = d.T;
   const int C = a.ctas;
   const size_t stride = (size_t)NRB * kBlockRows;
-  // pieces: CTA c (slot0) and every later non-empty CTA up to c_last (its first slot)
+  // pieces: unit vc (slot0) and every later non-empty unit up to c_last (its first slot),
+  // each in the CTA of the same row block
   float mmax = -INFINITY;
 #pragma unroll 4
-  for (int cc = c; cc <= d.c_last; ++cc) {
-    if (cc > c && cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;
-    const int slot = (cc == c) ? d.slot0 : 2 * cc;
+  for (int vcc = vc; vcc <= d.c_last; ++vcc) {
+    if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
+    const int slot = (vcc == vc) ? d.slot0 : 2 * (vcc * cl + crank);
     mmax = fmaxf(mmax, a.ws_ml[(size_t)slot * stride + row].x);
   }
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int cc = c; cc <= d.c_last; ++cc) {
-    if (cc > c && cta_begin(T, C, cc) == cta_begin(T, C, cc + 1)) continue;
-    const int slot = (cc == c) ? d.slot0 : 2 * cc;
+  for (int vcc = vc; vcc <= d.c_last; ++vcc) {
+    if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
+    const int slot = (vcc == vc) ? d.slot0 : 2 * (vcc * cl + crank);
     const float2 ml = a.ws_ml[(size_t)slot * stride + row];
     const float4 o = reinterpret_cast<const float4*>(a.ws_o + ((size_t)slot * stride + row) * kD)[quad];
     const float w = exp2f(ml.x - mmax);
@@ -1527,7 +1559,7 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
     acc.w += w * o.w;
   }
   const float inv = 1.f / L;
-  const int s_slot = row / a.G, g = row % a.G;
+  const int s_slot = prow / a.G, g = prow % a.G;
   const size_t orow = ((size_t)d.b * 2 * a.B + s_slot) * a.Hq + (size_t)d.h * a.G + g;
   uint2 pk;
   pk.x = pack_bf16(acc.x * inv, acc.y * inv);
@@ -1589,14 +1621,18 @@ static int rows_per_pair(const simsd_attn_params* p) { return 2 * p->B * (p->Hq 
 
 // Persistent grid: one CTA per SM; when every (request, kv head) pair fits on the SMs and
 // prompts are short, one CTA per pair instead (no pair is split, nothing to merge).
-static int grid_ctas(const simsd_attn_params* p) {
+// (With `cl` CTAs per unit: at most SMs / cl units.)
+static int grid_ctas(const simsd_attn_params* p, int cl = 1) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 148;
+  sms /= cl;
   const int64_t pairs = (int64_t)p->batch * p->Hkv;
   const int64_t avg_tiles = 1 + (p->batch > 0 ? (p->cache_tokens / p->batch + kTileKeys - 1) / kTileKeys : 0);
   if (pairs > 0 && pairs <= sms && avg_tiles <= 64) return (int)pairs;
   return sms;
 }
+// CTAs per schedule unit: a cluster of two for pairs of more than 128 rows.
+static int cluster_size(const simsd_attn_params* p) { return rows_per_pair(p) > 128 ? 2 : 1; }
 
 struct WsLayout {
   size_t o, ml, desc, bytes;
@@ -1622,7 +1658,8 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.R = rows_per_pair(p);
   a.nrb = NRB;
   a.tile_keys = NRB == 1 ? r128::kKeys : kTileKeys;
-  a.ctas = grid_ctas(p);
+  a.cl = NRB == 1 ? cluster_size(p) : 1;
+  a.ctas = grid_ctas(p, a.cl);
   a.layout = (int)p->cache_layout;
   a.q = (const __nv_bfloat16*)p->q;
   a.k_resp = (const __nv_bfloat16*)p->k_resp;
@@ -1636,7 +1673,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.out = (__nv_bfloat16*)p->out;
   a.lse = p->lse;
   a.dev_err = p->dev_err;
-  const WsLayout wl = ws_layout(a.ctas, NRB);
+  const WsLayout wl = ws_layout(a.ctas * a.cl, NRB);
   if (!ws || ws_bytes < wl.bytes || (((uintptr_t)ws) & 255)) return SIMSD_ERR_WORKSPACE;
   a.ws_o = (float*)((char*)ws + wl.o);
   a.ws_ml = (float2*)((char*)ws + wl.ml);
@@ -1668,11 +1705,25 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
     }
     attr_done[dev][NRB] = 1;
   }
-  if (NRB == 1)
-    attn_tc128_kernel<<<a.ctas, threads, smem_bytes, stream>>>(tmk, tmv, a);
-  else
+  cudaError_t le = cudaSuccess;
+  if (NRB == 1) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)a.cl;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = a.cl > 1 ? 1 : 0;
+    le = cudaLaunchKernelEx(&cfg, attn_tc128_kernel, tmk, tmv, a);
+  } else {
     attn_tc_kernel<NRB><<<a.ctas, threads, smem_bytes, stream>>>(tmk, tmv, a);
-  const cudaError_t le = cudaGetLastError();
+  }
+  if (le == cudaSuccess) le = cudaGetLastError();
   if (le != cudaSuccess) {
     cudaFuncAttributes fa;
     char what[200] = "attention kernel launch";
@@ -1685,7 +1736,8 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
     record_cuda_error(what, le);
     return SIMSD_ERR_CUDA;
   }
-  const dim3 mgrid(a.ctas, (a.R + 7) / 8);  // blocks without a split pair exit at once
+  // blocks without a split pair exit at once
+  const dim3 mgrid((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, NRB * kBlockRows) + 7) / 8));
   attn_tc_merge_kernel<NRB><<<mgrid, 256, 0, stream>>>(a);
   return last_launch_status();
 }
@@ -1701,8 +1753,8 @@ bool attn_tc_supported(const simsd_attn_params* p) {
 }
 
 size_t attn_tc_workspace(const simsd_attn_params* p) {
-  const int nrb = tc::rows_per_pair(p) > 128 ? 2 : 1;
-  return tc::ws_layout(tc::grid_ctas(p), nrb).bytes;
+  const int cl = tc::cluster_size(p);
+  return tc::ws_layout(tc::grid_ctas(p, cl) * cl, 1).bytes;
 }
 
 simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_bytes,
@@ -1713,7 +1765,7 @@ simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_byte
     return SIMSD_ERR_UNSUPPORTED;
   if (p->cache_tokens > 0 && ((((uintptr_t)p->k_cache) | ((uintptr_t)p->v_cache)) & mask))
     return SIMSD_ERR_UNSUPPORTED;
-  if (tc::rows_per_pair(p) > 128) return tc::launch<2>(p, ws, ws_bytes, stream);
+  // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: a cluster of two
   return tc::launch<1>(p, ws, ws_bytes, stream);
 }
 
