@@ -6,26 +6,28 @@
 // the response queries/keys at the copied position ids.
 //
 // Work decomposition. For each (request b, kv head h) the 2B*G query rows (response slot
-// s, head g of the group; row = s*G + g) form one or two 128-row blocks; a "pair" is
-// (b, h, all row blocks). Each pair is a sequence of 64-key tiles: tile 0 is the response
-// tail (the 2B response keys, rotated and masked here), tiles 1.. stream the prompt keys.
-// All pairs' tiles are concatenated and cut into equal contiguous ranges, one per
-// persistent CTA (stream-K); a CTA therefore sees at most two partial pairs (its first
-// and last), whose (O, max, sum) partials are merged by attn_tc_merge_kernel.
+// s, head g of the group; row = s*G + g) form a "pair". Each pair is a sequence of tiles:
+// tile 0 is the response tail (the 2B response keys, rotated and masked here), tiles 1..
+// stream the prompt keys, 128 at a time. All pairs' tiles are concatenated and cut into
+// equal contiguous ranges, one per schedule unit (stream-K); a unit therefore sees at
+// most two partial pairs (its first and last), whose (O, max, sum) partials are merged by
+// attn_tc_merge_kernel. A unit is one CTA for pairs of up to 128 rows and a cluster of two
+// CTAs (rows [0, 128) and [128, 256)) above that; the two load each prompt tile once,
+// half each, multicast into both.
 //
 // Per CTA, warp roles:
 //   producer warp  : TMA loads of prompt K and V tiles (128-byte swizzle) into a ring of
-//                    shared-memory stages.
-//   MMA warp       : one thread issues S = Q K^T (M = 128 rows, N = 64 keys, K = 128) into
-//                    one of two TMEM S buffers, then O += P V (M = 128, N = 128, K = 64)
-//                    into the TMEM O accumulator; completion is signalled with
-//                    tcgen05.commit to mbarriers.
+//                    three 64 KB shared-memory stages.
+//   MMA warp       : one thread issues S = Q K^T (M = 128 rows, N = 128 keys, K = 128; A =
+//                    the rotated Q in TMEM) into one of two TMEM S buffers, then O += P V
+//                    (M = 128, N = 128, K = 128 keys; A = bf16 P in TMEM) into the TMEM O
+//                    accumulator; completion is signalled with tcgen05.commit to mbarriers.
 //   softmax warps  : one thread per query row (TMEM lane). Per segment: load + rotate Q
-//                    into shared memory (and the response K/V tail tile); per tile: read
-//                    S from TMEM, apply the mask, online softmax in the log2 domain with
-//                    lazy rescaling of O (only when the running max grows by > 8), write P
-//                    (bf16) to shared memory; epilogue: O / l to global memory (or the
-//                    partial to the workspace).
+//                    into TMEM and build the response K/V tail tile; per tile: read S from
+//                    TMEM, apply the mask, and write P = 2^(s - m) (bf16) in place over the
+//                    S columns just read, in one pass unless the running max grows by more
+//                    than 2^8 (then O and the P already written are rescaled); epilogue:
+//                    O / l to global memory (or the partial to the workspace).
 // Every wait is bounded in time; on expiry the kernel raises SIMSD_DEVERR_TIMEOUT in the
 // error word and unwinds (no trap).
 #include <cuda.h>
@@ -44,55 +46,12 @@ namespace tc {
 constexpr int kTileKeys = 64;
 constexpr int kD = 128;
 constexpr int kBlockRows = 128;
-constexpr uint32_t kHalfTile = kTileKeys * 128;       // 64 rows x 128 B (one 64-element half)
-constexpr uint32_t kKVTile = 2 * kHalfTile;           // 16 KB: one K (or V) tile
-constexpr uint32_t kStageBytes = 2 * kKVTile;         // K + V
-constexpr uint32_t kQBlock = 2 * kBlockRows * 128;    // 32 KB: 128 rows x 128 dims
-constexpr uint32_t kPBlock = kBlockRows * 128;        // 16 KB: 128 rows x 64 keys
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
-#ifndef SIMSD_L2_PREFETCH_TILES
-#define SIMSD_L2_PREFETCH_TILES 0
-#endif
-constexpr uint32_t kPrefetchTiles = SIMSD_L2_PREFETCH_TILES;  // L2 prefetch distance beyond the ring
 constexpr int kMaxStages = 8;                         // stage barriers reserved in shared memory
 
-// NRB = 1: up to 128 query rows per pair; the two softmax warpgroups split each row's 64
-//          key columns (32 each) and keep separate O accumulators, merged at the end.
-// NRB = 2: up to 256 rows; warpgroup w owns row block w and all 64 columns.
-template <int NRB>
-struct Cfg {
-  static constexpr bool kSplitCols = NRB == 1;
-  // NRB = 1 keeps the rotated Q in TMEM and issues S = Q K^T with A from TMEM (a
-  // shared-memory A operand costs a fixed ~70 cycles per M=128 K=16 instruction, TMEM ~45)
-  static constexpr bool kQInTmem = NRB == 1;
-  static constexpr int kCols = kSplitCols ? 32 : 64;  // S columns per softmax thread
-  static constexpr int kStages = NRB == 1 ? 5 : 2;
-  // S is issued this many tiles ahead of P V; tiles jj .. jj + kSAhead hold stages until
-  // P V of tile jj completes, so kSAhead <= kStages - 1 keeps the producer able to refill
-  static constexpr int kSAhead = kStages - 1;
-  static_assert(kSAhead >= 1 && kSAhead <= kStages - 1, "lookahead vs stages");
-  static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;
-  static constexpr int kThreads = kSoftmaxThreads + 64;
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffP = kOffQ + (kQInTmem ? 0 : NRB * kQBlock);  // [rb][buf]
-  static constexpr uint32_t kOffStages = kOffP + NRB * 2 * kPBlock;
-  static constexpr uint32_t kOffTail = kOffStages + kStages * kStageBytes;
-  static constexpr uint32_t kOffBar = kOffTail + kStageBytes;
-  static constexpr uint32_t kBarBytes = 1024;
-  static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + base alignment
-  // TMEM columns: S buffers [rb][buf] x 64, two 128-column O accumulators, then (NRB = 1)
-  // the rotated Q as bf16 pairs (64 columns)
-  static constexpr uint32_t tmem_s(int rb, int buf) { return (uint32_t)(rb * 2 + buf) * 64u; }
-  static constexpr uint32_t tmem_o(int idx) { return (uint32_t)NRB * 128u + (uint32_t)idx * 128u; }
-  static constexpr uint32_t kTmemQ = 384;
-  static_assert(kStages <= kMaxStages, "stage barriers");
-};
 
 struct TcArgs {
-  int batch, B, Hq, Hkv, G, R, nrb, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
+  int batch, B, Hq, Hkv, G, R, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
   int cl;                                  // CTAs per schedule unit (a cluster): 1, or 2 when R > 128
   int tile_keys;                           // prompt keys per tile (64 or 128)
   int layout;
@@ -107,8 +66,8 @@ struct TcArgs {
   __nv_bfloat16* out;
   float* lse;
   uint32_t* dev_err;
-  float* ws_o;     // [2 * ctas][nrb * 128][128] partial numerators
-  float2* ws_ml;   // [2 * ctas][nrb * 128] partial (max, sum), log2 domain
+  float* ws_o;     // [2 * CTAs][128][128] partial numerators
+  float2* ws_ml;   // [2 * CTAs][128] partial (max, sum), log2 domain
   struct MergeDesc* ws_desc;  // [ctas] split pair starting in each CTA (or none)
   RopeTable rope;
 };
@@ -391,551 +350,6 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]
     }
     ptx::tmem_st32(taddr + 32 * half, w);
   }
-}
-
-// ------------------------------------------------------------------------- the kernel
-template <int NRB>
-__global__ void __launch_bounds__(Cfg<NRB>::kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   const __grid_constant__ TcArgs a) {
-  using C = Cfg<NRB>;
-  static_assert(sizeof(Shared) <= C::kBarBytes, "barrier area");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  Shared* sh = reinterpret_cast<Shared*>(smem + C::kOffBar);
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t sbase = ptx::smem_u32(smem);
-  auto bar = [&](int i) { return ptx::smem_u32(&sh->bars[i]); };
-
-  if (warp == C::kProducerWarp) {
-    const SchedStart s = warp_schedule(a, blockIdx.x, a.ctas, lane);
-    if (lane == 0) {
-      sh->T = s.T;
-      sh->t0 = s.t0;
-      sh->t1 = s.t1;
-      sh->Tb = s.Tb;
-      sh->b = s.b;
-      sh->abort = 0;
-      for (int i = 0; i < C::kStages; ++i) {
-        ptx::mbar_init(bar(kFull0 + i), 1);
-        ptx::mbar_init(bar(kEmpty0 + i), 1);
-      }
-      for (int i = 0; i < 2; ++i) {
-        ptx::mbar_init(bar(kSFull0 + i), 1);
-        ptx::mbar_init(bar(kSFree0 + i), C::kSoftmaxThreads);
-        ptx::mbar_init(bar(kPFull0 + i), C::kSoftmaxThreads);
-        ptx::mbar_init(bar(kPFree0 + i), 1);
-      }
-      ptx::mbar_init(bar(kQFull), C::kSoftmaxThreads);
-      ptx::mbar_init(bar(kDrain), 1);
-      ptx::fence_mbar_init();
-      ptx::prefetch_tensormap(&tmk);
-      ptx::prefetch_tensormap(&tmv);
-    }
-  } else if (warp == C::kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), C::kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-
-  SchedStart st;
-  st.T = sh->T;
-  st.t0 = sh->t0;
-  st.t1 = sh->t1;
-  st.Tb = sh->Tb;
-  st.b = sh->b;
-  const uint32_t tmem = sh->tmem_base;
-  const int twoB = 2 * a.B;
-
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      PromptTiles tiles, ahead;
-      tiles.init(a, st);
-      ahead.init(a, st);
-      uint32_t m = 0, prefetched = 0;
-      bool ok = true;
-      int h, tok;
-      while (ok && tiles.next(a, h, tok)) {
-        // keep the L2 warm kPrefetchTiles tiles beyond the shared-memory ring
-        int hp, tp;
-        while (kPrefetchTiles > 0 && prefetched <= m + C::kStages + kPrefetchTiles &&
-               ahead.next(a, hp, tp)) {
-          if (prefetched >= (uint32_t)C::kStages) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              if (a.layout == SIMSD_CACHE_NHD) {
-                ptx::tma_prefetch_l2_3d(&tmk, half * 64, hp, tp);
-                ptx::tma_prefetch_l2_3d(&tmv, half * 64, hp, tp);
-              } else {
-                ptx::tma_prefetch_l2_3d(&tmk, half * 64, tp, hp);
-                ptx::tma_prefetch_l2_3d(&tmv, half * 64, tp, hp);
-              }
-            }
-          }
-          ++prefetched;
-        }
-        const int s = m % C::kStages;
-        ok = wait_bar(sh, bar(kEmpty0 + s), ((m / C::kStages) & 1) ^ 1, a.dev_err);
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStageBytes);
-        const uint32_t kdst = sbase + C::kOffStages + s * kStageBytes;
-        const uint32_t vdst = kdst + kKVTile;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (a.layout == SIMSD_CACHE_NHD) {
-            ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, h, tok, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, h, tok, bar(kFull0 + s));
-          } else {
-            ptx::tma_load_3d(kdst + half * kHalfTile, &tmk, half * 64, tok, h, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalfTile, &tmv, half * 64, tok, h, bar(kFull0 + s));
-          }
-        }
-        ++m;
-      }
-      if (!ok) {  // let the loads already issued land before shared memory goes away
-        const uint32_t issued = m;
-        for (uint32_t k = issued > (uint32_t)C::kStages ? issued - C::kStages : 0; k < issued; ++k) {
-          const uint64_t t_start = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(bar(kFull0 + k % C::kStages), (k / C::kStages) & 1) &&
-                 ptx::globaltimer_ns() - t_start < 100000000ull) {
-          }
-        }
-      }
-    }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = ptx::idesc_bf16(128, kTileKeys, 0, 0);
-      constexpr uint32_t idPV = ptx::idesc_bf16(128, kD, 0, 1);
-      SegIter it;
-      it.init(a, st);
-      uint32_t j = 0, m = 0, nseg = 0;
-      bool ok = true;
-      // per tile (ring of 8 >= kSAhead + 1 tiles between the oldest pending P V and the
-      // newest S): where its V lives and which stage its P V releases
-      uint32_t vaddr_of[8];
-      int stage_of[8];
-      static_assert(C::kSAhead + 1 <= 8, "tile ring");
-      // S_jj = Q K_jj^T into S buffer jj % 2 (free once the softmax has read S_{jj-2}).
-      // Non-blocking: returns false (and issues nothing) while K_jj or the buffer is busy.
-      auto try_issue_s = [&](uint32_t jj, int i) -> bool {
-        const int buf = jj & 1;
-        const int s = m % C::kStages;
-        if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / C::kStages) & 1)) return false;
-        if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj >> 1) & 1) ^ 1)) return false;
-        uint32_t kaddr;
-        if (i == 0) {
-          kaddr = sbase + C::kOffTail;
-          stage_of[jj & 7] = -1;
-        } else {
-          kaddr = sbase + C::kOffStages + s * kStageBytes;
-          stage_of[jj & 7] = s;
-          ++m;
-        }
-        vaddr_of[jj & 7] = kaddr + kKVTile;
-        ptx::tc_fence_after();
-        if constexpr (C::kQInTmem) {
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
-            ptx::mma_f16_ts(tmem + C::tmem_s(0, buf), tmem + C::kTmemQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
-          }
-        } else {
-#pragma unroll
-          for (int rb = 0; rb < NRB; ++rb) {
-            const uint32_t qbase = sbase + C::kOffQ + rb * kQBlock;
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * (kBlockRows * 128) + (kk & 3) * 32;
-              const uint64_t ad = ptx::sdesc_sw128(qbase + koff, 16, 1024);
-              const uint64_t bd = ptx::sdesc_sw128(kaddr + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
-              ptx::mma_f16_ss(tmem + C::tmem_s(rb, buf), ad, bd, idS, kk > 0 ? 1u : 0u);
-            }
-          }
-        }
-        ptx::mma_commit(bar(kSFull0 + buf));
-        return true;
-      };
-      // O (+)= P_jj V_jj once the softmax has written P_jj. Non-blocking like try_issue_s.
-      auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
-        const int buf = jj & 1;
-        if (!ptx::mbar_test(bar(kPFull0 + buf), (jj >> 1) & 1)) return false;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int rb = 0; rb < NRB; ++rb) {
-          const uint32_t pbase = sbase + C::kOffP + (rb * 2 + buf) * kPBlock;
-#pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-            // key slice kk (16 keys) of P and V; with split columns, keys 0-31 feed O[0]
-            // and keys 32-63 feed O[1]
-            const int oidx = C::kSplitCols ? (kk >> 1) : rb;
-            const bool first_k = C::kSplitCols ? ((kk & 1) == 0) : (kk == 0);
-            const uint64_t ad = ptx::sdesc_sw128(pbase + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(vaddr_of[jj & 7] + kk * 16 * 128, kHalfTile, 1024);
-            ptx::mma_f16_ss(tmem + C::tmem_o(oidx), ad, bd, idPV, (first_in_seg && first_k) ? 0u : 1u);
-          }
-        }
-        ptx::mma_commit(bar(kPFree0 + buf));
-        if (stage_of[jj & 7] >= 0) ptx::mma_commit(bar(kEmpty0 + stage_of[jj & 7]));
-        return true;
-      };
-      while (ok && it.next(a)) {
-        if (it.invalid) {
-          it.advance(a);
-          continue;
-        }
-        ok = wait_bar(sh, bar(kQFull), nseg & 1, a.dev_err);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        // Event loop over the segment's tiles: P V of the oldest tile is issued as soon as
-        // its P is ready (it frees a stage), S of the next tile as soon as its K has landed
-        // and its S buffer is free; S may run up to kSAhead tiles ahead of P V.
-        constexpr uint32_t A = C::kSAhead;
-        const uint32_t jfirst = j, jend = j + (uint32_t)it.n;
-        uint32_t ns = jfirst, npv = jfirst;
-        uint64_t t_idle = 0;
-        uint32_t spins = 0;
-        while (npv < jend) {
-          bool progressed = false;
-          if (npv < ns && try_issue_pv(npv, npv == jfirst)) {
-            ++npv;
-            progressed = true;
-          }
-          if (ns < jend && ns <= npv + A && try_issue_s(ns, it.i0 + (int)(ns - jfirst))) {
-            ++ns;
-            progressed = true;
-          }
-          if (progressed) {
-            spins = 0;
-            continue;
-          }
-          if ((++spins & 63) == 0) {  // bounded: give up after kWaitLimitNs without progress
-            const uint64_t now = ptx::globaltimer_ns();
-            if (spins == 64) t_idle = now;
-            if (*(volatile int*)&sh->abort || now - t_idle > kWaitLimitNs) {
-              if (!*(volatile int*)&sh->abort) {
-                *(volatile int*)&sh->abort = 1;
-                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
-              }
-              ok = false;
-              break;
-            }
-          }
-        }
-        if (!ok) break;
-        j = jend;
-        ++nseg;
-        it.advance(a);
-      }
-      // drain: every MMA issued so far has completed before TMEM is released
-      ptx::mma_commit(bar(kDrain));
-      const uint64_t t_start = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar(kDrain), 0) &&
-             ptx::globaltimer_ns() - t_start < 100000000ull) {
-      }
-    }
-  } else {
-    // -------------------------------------------------------------- softmax warps
-    constexpr int NC = C::kCols;
-    const int wg = warp >> 2;                       // softmax warpgroup 0 / 1
-    const int rb = C::kSplitCols ? 0 : wg;          // row block
-    const int col0 = C::kSplitCols ? 32 * wg : 0;   // first S column of this thread
-    const int oidx = C::kSplitCols ? wg : rb;       // O accumulator
-    const int lrow = (warp & 3) * 32 + lane;        // TMEM lane = row within the block
-    const int row = rb * kBlockRows + lrow;         // row within the pair
-    const bool real = row < a.R;
-    const int s_slot = real ? row / a.G : 0;
-    const int g = real ? row % a.G : 0;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    uint8_t* qtile = smem + C::kOffQ + rb * kQBlock;
-    uint8_t* tailk = smem + C::kOffTail;
-    uint8_t* tailv = tailk + kKVTile;
-    const bool q_writer = !C::kSplitCols || wg == 0;
-    const bool tail_writer = C::kSplitCols ? (wg == 1) : (wg == 0);
-    SegIter it;
-    it.init(a, st);
-    uint32_t j = 0;
-    bool ok = true;
-    MergeDesc desc;
-    desc.b = -1;
-    desc.T = st.T;
-    while (ok && it.next(a)) {
-      const int b = it.b, h = it.h;
-      if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
-        const int64_t pe = it.t + it.nt;
-        desc.b = b;
-        desc.h = h;
-        desc.c_last = (int)((pe * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
-        desc.slot0 = 2 * blockIdx.x + (it.first ? 0 : 1);
-      }
-      const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
-      if (it.invalid) {
-        if (real && q_writer) {
-          uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
-          if (a.lse) a.lse[orow] = -INFINITY;
-        }
-        if (tid == 0 && h == 0 && a.prompt_len[b] < 0) atomicOr(a.dev_err, SIMSD_DEVERR_PROMPT_LEN);
-        it.advance(a);
-        continue;
-      }
-      const int P = a.prompt_len[b];
-      // ---- segment prologue: rotated Q rows (and the response tail tile)
-      // (cos, sin) of the 2B response positions, computed once per segment into the P
-      // area (idle here: the previous segment's last P V has completed)
-      float2* rtab = reinterpret_cast<float2*>(smem + C::kOffP);
-      for (int e = tid; e < twoB * 64; e += C::kSoftmaxThreads) {
-        const int sidx = e >> 6, d = e & 63;
-        float sn, cs;
-        rope_sincos(a.pos_ids[(size_t)b * twoB + sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
-        rtab[e] = make_float2(cs, sn);
-      }
-      ptx::named_bar_sync(1, C::kSoftmaxThreads);
-      {
-        uint4 v[16];
-        if (q_writer) {
-          if (real) {
-            load_row(v, a.q + orow * kD);
-            rope_row(v, rtab + s_slot * 64, a.scale_log2);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
-          }
-          if constexpr (C::kQInTmem) {
-            // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
-            uint32_t w[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                w[4 * c] = v[8 * half + c].x;
-                w[4 * c + 1] = v[8 * half + c].y;
-                w[4 * c + 2] = v[8 * half + c].z;
-                w[4 * c + 3] = v[8 * half + c].w;
-              }
-              ptx::tmem_st32(tmem + lane_off + C::kTmemQ + 32 * half, w);
-            }
-            ptx::tmem_st_wait();
-          } else {
-            store_row_sw(qtile, kBlockRows * 128, lrow, v);
-          }
-        }
-        if (it.has_tail && tail_writer) {
-          const int key = lrow & 63;
-          const bool is_v = lrow >= 64;
-          if (key < twoB) {
-            const size_t krow = (((size_t)b * twoB + key) * a.Hkv + h) * kD;
-            load_row(v, (is_v ? a.v_resp : a.k_resp) + krow);
-            if (!is_v) rope_row(v, rtab + key * 64, 1.f);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
-          }
-          store_row_sw(is_v ? tailv : tailk, kHalfTile, key, v);
-        }
-      }
-      ptx::named_bar_sync(1, C::kSoftmaxThreads);  // table reads done before P reuses the area
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kQFull));
-      // visibility of this thread's response-key columns (bit c = column col0 + c visible)
-      uint64_t vis = 0;
-      if (it.has_tail) {
-        const uint8_t* lab = a.labels + (size_t)b * twoB;
-        if (real) {
-          const int t = row_threshold(lab[s_slot]);
-          for (int k = 0; k < twoB; ++k)
-            if (response_key_visible(lab[k], t)) vis |= 1ull << k;
-        } else {
-          vis = twoB == 64 ? ~0ull : ((1ull << twoB) - 1);
-        }
-        vis >>= col0;
-      }
-      float m_used = -INFINITY, l = 0.f;
-      const uint32_t jfirst = j;
-      for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
-        const int buf = j & 1;
-        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
-        if (!ok) break;
-        ptx::tc_fence_after();
-        float x[NC];
-        {
-          uint32_t sa[32];
-          const uint32_t ts = tmem + lane_off + C::tmem_s(rb, buf) + col0;
-          if constexpr (NC == 32) {
-            ptx::tmem_ld32(ts, sa);
-            ptx::tmem_ld_wait(sa);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sa[c]);
-          } else {
-            uint32_t sb[32];
-            ptx::tmem_ld32(ts, sa);
-            ptx::tmem_ld32(ts + 32, sb);
-            ptx::tmem_ld_wait(sa);
-            ptx::tmem_ld_wait(sb);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              x[c] = __uint_as_float(sa[c]);
-              x[c + 32] = __uint_as_float(sb[c]);
-            }
-          }
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kSFree0 + buf));
-        if (i == 0) {
-#pragma unroll
-          for (int c = 0; c < NC; ++c) x[c] = ((vis >> c) & 1ull) ? x[c] : -INFINITY;
-        } else {
-          const int nvalid = P - (i - 1) * kTileKeys - col0;
-          if (nvalid < NC) {
-#pragma unroll
-            for (int c = 0; c < NC; ++c) x[c] = c < nvalid ? x[c] : -INFINITY;
-          }
-        }
-        float mt;
-        {
-          float mx[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = x[u];
-#pragma unroll
-          for (int c = 8; c < NC; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-          mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        }
-        // lazy rescale: only when some row's max grew by more than 2^8; warp-uniform because
-        // TMEM loads/stores are warp-collective
-        if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
-          const float m_new = fmaxf(m_used, mt);
-          if (j != jfirst) {  // rescale O: the previous P V must have landed
-            const uint32_t jp = j - 1;
-            ok = __all_sync(0xffffffffu,
-                            wait_bar(sh, bar(kPFree0 + (jp & 1)), (jp >> 1) & 1, a.dev_err));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const float alpha = ptx::ex2(m_used - m_new);
-            l *= alpha;
-            const uint32_t to = tmem + lane_off + C::tmem_o(oidx);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t o[32];
-              ptx::tmem_ld32(to + 32 * k, o);
-              ptx::tmem_ld_wait(o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(to + 32 * k, o);
-            }
-            ptx::tmem_st_wait();
-          }
-          m_used = m_new;
-        }
-        // a thread whose columns have all been masked so far (possible with split columns:
-        // the tail tile's 2B keys, or a ragged last tile) keeps p = 0, l = 0
-        const float msafe = m_used == -INFINITY ? 0.f : m_used;
-        uint32_t pk[NC / 2];
-        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < NC; c += 2) {
-          const float p0 = ptx::ex2(x[c] - msafe);
-          const float p1 = ptx::ex2(x[c + 1] - msafe);
-          ls0 += p0;
-          ls1 += p1;
-          pk[c >> 1] = pack_bf16(p0, p1);
-        }
-        l += ls0 + ls1;
-        // P buffer `buf` is free once the P V that last read it (tile j - 2) completed
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(sh, bar(kPFree0 + buf), ((j >> 1) & 1) ^ 1, a.dev_err));
-        if (!ok) break;
-        uint8_t* pt = smem + C::kOffP + (rb * 2 + buf) * kPBlock;
-#pragma unroll
-        for (int c = 0; c < NC / 8; ++c)
-          *reinterpret_cast<uint4*>(pt + sw128(lrow, c + col0 / 8)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kPFull0 + buf));
-      }
-      if (!ok) break;
-      // ---- epilogue: wait for the last P V, then O / l (or the partial)
-      const uint32_t jl = j - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kPFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      // combine the two column halves (split mode): exchange (max, sum) through the tail
-      // K/V area, which no MMA reads any more in this segment and which the next prologue
-      // rewrites only after its first softmax-wide barrier
-      float wA = 1.f, wB = 0.f, m_all = m_used, l_all = l;
-      int dcol0 = 0, ncols = kD;
-      if constexpr (C::kSplitCols) {
-        float2* xch = reinterpret_cast<float2*>(smem + C::kOffTail);
-        xch[wg * kBlockRows + lrow] = make_float2(m_used, l);
-        ptx::named_bar_sync(1, C::kSoftmaxThreads);
-        const float2 mlA = xch[lrow], mlB = xch[kBlockRows + lrow];
-        m_all = fmaxf(mlA.x, mlB.x);  // finite: every row sees at least B keys
-        wA = mlA.x == -INFINITY ? 0.f : ptx::ex2(mlA.x - m_all);
-        wB = mlB.x == -INFINITY ? 0.f : ptx::ex2(mlB.x - m_all);
-        l_all = wA * mlA.y + wB * mlB.y;
-        dcol0 = 64 * wg;
-        ncols = 64;
-      }
-      const uint32_t toA = tmem + lane_off + C::tmem_o(C::kSplitCols ? 0 : oidx);
-      const uint32_t toB = tmem + lane_off + C::tmem_o(1);
-      const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
-      const float inv = it.full ? 1.f / l_all : 1.f;
-      for (int k = 0; k < ncols / 32; ++k) {
-        const int dc = dcol0 + 32 * k;
-        uint32_t o[32];
-        ptx::tmem_ld32(toA + dc, o);
-        ptx::tmem_ld_wait(o);
-        float f[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * wA;
-        if constexpr (C::kSplitCols) {
-          uint32_t o2[32];
-          ptx::tmem_ld32(toB + dc, o2);
-          ptx::tmem_ld_wait(o2);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = fmaf(__uint_as_float(o2[e]), wB, f[e]);
-        }
-        if (!real) continue;
-        if (it.full) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + dc);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pack_bf16(f[8 * c] * inv, f[8 * c + 1] * inv),
-                                pack_bf16(f[8 * c + 2] * inv, f[8 * c + 3] * inv),
-                                pack_bf16(f[8 * c + 4] * inv, f[8 * c + 5] * inv),
-                                pack_bf16(f[8 * c + 6] * inv, f[8 * c + 7] * inv));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              a.ws_o + ((size_t)slot * (NRB * kBlockRows) + row) * kD + dc);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            dst[c] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
-        }
-      }
-      if (real && q_writer) {
-        if (it.full) {
-          if (a.lse) a.lse[orow] = (m_all + __log2f(l_all)) * 0.69314718055994530942f;
-        } else {
-          a.ws_ml[(size_t)slot * (NRB * kBlockRows) + row] = make_float2(m_all, l_all);
-        }
-      }
-      ptx::tc_fence_before();
-      it.advance(a);
-    }
-    if (tid == 0) a.ws_desc[blockIdx.x] = desc;
-  }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == C::kMmaWarp) ptx::tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // =========================================================================================
@@ -1520,7 +934,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 // Merges the pieces of every pair split between CTAs. Block (c, y) reads CTA c's merge
 // descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that pair:
 // one thread per (row, 4 output elements), so every load is independent.
-template <int NRB>
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
   const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
   const MergeDesc d = a.ws_desc[c];
@@ -1530,10 +943,10 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   const int row = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the CTA's block
   const int prow = crank * 128 + row;                    // row within the pair
   const int quad = threadIdx.x & 31;
-  if (row >= NRB * kBlockRows || prow >= a.R) return;
+  if (row >= kBlockRows || prow >= a.R) return;
   const int64_t T = d.T;
   const int C = a.ctas;
-  const size_t stride = (size_t)NRB * kBlockRows;
+  const size_t stride = kBlockRows;
   // pieces: unit vc (slot0) and every later non-empty unit up to c_last (its first slot),
   // each in the CTA of the same row block
   float mmax = -INFINITY;
@@ -1637,18 +1050,16 @@ static int cluster_size(const simsd_attn_params* p) { return rows_per_pair(p) > 
 struct WsLayout {
   size_t o, ml, desc, bytes;
 };
-static WsLayout ws_layout(int ctas, int nrb) {
+static WsLayout ws_layout(int ctas) {
   WsLayout w;
   w.o = 0;
-  w.ml = align_up(w.o + (size_t)2 * ctas * nrb * kBlockRows * kD * sizeof(float), 256);
-  w.desc = align_up(w.ml + (size_t)2 * ctas * nrb * kBlockRows * sizeof(float2), 256);
+  w.ml = align_up(w.o + (size_t)2 * ctas * kBlockRows * kD * sizeof(float), 256);
+  w.desc = align_up(w.ml + (size_t)2 * ctas * kBlockRows * sizeof(float2), 256);
   w.bytes = align_up(w.desc + (size_t)ctas * sizeof(MergeDesc), 256);
   return w;
 }
 
-template <int NRB>
 static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  using C = Cfg<NRB>;
   TcArgs a;
   a.batch = p->batch;
   a.B = p->B;
@@ -1656,9 +1067,8 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.Hkv = p->Hkv;
   a.G = p->Hq / p->Hkv;
   a.R = rows_per_pair(p);
-  a.nrb = NRB;
-  a.tile_keys = NRB == 1 ? r128::kKeys : kTileKeys;
-  a.cl = NRB == 1 ? cluster_size(p) : 1;
+  a.tile_keys = r128::kKeys;
+  a.cl = cluster_size(p);
   a.ctas = grid_ctas(p, a.cl);
   a.layout = (int)p->cache_layout;
   a.q = (const __nv_bfloat16*)p->q;
@@ -1673,7 +1083,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.out = (__nv_bfloat16*)p->out;
   a.lse = p->lse;
   a.dev_err = p->dev_err;
-  const WsLayout wl = ws_layout(a.ctas * a.cl, NRB);
+  const WsLayout wl = ws_layout(a.ctas * a.cl);
   if (!ws || ws_bytes < wl.bytes || (((uintptr_t)ws) & 255)) return SIMSD_ERR_WORKSPACE;
   a.ws_o = (float*)((char*)ws + wl.o);
   a.ws_ml = (float2*)((char*)ws + wl.ml);
@@ -1689,45 +1099,38 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
     return SIMSD_ERR_CUDA;
   }
 
-  // pairs of <= 128 rows: the all-TMEM 128-key kernel; 129..256 rows: two row blocks
-  const void* kfn = NRB == 1 ? (const void*)attn_tc128_kernel : (const void*)attn_tc_kernel<NRB>;
-  const int threads = NRB == 1 ? r128::kThreads : C::kThreads;
-  const uint32_t smem_bytes = NRB == 1 ? r128::kSmemBytes : C::kSmemBytes;
-  static int attr_done[64][3];
+  const int threads = r128::kThreads;
+  const uint32_t smem_bytes = r128::kSmemBytes;
+  static bool attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev][NRB]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(attn_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem_bytes);
     if (e != cudaSuccess) {
       record_cuda_error("cudaFuncSetAttribute", e);
       return SIMSD_ERR_CUDA;
     }
-    attr_done[dev][NRB] = 1;
+    attr_done[dev] = true;
   }
-  cudaError_t le = cudaSuccess;
-  if (NRB == 1) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)a.cl;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = smem_bytes;
-    cfg.stream = stream;
-    cfg.attrs = at;
-    cfg.numAttrs = a.cl > 1 ? 1 : 0;
-    le = cudaLaunchKernelEx(&cfg, attn_tc128_kernel, tmk, tmv, a);
-  } else {
-    attn_tc_kernel<NRB><<<a.ctas, threads, smem_bytes, stream>>>(tmk, tmv, a);
-  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;  // pairs of more than 128 rows: clusters of 2
+  at[0].val.clusterDim.x = (unsigned)a.cl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = a.cl > 1 ? 1 : 0;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc128_kernel, tmk, tmv, a);
   if (le == cudaSuccess) le = cudaGetLastError();
   if (le != cudaSuccess) {
     cudaFuncAttributes fa;
     char what[200] = "attention kernel launch";
-    if (cudaFuncGetAttributes(&fa, kfn) == cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, attn_tc128_kernel) == cudaSuccess)
       snprintf(what, sizeof(what),
                "attention kernel launch (threads %d, regs %d, max threads %d, dyn smem %u, "
                "max dyn smem %d, static smem %zu, local %zu)",
@@ -1737,8 +1140,8 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
     return SIMSD_ERR_CUDA;
   }
   // blocks without a split pair exit at once
-  const dim3 mgrid((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, NRB * kBlockRows) + 7) / 8));
-  attn_tc_merge_kernel<NRB><<<mgrid, 256, 0, stream>>>(a);
+  const dim3 mgrid((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, kBlockRows) + 7) / 8));
+  attn_tc_merge_kernel<<<mgrid, 256, 0, stream>>>(a);
   return last_launch_status();
 }
 
@@ -1754,7 +1157,7 @@ bool attn_tc_supported(const simsd_attn_params* p) {
 
 size_t attn_tc_workspace(const simsd_attn_params* p) {
   const int cl = tc::cluster_size(p);
-  return tc::ws_layout(tc::grid_ctas(p, cl) * cl, 1).bytes;
+  return tc::ws_layout(tc::grid_ctas(p, cl) * cl).bytes;
 }
 
 simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_bytes,
@@ -1766,7 +1169,7 @@ simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_byte
   if (p->cache_tokens > 0 && ((((uintptr_t)p->k_cache) | ((uintptr_t)p->v_cache)) & mask))
     return SIMSD_ERR_UNSUPPORTED;
   // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: a cluster of two
-  return tc::launch<1>(p, ws, ws_bytes, stream);
+  return tc::launch(p, ws, ws_bytes, stream);
 }
 
 }  // namespace simsd
