@@ -212,11 +212,9 @@ __device__ __forceinline__ int unpack_token(unsigned long long w) {
 // (0, 1/3], is summed as an odd series up to s^13 (truncation below 2e-8 relative; 1 - u is
 // exact). Below 1/2 the result is at least ln 2 and lg2's absolute error is harmless.
 __device__ __forceinline__ float neg_log_uniform(float u) {
-  if (u < 0.5f) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(u));
-    return y * -0.6931471805599453f;
-  }
+  float y;  // both forms, then a select: no divergence between the lanes of a warp
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(u));
+  const float below = y * -0.6931471805599453f;
   const float sv = __fdividef(1.f - u, 1.f + u);
   const float s2 = sv * sv;
   float poly = 2.f / 13.f;
@@ -226,13 +224,13 @@ __device__ __forceinline__ float neg_log_uniform(float u) {
   poly = fmaf(poly, s2, 2.f / 5.f);
   poly = fmaf(poly, s2, 2.f / 3.f);
   poly = fmaf(poly, s2, 2.f);
-  return sv * poly;
+  return u < 0.5f ? below : sv * poly;
 }
 
 // Race keys of the 4 entries of counter group g (entries 4g .. 4g + 3 below `end`) on the
 // residual max(0, p - q), or on p when `on_p`. p and q use the ex2 instruction (a few ulp),
 // which moves a key by about 1e-6 relative: only a race whose two best keys are that close
-// can change winner. The group's counter block is drawn only if one of its keys is positive.
+// can change winner.
 __device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], const float (&d)[4],
                                            float T, bool unit_T, float mt, float inv_st, float md,
                                            float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
@@ -255,16 +253,16 @@ __device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], 
     pos |= key[j] > 0.f;
   }
   anyp |= pos;
-  if (!pos && !on_p) return;
+  // no branch around the counter block: the groups of a batch then run their Philox
+  // rounds side by side (the few groups without a positive key are drawn for nothing)
   Philox4 c4 = {r, off_lo, off_hi, kResampleTag | (uint32_t)g};
   const Philox4 rnd = philox4x32_10(c4, key0, key1);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    if (key[j] > 0.f || (on_p && key[j] >= 0.f)) {
-      const float E = neg_log_uniform(word_to_uniform(philox_word(rnd, j)));
-      const unsigned long long kr = pack_key(__fdividef(key[j], E), 4 * g + j);
-      best = kr > best ? kr : best;
-    }
+    const float E = neg_log_uniform(word_to_uniform(philox_word(rnd, j)));
+    const unsigned long long kr = pack_key(__fdividef(key[j], E), 4 * g + j);
+    const bool take = key[j] > 0.f || (on_p && key[j] >= 0.f);
+    best = (take && kr > best) ? kr : best;
   }
 }
 
