@@ -141,6 +141,18 @@ def test_attention_bf16_ragged_tiles_full_compare(layout, B):
     _attention_parity(w, inputs, meta, st)
 
 
+@pytest.mark.parametrize("Hq,Hkv,B", [(6, 2, 32), (10, 2, 13), (8, 1, 9)])
+def test_attention_bf16_cluster_partial_second_block(Hq, Hkv, B):
+    # 2B*G rows per (request, kv-head) pair between 129 and 255: the pair runs on a
+    # cluster of two CTAs whose second CTA holds a partial row block (64, 2 and 16 rows)
+    w = MEDIUM.with_(Hq=Hq, Hkv=Hkv, B=B, gamma=B)
+    assert 128 < 2 * B * (Hq // Hkv) < 256
+    inputs, meta = H.make_case(w, seed=100 + B, prompt_len=[0, 61, 128, 1000 + 37])
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+    assert int(st.dev_err.item()) == 0
+
+
 def test_attention_bf16_identity_tau_and_d64():
     w = MEDIUM.with_(D=64, B=4, gamma=4)
     tau = [[1, 2, 3, 4]] * w.batch
