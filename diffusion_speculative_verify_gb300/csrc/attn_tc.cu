@@ -8,10 +8,11 @@
 // Work decomposition. For each (request b, kv head h) the 2B*G query rows (response slot
 // s, head g of the group; row = s*G + g) form a "pair". Each pair is a sequence of tiles:
 // tile 0 is the response tail (the 2B response keys, rotated and masked here), tiles 1..
-// stream the prompt keys, 128 at a time. All pairs' tiles are concatenated and cut into
-// equal contiguous ranges, one per schedule unit (stream-K); a unit therefore sees at
-// most two partial pairs (its first and last), whose (O, max, sum) partials are merged by
-// attn_tc_merge_kernel. A unit is one CTA for pairs of up to 128 rows and a cluster of two
+// stream the prompt keys, 128 at a time. All pairs' tiles, each pair with a start-up share
+// (its prologue and epilogue cost in tile units), are concatenated and cut into equal
+// contiguous ranges, one per schedule unit (stream-K); a unit therefore sees at most two
+// partial pairs (its first and last), whose (O, max, sum) partials are merged by
+// attn_tc_merge_kernel, a programmatic dependent launch. A unit is one CTA for pairs of up to 128 rows and a cluster of two
 // CTAs (rows [0, 128) and [128, 256)) above that; the two load each prompt tile once,
 // half each, multicast into both.
 //
@@ -48,12 +49,17 @@ constexpr int kD = 128;
 constexpr int kBlockRows = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
 constexpr int kMaxStages = 8;                         // stage barriers reserved in shared memory
+// Start-up and finish of one pair segment (prologue, epilogue, pipeline refill) in units of
+// one prompt tile's streaming time; the schedule charges it to every pair.
+constexpr int kSegCost = 3;
+constexpr int kPrefetchAhead = 4;  // tiles before a segment's end at which the next one is prefetched
 
 
 struct TcArgs {
   int batch, B, Hq, Hkv, G, R, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
   int cl;                                  // CTAs per schedule unit (a cluster): 1, or 2 when R > 128
   int tile_keys;                           // prompt keys per tile (64 or 128)
+  int seg_cost;                            // virtual units charged per pair for start-up
   int layout;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_resp;
@@ -80,69 +86,95 @@ struct MergeDesc {
 };
 
 // ----------------------------------------------------------------------- scheduling
-__device__ __forceinline__ bool request_invalid(const TcArgs& a, int b) {
-  return a.prompt_len[b] < 0 || a.labels[(size_t)b * 2 * a.B] == kLabelInvalid;
-}
+// Pair (b, h) has nt(b) = 1 + ceil(P_b / 128) tiles (1 for an invalid request). Besides its
+// tiles it is charged `seg_cost` virtual units for its start-up and finish (prologue,
+// epilogue, pipeline refill), so it spans nt(b) + seg_cost units of the virtual sequence
+// that is cut into equal contiguous ranges, one per schedule unit. A range that begins
+// inside a pair's start-up share starts at the pair's tile 0; one that ends inside it does
+// not take the pair.
 __device__ __forceinline__ int tiles_per_pair(const TcArgs& a, int b) {
-  if (request_invalid(a, b)) return 1;
-  return 1 + (a.prompt_len[b] + a.tile_keys - 1) / a.tile_keys;
+  const int P = a.prompt_len[b];
+  const uint8_t l0 = a.labels[(size_t)b * 2 * a.B];  // both loads issued together
+  if ((P < 0) | (l0 == kLabelInvalid)) return 1;
+  return 1 + (P + a.tile_keys - 1) / a.tile_keys;
+}
+__device__ __forceinline__ bool request_invalid(const TcArgs& a, int b) {
+  const int P = a.prompt_len[b];
+  const uint8_t l0 = a.labels[(size_t)b * 2 * a.B];
+  return (P < 0) | (l0 == kLabelInvalid);
 }
 
-// CTA c covers global tiles [c*T/C, (c+1)*T/C).
+// Unit c covers virtual positions [c*T/C, (c+1)*T/C).
 __device__ __forceinline__ int64_t cta_begin(int64_t T, int C, int c) {
   return (T * (int64_t)c) / C;
 }
 
 struct SchedStart {
-  int64_t T, t0, t1, Tb;  // total tiles, this CTA's range, first tile of request b
+  int64_t T, t0, t1, Tb;  // virtual total, this unit's range, first position of request b
   int b;
 };
 
-// One warp: total tile count and the request containing tile `t0` of CTA `c`.
-__device__ SchedStart warp_schedule(const TcArgs& a, int c, int C, int lane) {
-  const int ppr = a.Hkv;  // pairs per request
-  int64_t tot = 0;
-  for (int base = 0; base < a.batch; base += 32) {
-    const int b = base + lane;
-    int64_t v = b < a.batch ? (int64_t)ppr * tiles_per_pair(a, b) : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    tot += v;
+// Threads 0..127 (named barrier 1): each sums the virtual lengths of a contiguous run of
+// requests, a block scan places the runs, and the thread whose run holds t0 finds the
+// request. Writes T, t0, t1, b and Tb to shared memory.
+__device__ void block_schedule(const TcArgs& a, int c, int C, int tid, int64_t* wsum,
+                               int64_t* out_T, int64_t* out_t0, int64_t* out_t1,
+                               int64_t* out_Tb, int* out_b) {
+  const int lane = tid & 31, w = tid >> 5;
+  const int k = (a.batch + 127) >> 7;
+  const int b0 = tid * k;
+  int64_t sum = 0;
+  for (int i = 0; i < k; ++i) {
+    const int b = b0 + i;
+    if (b < a.batch) sum += (int64_t)a.Hkv * (tiles_per_pair(a, b) + a.seg_cost);
   }
-  SchedStart s;
-  s.T = tot;
-  s.t0 = cta_begin(tot, C, c);
-  s.t1 = cta_begin(tot, C, c + 1);
-  s.b = a.batch;
-  s.Tb = tot;
-  int64_t cum = 0;
-  for (int base = 0; base < a.batch; base += 32) {
-    const int b = base + lane;
-    const int64_t v = b < a.batch ? (int64_t)ppr * tiles_per_pair(a, b) : 0;
-    int64_t incl = v;
+  int64_t incl = sum;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && cum + incl > s.t0);
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      const int64_t excl = __shfl_sync(0xffffffffu, incl - v, L);
-      s.b = base + L;
-      s.Tb = cum + excl;
-      break;
-    }
-    cum += __shfl_sync(0xffffffffu, incl, 31);
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
   }
-  return s;
+  if (lane == 31) wsum[w] = incl;
+  ptx::named_bar_sync(1, 128);
+  int64_t T = 0, before = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t v = wsum[i];
+    before += i < w ? v : 0;
+    T += v;
+  }
+  const int64_t excl = before + incl - sum;
+  const int64_t t0 = cta_begin(T, C, c);
+  if (tid == 0) {
+    *out_T = T;
+    *out_t0 = t0;
+    *out_t1 = cta_begin(T, C, c + 1);
+    if (t0 >= T) {
+      *out_b = a.batch;
+      *out_Tb = T;
+    }
+  }
+  if (t0 < T && excl <= t0 && t0 < excl + sum) {  // exactly one thread
+    int64_t cum = excl;
+    for (int i = 0; i < k; ++i) {
+      const int b = b0 + i;
+      const int64_t len = (int64_t)a.Hkv * (tiles_per_pair(a, b) + a.seg_cost);
+      if (t0 < cum + len) {
+        *out_b = b;
+        *out_Tb = cum;
+        break;
+      }
+      cum += len;
+    }
+  }
 }
 
-// Walks the segments (pair pieces) of one CTA's tile range.
+// Walks the segments (the nonempty pieces of pairs) of one unit's virtual range.
 struct SegIter {
-  int64_t t, t1, Tb, t0;
-  int b, nt, ppr, batch;
-  // current segment
+  int64_t t, t0, t1, Tb;  // virtual: current position, the range, first position of request b
+  int64_t pend, send;     // virtual ends of the current segment's pair and of the segment
+  int b, nt, ppr, batch, sc;
+  // current segment: kv head, first tile and tile count
   int h, i0, n;
   bool first, full, has_tail, invalid;
 
@@ -154,29 +186,37 @@ struct SegIter {
     b = s.b;
     ppr = a.Hkv;
     batch = a.batch;
+    sc = a.seg_cost;
     nt = (b < batch) ? tiles_per_pair(a, b) : 1;
   }
-  // Prepares the segment starting at t; false when the range is exhausted.
+  // Prepares the next nonempty segment at or after t; false when the range is exhausted.
   __device__ bool next(const TcArgs& a) {
-    if (t >= t1 || b >= batch) return false;
-    const int64_t rel = t - Tb;
-    const int q = (int)(rel / nt);
-    i0 = (int)(rel % nt);
-    const int64_t pair_start = Tb + (int64_t)q * nt;
-    const int64_t pair_end = pair_start + nt;
-    const int64_t seg_end = pair_end < t1 ? pair_end : t1;
-    n = (int)(seg_end - t);
-    h = q;
-    first = (t == t0);
-    full = (i0 == 0) && (seg_end == pair_end);
-    has_tail = (i0 == 0);
-    invalid = request_invalid(a, b);
-    return true;
+    while (t < t1 && b < batch) {
+      const int L = nt + sc;
+      const int64_t rel = t - Tb;
+      const int q = (int)(rel / L);
+      const int64_t pstart = Tb + (int64_t)q * L;
+      pend = pstart + L;
+      send = pend < t1 ? pend : t1;
+      i0 = max((int)(t - pstart) - sc, 0);
+      n = max((int)(send - pstart) - sc, 0) - i0;
+      if (n > 0) {
+        h = q;
+        first = (t == t0);
+        full = (i0 == 0) && (send == pend);
+        has_tail = (i0 == 0);
+        invalid = request_invalid(a, b);
+        return true;
+      }
+      advance(a);  // only the pair's start-up share lies in the range
+    }
+    return false;
   }
   __device__ void advance(const TcArgs& a) {
-    t += n;
-    if (t >= Tb + (int64_t)ppr * nt) {
-      Tb += (int64_t)ppr * nt;
+    t = send;
+    const int64_t rend = Tb + (int64_t)ppr * (nt + sc);
+    if (t >= rend) {
+      Tb = rend;
       ++b;
       nt = (b < batch) ? tiles_per_pair(a, b) : 1;
     }
@@ -225,8 +265,7 @@ struct Shared {
   int abort;
   int64_t T, t0, t1, Tb;
   int b;
-  int pos[2 * kMaxB];       // position ids of the current pair's response slots
-  uint8_t lab[2 * kMaxB];   // their labels
+  int64_t wsum[4];          // block scan of the schedule
 };
 
 
@@ -278,6 +317,17 @@ __device__ __forceinline__ void rope_row(uint4 (&v)[16], const float2* cs, float
       hi[e] = pack_bf16((x0 * t.y + y0 * t.x) * scale, (x1 * t.w + y1 * t.z) * scale);
     }
   }
+}
+
+// sin / cos of the RoPE angle pos * omega_d: the fraction of a turn is formed exactly as
+// in rope_sincos, then the hardware approximations take it (absolute error about 2^-21 on
+// [-pi, pi]). Used where the rotated values are rounded to bf16 (relative step 2^-8).
+__device__ __forceinline__ void rope_sincos_fast(int pos, float c_hi, float c_lo, float* s, float* c) {
+  const float x = (float)pos;
+  const float a = x * c_hi;
+  const float e = fmaf(x, c_hi, -a);
+  const float f = (a - rintf(a)) + fmaf(x, c_lo, e);
+  __sincosf(6.28318530717958647692f * f, s, c);
 }
 
 // Max over the valid entries (bit c of vm) of a 32-column chunk of fp32 scores.
@@ -335,6 +385,42 @@ __device__ __forceinline__ void store_row_sw(uint8_t* tile, uint32_t half_bytes,
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half_bytes + sw128(r, c & 7)) = v[c];
 }
 
+// L2 prefetch of what the prologue of the segment (request nb, kv head nh, with a tail tile
+// when ntail) loads: this thread's Q row, its tail K or V row (same thread mapping as the
+// prologue) and the labels and position ids.
+__device__ __forceinline__ void prefetch_prologue(const TcArgs& a, int nb, int nh, int ntail, int twoB,
+                                                  int s_slot, int g, bool real, int rw, int tid) {
+  if (real) {
+    const __nv_bfloat16* qrow = a.q + (((size_t)nb * twoB + s_slot) * a.Hq + (size_t)nh * a.G + g) * kD;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + 64));
+  }
+  if (ntail) {
+    int key;
+    bool tail_row, tail_k;
+    if (128 - rw >= 2 * twoB) {
+      const int e = tid - rw;
+      tail_row = e >= 0 && e < 2 * twoB;
+      tail_k = e < twoB;
+      key = tail_k ? e : e - twoB;
+    } else {
+      key = tid & 63;
+      tail_row = key < twoB;
+      tail_k = tid < 64;
+    }
+    if (tail_row) {
+      const __nv_bfloat16* trow =
+          (tail_k ? a.k_resp : a.v_resp) + (((size_t)nb * twoB + key) * a.Hkv + nh) * kD;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
+    }
+  }
+  if (tid == 0) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.labels + (size_t)nb * twoB));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.pos_ids + (size_t)nb * twoB));
+  }
+}
+
 // A 128-element bf16 row (16 chunks) into 64 TMEM columns of this thread's lane:
 // elements (2c, 2c + 1) in column c, the lower index in the low half.
 __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]) {
@@ -388,6 +474,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
                       const __grid_constant__ TcArgs a) {
   using namespace r128;
   static_assert(sizeof(Shared) <= 1024, "barrier area");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // let the merge grid be placed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
@@ -407,13 +494,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   const int row0 = crank * 128;  // first pair row of this CTA
 
   if (warp == kProducerWarp) {
-    const SchedStart s = warp_schedule(a, vcta, a.ctas, lane);
     if (lane == 0) {
-      sh->T = s.T;
-      sh->t0 = s.t0;
-      sh->t1 = s.t1;
-      sh->Tb = s.Tb;
-      sh->b = s.b;
       sh->abort = 0;
       for (int i = 0; i < kStages; ++i) {
         ptx::mbar_init(bar(kFull0 + i), 1);
@@ -434,6 +515,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   } else if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
+  } else {
+    block_schedule(a, vcta, a.ctas, tid, sh->wsum, &sh->T, &sh->t0, &sh->t1, &sh->Tb, &sh->b);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -649,10 +732,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     while (ok && it.next(a)) {
       const int b = it.b, h = it.h;
       if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
-        const int64_t pe = it.t + it.nt;
         desc.b = b;
         desc.h = h;
-        desc.c_last = (int)((pe * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
+        desc.c_last = (int)((it.pend * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
         desc.slot0 = 2 * blockIdx.x + (it.first ? 0 : 1);
       }
       const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
@@ -688,6 +770,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         tail_row = has_tail && key < twoB;
         tail_k = tid < 64;
       }
+      // labels and position ids of the 2B response slots: every warp holds slot `lane` and
+      // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip);
+      // issued before the row loads, whose many requests would otherwise delay them
+      const size_t lrow = (size_t)b * twoB;
+      const uint32_t lab_lo = lane < twoB ? a.labels[lrow + lane] : 0u;
+      const uint32_t lab_hi = lane + 32 < twoB ? a.labels[lrow + 32 + lane] : 0u;
+      const int pos_lo = lane < twoB ? a.pos_ids[lrow + lane] : 0;
+      const int pos_hi = lane + 32 < twoB ? a.pos_ids[lrow + 32 + lane] : 0;
       uint4 v[16];
       const __nv_bfloat16* trow =
           (tail_k ? a.k_resp : a.v_resp) + (((size_t)b * twoB + (tail_row ? key : 0)) * a.Hkv + h) * kD;
@@ -700,32 +790,42 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
       }
-      uint8_t lab_r = 0;
-      int pos_r = 0;
-      if (tid < twoB) {
-        lab_r = a.labels[(size_t)b * twoB + tid];
-        pos_r = a.pos_ids[(size_t)b * twoB + tid];
-      }
-      if (!loads_signalled) {  // the loads above are issued: the prompt stream may follow
-        ptx::mbar_arrive(bar(kLoads));
-        loads_signalled = true;
-      }
-      if (tid < twoB) {
-        sh->lab[tid] = lab_r;
-        sh->pos[tid] = pos_r;
-      }
-      ptx::named_bar_sync(1, 128);
       // (cos, sin) of the 2B response positions, over the tail K and V area (2B <= 64:
       // at most 32 KB); the tail rows are stored once every read of the table is done. Rows
       // are 66 float2 apart where that fits (16 bytes of padding: threads reading different
-      // positions' rows then hit different banks), else 64.
+      // positions' rows then hit different banks), else 64. Thread t fills pair t % 64 of
+      // the slots t / 64, t / 64 + 2, ... (the slot is warp-uniform).
       float2* rtab = reinterpret_cast<float2*>(tailk);
       const int tstride = twoB * 66 * 8 <= (int)(2 * kTailKV) ? 66 : 64;
-      for (int e = tid; e < twoB * 64; e += 128) {
-        const int sidx = e >> 6, d = e & 63;
-        float sn, cs;
-        rope_sincos(sh->pos[sidx], a.rope.c_hi[d], a.rope.c_lo[d], &sn, &cs);
-        rtab[sidx * tstride + d] = make_float2(cs, sn);
+      {
+        const int d = tid & 63;
+        const float c_hi = a.rope.c_hi[d], c_lo = a.rope.c_lo[d];
+        for (int sidx = tid >> 6; sidx < twoB; sidx += 2) {
+          const int ps = __shfl_sync(0xffffffffu, sidx < 32 ? pos_lo : pos_hi, sidx & 31);
+          float sn, cs;
+          rope_sincos_fast(ps, c_hi, c_lo, &sn, &cs);
+          rtab[sidx * tstride + d] = make_float2(cs, sn);
+        }
+      }
+      // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
+      uint32_t vis0 = 0, vis1 = 0;
+      if (has_tail) {
+        const uint32_t own_lo = __shfl_sync(0xffffffffu, lab_lo, s_slot & 31);
+        const uint32_t own_hi = __shfl_sync(0xffffffffu, lab_hi, s_slot & 31);
+        const int th = row_threshold((uint8_t)(s_slot < 32 ? own_lo : own_hi));
+        for (int k = 0; k < twoB; ++k) {
+          const uint32_t lk = __shfl_sync(0xffffffffu, k < 32 ? lab_lo : lab_hi, k & 31);
+          if (response_key_visible((uint8_t)lk, th)) {
+            if (k < 32)
+              vis0 |= 1u << k;
+            else
+              vis1 |= 1u << (k - 32);
+          }
+        }
+        if (!real) {
+          vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
+          vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
+        }
       }
       ptx::named_bar_sync(1, 128);
       if (warp_active) {
@@ -750,6 +850,10 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
       }
+      if (!loads_signalled) {  // this prologue's rows have landed: the prompt stream may start
+        ptx::mbar_arrive(bar(kLoads));
+        loads_signalled = true;
+      }
       ptx::named_bar_sync(1, 128);  // table reads done
       if (early) {
         if (tail_row) store_row_sw(tail_k ? tailk : tailv, kTailHalf, key, v);
@@ -765,27 +869,24 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kQFull));
-      // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
-      uint32_t vis0 = 0, vis1 = 0;
-      if (has_tail) {
-        if (real) {
-          const int th = row_threshold(sh->lab[s_slot]);
-          for (int k = 0; k < twoB; ++k)
-            if (response_key_visible(sh->lab[k], th)) {
-              if (k < 32)
-                vis0 |= 1u << k;
-              else
-                vis1 |= 1u << (k - 32);
-            }
-        } else {
-          vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
-          vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
-        }
-      }
       float m_used = -INFINITY, l = 0.f;
       const uint32_t jfirst = j;
+      // The next segment's Q rows, tail rows and labels go into L2 a few tiles before this
+      // segment ends, so that its prologue does not wait behind the K/V stream in flight.
+      int pf_b = -1, pf_h = 0;  // next segment: request, kv head | has_tail << 16
+      {
+        SegIter nx = it;
+        nx.advance(a);
+        if (nx.next(a) && !nx.invalid) {
+          pf_b = nx.b;
+          pf_h = nx.h | (nx.has_tail ? 1 << 16 : 0);
+        }
+      }
+      const int pf_at = max(it.i0, it.i0 + it.n - kPrefetchAhead);
       for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
         const int buf = j & 1;
+        if (pf_b >= 0 && i == pf_at)
+          prefetch_prologue(a, pf_b, pf_h & 0xffff, pf_h >> 16, twoB, s_slot, g, real, rw, tid);
         ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
         if (!ok) break;
         if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
@@ -935,6 +1036,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 // descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that pair:
 // one thread per (row, 4 output elements), so every load is independent.
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the attention grid has completed
   const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
   const MergeDesc d = a.ws_desc[c];
   if (d.b < 0) return;
@@ -1068,6 +1170,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.G = p->Hq / p->Hkv;
   a.R = rows_per_pair(p);
   a.tile_keys = r128::kKeys;
+  a.seg_cost = kSegCost;
   a.cl = cluster_size(p);
   a.ctas = grid_ctas(p, a.cl);
   a.layout = (int)p->cache_layout;
@@ -1139,9 +1242,24 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
     record_cuda_error(what, le);
     return SIMSD_ERR_CUDA;
   }
-  // blocks without a split pair exit at once
-  const dim3 mgrid((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, kBlockRows) + 7) / 8));
-  attn_tc_merge_kernel<<<mgrid, 256, 0, stream>>>(a);
+  // blocks without a split pair exit at once. A programmatic dependent of the attention
+  // kernel: its blocks are placed while the attention CTAs run and wait (griddepcontrol)
+  // for their completion, so the launch latency is hidden.
+  cudaLaunchConfig_t mcfg = {};
+  cudaLaunchAttribute mat[1];
+  mat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  mat[0].val.programmaticStreamSerializationAllowed = 1;
+  mcfg.gridDim = dim3((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, kBlockRows) + 7) / 8));
+  mcfg.blockDim = dim3(256);
+  mcfg.dynamicSmemBytes = 0;
+  mcfg.stream = stream;
+  mcfg.attrs = mat;
+  mcfg.numAttrs = 1;
+  cudaError_t me = cudaLaunchKernelEx(&mcfg, attn_tc_merge_kernel, a);
+  if (me != cudaSuccess) {
+    record_cuda_error("merge kernel launch", me);
+    return SIMSD_ERR_CUDA;
+  }
   return last_launch_status();
 }
 
