@@ -44,13 +44,36 @@ struct AcceptPlan {
   size_t off_stats, off_winners, off_anypos, off_ticket, bytes;
 };
 
-constexpr int kStatChunk = 2048;  // vocabulary entries per (row, chunk) work item: 8 KB
+// Warps of the stats kernel and CTAs of the finish kernel resident at once on the current
+// device (occupancy query, cached per device).
+int resident_stat_warps();
+int resident_finish_ctas();
 
+// K3a cuts every verified row into nchunk_a equal chunks, one work item per (row, chunk),
+// and the items are dealt to the resident warps round-robin. nchunk_a is the smallest count
+// whose items fill the warps' last round to at least 97 % (the kernel's time is set by the
+// warps that take the most items), else the best fill; chunks stay at least 512 entries.
+// K3b takes one wave of CTAs, nchunk_b per request.
 AcceptPlan make_plan(int batch, int gamma, int V) {
   AcceptPlan p;
-  p.nchunk_a = (V + kStatChunk - 1) / kStatChunk;
-  p.chunk_a = kStatChunk;
-  long nb = batch > 0 ? (608 + batch - 1) / batch : 1;
+  const long rows = (long)batch * gamma * 2;
+  const long W = std::max(1, resident_stat_warps());
+  const long ncmax = std::max<long>(1, (V + 511) / 512);
+  long best_nc = 1;
+  double best_fill = -1.0;
+  for (long nc = 1; nc <= ncmax && rows > 0; ++nc) {
+    const long items = rows * nc;
+    const long rounds = (items + W - 1) / W;
+    const double fill = (double)items / (double)(rounds * W);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best_nc = nc;
+    }
+    if (fill >= 0.97) break;
+  }
+  p.chunk_a = (int)(((V + best_nc - 1) / best_nc + 3) / 4 * 4);
+  p.nchunk_a = (V + p.chunk_a - 1) / p.chunk_a;
+  long nb = batch > 0 ? std::max(1, resident_finish_ctas()) / batch : 1;
   const long max_nb = (V + 1023) / 1024;
   if (nb > max_nb) nb = max_nb;
   if (nb < 1) nb = 1;
@@ -98,11 +121,13 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 }
 
 // ----------------------------------------------------------------------------- K3a
-// One warp per (row, chunk) work item of kStatChunk vocabulary entries; a persistent grid of
-// warps strides over the items, so there is no block-level synchronisation and every lane
-// keeps kStatChunk / 32 / 4 float4 loads in flight at once. exp is evaluated as
-// 2^((x - m) * log2 e) with the ex2 instruction (about 2 ulp; the acceptance decisions use
-// the accurate exp on single values).
+// One warp per (row, chunk) work item; a persistent grid of warps strides over the items,
+// so there is no block-level synchronisation. A lane streams its share of the chunk in
+// batches of kPer float4 loads in flight, keeping a running (max, sum exp) across batches.
+// exp is evaluated as 2^((x - m) * log2 e) with the ex2 instruction (about 2 ulp; the
+// acceptance decisions use the accurate exp on single values).
+constexpr int kPer = 16;  // float4 loads in flight per lane
+
 __device__ __forceinline__ float exp_shifted(float x, float m) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"((x - m) * 1.4426950408889634f));
@@ -130,7 +155,6 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
   }
   const bool unit_T = (T == 1.f);
   const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
-  constexpr int kPer = kStatChunk / 32 / 4;  // float4 per lane
   for (long item = warp_global; item < items; item += nwarps) {
     const int chunk = (int)(item % nchunk);
     const long row = item / nchunk;
@@ -140,39 +164,46 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
     const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
     float m = -INFINITY, sum = 0.f;
-    if (hit) {
+    const int c0 = chunk * plan.chunk_a;
+    const int len = min(plan.chunk_a, V - c0);
+    if (hit && len > 0) {
       const int k = __ffs(hit) - 1;
       const float* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
-      const int c0 = chunk * kStatChunk;
-      const int len = min(kStatChunk, V - c0);
       if (vec_ok) {
         const float4* src = reinterpret_cast<const float4*>(rowp + c0);
         const int n4 = len >> 2;
-        float4 x[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int i4 = lane + 32 * u;
-          x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
-                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          if (!unit_T) {
-            x[u].x = scale_logit(x[u].x, T, false);
-            x[u].y = scale_logit(x[u].y, T, false);
-            x[u].z = scale_logit(x[u].z, T, false);
-            x[u].w = scale_logit(x[u].w, T, false);
-          }
-          m = fmaxf(m, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
-        }
-        if (m != -INFINITY) {
-          float s0 = 0.f, s1 = 0.f;
+        for (int base = 0; base < n4; base += 32 * kPer) {
+          float4 x[kPer];
 #pragma unroll
           for (int u = 0; u < kPer; ++u) {
-            s0 += exp_shifted(x[u].x, m) + exp_shifted(x[u].y, m);
-            s1 += exp_shifted(x[u].z, m) + exp_shifted(x[u].w, m);
+            const int i4 = base + lane + 32 * u;
+            x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
           }
-          sum = s0 + s1;
+          float mb = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            if (!unit_T) {
+              x[u].x = scale_logit(x[u].x, T, false);
+              x[u].y = scale_logit(x[u].y, T, false);
+              x[u].z = scale_logit(x[u].z, T, false);
+              x[u].w = scale_logit(x[u].w, T, false);
+            }
+            mb = fmaxf(mb, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+          }
+          if (mb > m) {  // rescale what was summed so far to the new maximum
+            sum = (m == -INFINITY) ? 0.f : sum * exp_shifted(m, mb);
+            m = mb;
+          }
+          if (m != -INFINITY) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+              s0 += exp_shifted(x[u].x, m) + exp_shifted(x[u].y, m);
+              s1 += exp_shifted(x[u].z, m) + exp_shifted(x[u].w, m);
+            }
+            sum += s0 + s1;
+          }
         }
       } else {
         for (int v = lane; v < len; v += 32) {
@@ -316,8 +347,6 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     AcceptPlan plan, AcceptWs ws, int32_t* __restrict__ accepted_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_pos,
     int32_t* __restrict__ n_commit, uint32_t* __restrict__ dev_err) {
-  // launched as a programmatic dependent of K3a: wait for K3a's results before any read
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int chunk = blockIdx.x % plan.nchunk_b;
   const int r = blockIdx.x / plan.nchunk_b;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -328,6 +357,42 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __shared__ int s_a, s_bad;
   __shared__ float s_mt, s_st, s_md, s_sd;
   __shared__ float2 s_rowstat[2 * kMaxB];  // merged (max, sum exp) per (step, model)
+
+  // Everything that does not read K3a's results comes before the grid dependency wait, so
+  // it overlaps K3a's last items: warp 0 checks the step labels, orders the steps, and loads
+  // each verified step's draft token, the two logits at that token and its uniform.
+  int bad_w = 0, k_w = 0, x_w = 0;  // warp 0: error bits, slot and token of step `lane`
+  float tx = 0.f, dx = 0.f, u = 0.f;
+  if (w == 0) {
+    // step labels of the data half -> order o_t; validity of the permutation
+    const uint8_t lb = lane < B ? lab[lane] : 0;
+    const int tau = lb & 0x7F;
+    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau >= 1 && tau <= B);
+    const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
+    const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
+    const unsigned full = B == 32 ? 0xffffffffu : ((1u << B) - 1u);
+    const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
+    if (perm && lane < B) s_order[tau - 1] = lane;
+    __syncwarp();
+    bad_w = perm ? 0 : (int)SIMSD_DEVERR_TAU;
+    if (perm && lane < gamma) {
+      k_w = s_order[lane];
+      x_w = tokens[(size_t)r * B + k_w];
+    }
+    const bool tok_bad = perm && lane < gamma && (x_w < 0 || x_w >= V);
+    if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
+    if (!bad_w && lane < gamma) {
+      const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
+      tx = scale_logit(target[rowoff], T, unit_T);
+      dx = scale_logit(draft[rowoff], T, unit_T);
+      Philox4 c4 = {(uint32_t)r, off_lo, off_hi, (uint32_t)(lane >> 2)};
+      const Philox4 rnd = philox4x32_10(c4, key0, key1);
+      u = word_to_uniform(philox_word(rnd, lane & 3));
+    }
+  }
+
+  // launched as a programmatic dependent of K3a: wait for K3a's results before reading them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // merge the chunk partials of every verified (step, model) row: warp w takes rows
   // w, w + 8, ...; its lanes stride over the chunks
@@ -349,26 +414,8 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __syncthreads();
 
   if (w == 0) {
-    // step labels of the data half -> order o_t; validity of the permutation
-    const uint8_t lb = lane < B ? lab[lane] : 0;
-    const int tau = lb & 0x7F;
-    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau >= 1 && tau <= B);
-    const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
-    const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
-    const unsigned full = B == 32 ? 0xffffffffu : ((1u << B) - 1u);
-    const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
-    if (perm && lane < B) s_order[tau - 1] = lane;
-    __syncwarp();
-    int bad = perm ? 0 : (int)SIMSD_DEVERR_TAU;
-    int x = 0, k = 0;
-    if (perm && lane < gamma) {
-      k = s_order[lane];
-      x = tokens[(size_t)r * B + k];
-    }
-    const bool tok_bad = perm && lane < gamma && (x < 0 || x >= V);
-    if (__any_sync(0xffffffffu, tok_bad)) bad |= (int)SIMSD_DEVERR_TOKEN;
     int a = gamma;
-    if (!bad) {
+    if (!bad_w) {
       bool acc = true;
       float mt = 0.f, st = 0.f, md = 0.f, sd = 0.f;
       if (lane < gamma) {
@@ -377,12 +424,8 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
         st = rt.y;
         md = rd.x;
         sd = rd.y;
-        const size_t rowoff = ((size_t)r * B + k) * (size_t)V + x;
-        const float px = __fdiv_rn(expf(scale_logit(target[rowoff], T, unit_T) - mt), st);
-        const float qx = __fdiv_rn(expf(scale_logit(draft[rowoff], T, unit_T) - md), sd);
-        Philox4 c4 = {(uint32_t)r, off_lo, off_hi, (uint32_t)(lane >> 2)};
-        const Philox4 rnd = philox4x32_10(c4, key0, key1);
-        const float u = word_to_uniform(philox_word(rnd, lane & 3));
+        const float px = __fdiv_rn(expf(tx - mt), st);
+        const float qx = __fdiv_rn(expf(dx - md), sd);
         acc = (px >= qx) || (u * qx < px);
       }
       const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && !acc);
@@ -396,7 +439,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     }
     if (lane == 0) {
       s_a = a;
-      s_bad = bad;
+      s_bad = bad_w;
     }
   }
   __syncthreads();
@@ -491,6 +534,32 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   }
 }
 
+// Resident blocks per SM of `kernel` x SMs of the current device, cached per device.
+template <typename K>
+int resident_blocks(K kernel, int threads, int* cache) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    const int sms = device_sm_count();
+    cache[dev] = per_sm * (sms > 0 ? sms : 148);
+  }
+  return cache[dev];
+}
+
+int resident_stat_warps() {
+  static int cache[64];
+  return resident_blocks(accept_stats_kernel, kStatThreads, cache) * (kStatThreads / 32);
+}
+
+int resident_finish_ctas() {
+  static int cache[64];
+  return resident_blocks(accept_finish_kernel, kFinishThreads, cache);
+}
+
 }  // namespace
 
 }  // namespace simsd
@@ -530,18 +599,9 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   const long grid_b = (long)batch * plan.nchunk_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
-  // persistent grid: as many stats CTAs as can be resident at once
-  static int resident[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && resident[dev] == 0) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_stats_kernel, kStatThreads, 0) != cudaSuccess || per_sm < 1)
-      per_sm = 2;
-    const int sms = device_sm_count();
-    resident[dev] = per_sm * (sms > 0 ? sms : 148);
-  }
-  const long max_ctas = dev < 64 ? resident[dev] : 296;
+  // persistent grid: as many stats CTAs as can be resident at once (fewer if the items are
+  // fewer than the resident warps)
+  const long max_ctas = std::max(1, resident_stat_warps() / (kStatThreads / 32));
   const long warps_needed = (long)batch * gamma * 2 * plan.nchunk_a;
   const long grid_stats = std::max<long>(1, std::min<long>((warps_needed + kStatThreads / 32 - 1) / (kStatThreads / 32),
                                                            max_ctas));

@@ -188,6 +188,9 @@ simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
  * verified token outside [0, V) (SIMSD_DEVERR_TOKEN) -> accepted_len = -1, n_commit = 0,
  * out_tokens = out_pos = -1 for that request.
  * --------------------------------------------------------------------------------- */
+/* Bytes of workspace simsd_accept needs for these sizes on the current device (the work
+ * split follows the device's resident warps). The workspace must be 256-byte aligned; its
+ * contents need no initialisation and are scratch after the call. */
 size_t simsd_accept_workspace(int batch, int B, int gamma, int V);
 
 simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
