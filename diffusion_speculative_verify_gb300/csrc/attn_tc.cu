@@ -495,6 +495,28 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
+      // When every unit is one pair, this unit's pair is known before the schedule: its
+      // first prompt tiles go into L2 now, so that the stream, which starts after the first
+      // prologue, finds them there.
+      if (cl == 1 && (int64_t)a.batch * a.Hkv == (int64_t)a.ctas) {
+        const int gb = vcta / a.Hkv, gh = vcta - (vcta / a.Hkv) * a.Hkv;
+        const int P = a.prompt_len[gb];
+        const int64_t cs = a.cache_start[gb];
+        const int n = min(kStages, (max(P, 0) + kKeys - 1) / kKeys);
+        for (int i = 0; i < n; ++i) {
+          const int tok = (int)(cs + (int64_t)i * kKeys);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (a.layout == SIMSD_CACHE_NHD) {
+              ptx::tma_prefetch_3d(&tmk, half * 64, gh, tok);
+              ptx::tma_prefetch_3d(&tmv, half * 64, gh, tok);
+            } else {
+              ptx::tma_prefetch_3d(&tmk, half * 64, tok, gh);
+              ptx::tma_prefetch_3d(&tmv, half * 64, tok, gh);
+            }
+          }
+        }
+      }
       sh->abort = 0;
       for (int i = 0; i < kStages; ++i) {
         ptx::mbar_init(bar(kFull0 + i), 1);
@@ -516,6 +538,18 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   } else {
+    {  // Before the schedule is known: this unit's likely first pair (exact when every unit
+       // is one whole pair) has its prologue rows prefetched into L2, so that the first
+       // prologue's loads hit there instead of paying a cold access after the schedule.
+      const int64_t pairs = (int64_t)a.batch * a.Hkv;
+      const int64_t gp = pairs > 0 ? ((int64_t)vcta * pairs) / a.ctas : 0;
+      const int gb = (int)(gp / a.Hkv), gh = (int)(gp % a.Hkv);
+      const int prow = row0 + tid;
+      const bool real = prow < a.R;
+      const int rw = (min(128, a.R - row0) + 31) & ~31;
+      if (gb < a.batch)
+        prefetch_prologue(a, gb, gh, 1, 2 * a.B, real ? prow / a.G : 0, real ? prow % a.G : 0, real, rw, tid);
+    }
     block_schedule(a, vcta, a.ctas, tid, sh->wsum, &sh->T, &sh->t0, &sh->t1, &sh->Tb, &sh->b);
   }
   ptx::tc_fence_before();

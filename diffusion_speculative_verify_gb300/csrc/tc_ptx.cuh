@@ -105,6 +105,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
+// Prefetch of one box of a tiled 3-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"((uint64_t)map),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 
 // ---------------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
