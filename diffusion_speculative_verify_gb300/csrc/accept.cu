@@ -33,15 +33,14 @@ constexpr int kFinishThreads = 256;
 
 struct AcceptWs {
   float2* stats;                // [batch][gamma][2][nchunk]  (max, sum exp) per chunk
-  unsigned long long* winners;  // [batch][2]  race winners: residual, target
-  unsigned* any_pos;            // [batch]     residual has a positive entry
+  unsigned long long* winners;  // [batch][2]  race winners: residual, target (0: no positive residual)
   unsigned* ticket;             // [batch]     CTAs of K3b finished
 };
 
 struct AcceptPlan {
   int nchunk_a, chunk_a;  // K3a: chunks per row, elements per chunk (multiple of 4)
   int nchunk_b, chunk_b;  // K3b: chunks per request, elements per chunk (multiple of 4)
-  size_t off_stats, off_winners, off_anypos, off_ticket, bytes;
+  size_t off_stats, off_winners, off_ticket, bytes;
 };
 
 // Warps of the stats kernel and CTAs of the finish kernel resident at once on the current
@@ -84,8 +83,6 @@ AcceptPlan make_plan(int batch, int gamma, int V) {
   off = align_up(off + (size_t)batch * gamma * 2 * p.nchunk_a * sizeof(float2), 256);
   p.off_winners = off;
   off = align_up(off + (size_t)batch * 2 * sizeof(unsigned long long), 256);
-  p.off_anypos = off;
-  off = align_up(off + (size_t)batch * sizeof(unsigned), 256);
   p.off_ticket = off;
   off = align_up(off + (size_t)batch * sizeof(unsigned), 256);
   p.bytes = off;
@@ -149,7 +146,6 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     for (int i = threadIdx.x; i < batch; i += blockDim.x) {
       ws.winners[2 * i] = 0ull;
       ws.winners[2 * i + 1] = 0ull;
-      ws.any_pos[i] = 0u;
       ws.ticket[i] = 0u;
     }
   }
@@ -266,9 +262,8 @@ __device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], 
                                            float T, bool unit_T, float mt, float inv_st, float md,
                                            float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
                                            uint32_t off_hi, uint32_t key0, uint32_t key1,
-                                           unsigned long long& best, bool& anyp) {
+                                           unsigned long long& best) {
   float key[4];
-  bool pos = false;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     // p and q rounded on their own (no fused multiply-add into p - q): where the two agree
@@ -281,9 +276,7 @@ __device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], 
       key[j] = __fsub_rn(p, q);
     }
     if (4 * g + j >= end) key[j] = on_p ? -1.f : 0.f;
-    pos |= key[j] > 0.f;
   }
-  anyp |= pos;
   // no branch around the counter block: the groups of a batch then run their Philox
   // rounds side by side (the few groups without a positive key are drawn for nothing)
   Philox4 c4 = {r, off_lo, off_hi, kResampleTag | (uint32_t)g};
@@ -305,7 +298,7 @@ __device__ __forceinline__ void race_range(const float* __restrict__ trow, const
                                            float T, bool unit_T, float mt, float inv_st, float md,
                                            float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
                                            uint32_t off_hi, uint32_t key0, uint32_t key1,
-                                           unsigned long long& best, bool& anyp) {
+                                           unsigned long long& best) {
   const int g0 = c0 / 4, g1 = c0 < c1 ? (c1 + 3) / 4 : g0;
   for (int gb = g0 + t; gb < g1; gb += 4 * nthreads) {
     float tv[4][4], dv[4][4];
@@ -335,7 +328,7 @@ __device__ __forceinline__ void race_range(const float* __restrict__ trow, const
       const int g = gb + u * nthreads;
       if (g < g1)
         race_group(g, c1, tv[u], dv[u], T, unit_T, mt, inv_st, md, inv_sd, on_p, r, off_lo,
-                   off_hi, key0, key1, best, anyp);
+                   off_hi, key0, key1, best);
     }
   }
 }
@@ -395,21 +388,39 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // merge the chunk partials of every verified (step, model) row: warp w takes rows
-  // w, w + 8, ...; its lanes stride over the chunks
-  for (int row = w; row < 2 * gamma; row += kFinishThreads / 32) {
-    const float2* src = ws.stats + ((size_t)r * gamma * 2 + row) * plan.nchunk_a;
-    float m = -INFINITY, sum = 0.f;
-    for (int c = lane; c < plan.nchunk_a; c += 32) {
-      const float2 v = src[c];
-      lse_merge(m, sum, v.x, v.y);
+  // w, w + 8, ...; all of a warp's loads are issued before any is reduced
+  constexpr int kWarps = kFinishThreads / 32;
+  constexpr int kRowsPerWarp = (2 * kMaxB + kWarps - 1) / kWarps;
+  const float2* rstats = ws.stats + (size_t)r * gamma * 2 * plan.nchunk_a;
+  for (int c0 = 0; c0 < plan.nchunk_a; c0 += 32) {
+    float2 v[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int row = w + kWarps * i, c = c0 + lane;
+      v[i] = (row < 2 * gamma && c < plan.nchunk_a) ? rstats[(size_t)row * plan.nchunk_a + c]
+                                                   : make_float2(-INFINITY, 0.f);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-      lse_merge(m, sum, m2, s2);
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int row = w + kWarps * i;
+      if (row >= 2 * gamma) break;  // warp-uniform
+      float m = v[i].x, sum = v[i].y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        lse_merge(m, sum, m2, s2);
+      }
+      if (lane == 0) {
+        if (c0 == 0) {
+          s_rowstat[row] = make_float2(m, sum);
+        } else {  // more than 32 chunks: fold into the earlier ones
+          float mm = s_rowstat[row].x, ss = s_rowstat[row].y;
+          lse_merge(mm, ss, m, sum);
+          s_rowstat[row] = make_float2(mm, ss);
+        }
+      }
     }
-    if (lane == 0) s_rowstat[row] = make_float2(m, sum);
   }
   __syncthreads();
 
@@ -469,20 +480,17 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     const int c0 = chunk * plan.chunk_b;
     const int c1 = min(V, c0 + plan.chunk_b);
     unsigned long long best_res = 0ull;
-    bool anyp = false;
     const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
     race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
-               1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res, anyp);
+               1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
       best_res = b1 > best_res ? b1 : best_res;
     }
-    anyp = __any_sync(0xffffffffu, anyp);
-    if (lane == 0) {
-      atomicMax(&ws.winners[2 * r], best_res);
-      if (anyp) atomicOr(&ws.any_pos[r], 1u);
-    }
+    // a residual entry is taken only where it is positive, and its packed key is then
+    // nonzero: a winner word still 0 at the end means the residual vanished everywhere
+    if (lane == 0 && best_res != 0ull) atomicMax(&ws.winners[2 * r], best_res);
   }
   // last CTA of this request writes the outputs
   __shared__ bool s_last;
@@ -498,16 +506,15 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __shared__ unsigned long long s_win;
   if (tid == 0) s_win = atomicAdd(&ws.winners[2 * r], 0ull);
   __syncthreads();
-  if (a < gamma && atomicAdd(&ws.any_pos[r], 0u) == 0u) {
+  if (a < gamma && s_win == 0ull) {
     // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
     // over the whole row, done here by the last CTA (never on typical inputs)
     const int k = s_order[a];
     const float* trow = target + ((size_t)r * B + k) * (size_t)V;
     unsigned long long best = 0ull;
-    bool anyp = false;
     const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
     race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
-               1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best, anyp);
+               1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -593,7 +600,6 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   AcceptWs ws;
   ws.stats = (float2*)(base + plan.off_stats);
   ws.winners = (unsigned long long*)(base + plan.off_winners);
-  ws.any_pos = (unsigned*)(base + plan.off_anypos);
   ws.ticket = (unsigned*)(base + plan.off_ticket);
   const long grid_a = (long)batch * gamma * 2 * plan.nchunk_a;
   const long grid_b = (long)batch * plan.nchunk_b;
