@@ -50,8 +50,10 @@ constexpr int kBlockRows = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
 constexpr int kMaxStages = 8;                         // stage barriers reserved in shared memory
 // Start-up and finish of one pair segment (prologue, epilogue, pipeline refill) in units of
-// one prompt tile's streaming time; the schedule charges it to every pair.
-constexpr int kSegCost = 3;
+// one prompt tile's time; the schedule charges it to every pair. It grows with the response
+// span (the RoPE table, the tail rows and the visibility masks scale with 2B): measured on
+// GB300, 2B = 16 costs about 5 tiles and 2B = 64 about 8 to 10.
+static int seg_cost_tiles(int twoB) { return 4 + twoB / 16; }
 constexpr int kPrefetchAhead = 4;  // tiles before a segment's end at which the next one is prefetched
 
 
@@ -1204,7 +1206,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.G = p->Hq / p->Hkv;
   a.R = rows_per_pair(p);
   a.tile_keys = r128::kKeys;
-  a.seg_cost = kSegCost;
+  a.seg_cost = seg_cost_tiles(2 * p->B);
   a.cl = cluster_size(p);
   a.ctas = grid_ctas(p, a.cl);
   a.layout = (int)p->cache_layout;
