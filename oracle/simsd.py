@@ -200,9 +200,22 @@ def _order_from_labels(labels_row, B):
     return order
 
 
+def greedy_choice(logits):
+    """The target's own deterministic next token at temperature 0: the first index of the
+    largest logit (SPOT page, verification step of Algorithm 2: at T = 0 the target's
+    transition is Phi_0)."""
+    return int(np.argmax(np.asarray(logits, dtype=np.float64)))
+
+
 def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
            seed, offset, requests=None, request_ids=None):
     """Speculative acceptance along the draft's time order, then residual resampling.
+
+    temperature == 0 is greedy verification (SPOT page, Algorithm 2 and its verification
+    paragraph: at T = 0 the target's own next commit is the deterministic Phi_0; an edge is
+    accepted iff the draft agrees with it, otherwise the target's own result is
+    committed): step r is accepted iff x = argmax of the target logits at k; at the first
+    mismatch the committed token is that argmax. Draft logits and uniforms are unused.
 
     For steps r = 1..gamma: slot k = o_r, x = draft token at k, p = softmax(target
     logits at k / T), q = softmax(draft logits at k / T); accept if p_x >= q_x, else
@@ -226,6 +239,7 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
     err = 0
     diag = {}
     req_list = range(b) if requests is None else requests
+    greedy = float(temperature) == 0.0
     for r in req_list:
         order = _order_from_labels(labels[r], B)
         if order is None:
@@ -236,6 +250,22 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
             err |= ERR_TOKEN
             continue
         rid = r if request_ids is None else int(request_ids[r])
+        if greedy:
+            a = 0
+            for k in steps:
+                if int(toks[r, k]) != greedy_choice(tl[r, k]):
+                    break
+                a += 1
+            for step in range(a):
+                out_tokens[r, step] = int(toks[r, steps[step]])
+                out_pos[r, step] = steps[step]
+            if a < gamma:
+                out_tokens[r, a] = greedy_choice(tl[r, steps[a]])
+                out_pos[r, a] = steps[a]
+            acc_len[r] = a
+            n_commit[r] = a + (1 if a < gamma else 0)
+            diag[r] = {"margins": [], "race_top2": None}
+            continue
         u = philox.accept_uniforms(seed, offset, rid, gamma)
         a = 0
         margins = []

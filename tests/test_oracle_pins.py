@@ -348,6 +348,63 @@ def test_temperature_scales_logits():
     np.testing.assert_allclose(p_t2, p_half, atol=1e-15)
 
 
+# ------------------------------------------- greedy verification (temperature 0)
+def _greedy_case(seed, b=8, B=6, V=60):
+    """Target logits with a clear winner per row (gap >= 3: every other entry of the fp64
+    softmax at T = 1e-3 underflows to 0), a greedy drafter (draft token = argmax of the
+    draft logits) that agrees with the target on a random prefix of steps."""
+    rng = np.random.default_rng(seed)
+    tl = rng.standard_normal((b, B, V)) * 2
+    dl = tl + rng.standard_normal((b, B, V))
+    for r in range(b):
+        for k in range(B):
+            tl[r, k, int(np.argmax(tl[r, k]))] += 3.0
+            dl[r, k, int(np.argmax(dl[r, k]))] += 3.0
+    tau = [list(rng.permutation(B) + 1) for _ in range(b)]
+    for r in range(b):
+        agree = int(rng.integers(0, B + 1))
+        for t in range(1, B + 1):
+            k = tau[r].index(t)
+            if t <= agree:
+                dl[r, k] = tl[r, k]            # the drafter's choice is the target's
+            elif int(np.argmax(dl[r, k])) == int(np.argmax(tl[r, k])):
+                w = (int(np.argmax(tl[r, k])) + 1) % V
+                dl[r, k, w] = dl[r, k].max() + 3.0
+    toks = np.argmax(dl, axis=-1)
+    return tl, dl, toks, tau
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_greedy_is_the_zero_temperature_limit_of_the_stochastic_rule(seed):
+    # at T -> 0 p and q are one-hot; min(1, p/q) accepts exactly when the draft token is
+    # the target's argmax, and the residual max(0, p - q) is one-hot on that argmax, so
+    # the race commits it: the fp64 softmax + race path at T = 1e-3 must agree with the
+    # argmax path at T = 0 on every output
+    tl, dl, toks, tau = _greedy_case(seed)
+    B = tl.shape[1]
+    cold = _accept_case(tl, dl, toks, tau, B, T=1e-3)
+    greedy = _accept_case(tl, dl, toks, tau, B, T=0.0)
+    for key in ("accepted_len", "n_commit", "out_tokens", "out_pos"):
+        np.testing.assert_array_equal(greedy[key], cold[key])
+    assert 0 < int(greedy["accepted_len"].sum()) < B * tl.shape[0]   # both branches used
+
+
+def test_greedy_ignores_draft_logits_and_seed_and_takes_the_first_maximum():
+    B, V = 3, 12
+    tl = np.zeros((1, B, V))
+    tl[0, :, 5] = 2.0
+    tl[0, :, 9] = 2.0                          # tie: the first index (5) is the choice
+    toks = np.array([[5, 9, 5]])
+    base = _accept_case(tl, np.zeros_like(tl), toks, [[1, 2, 3]], B, seed=1, T=0.0)
+    assert base["accepted_len"][0] == 1
+    assert base["out_tokens"][0].tolist() == [5, 5, -1]
+    assert base["out_pos"][0].tolist() == [0, 1, -1]
+    other = _accept_case(tl, np.random.default_rng(3).standard_normal(tl.shape), toks,
+                         [[1, 2, 3]], B, seed=77, offset=5, T=0.0)
+    for key in ("accepted_len", "n_commit", "out_tokens", "out_pos"):
+        np.testing.assert_array_equal(base[key], other[key])
+
+
 # ----------------------------------------------- P8: Monte Carlo, lossless accept
 def test_monte_carlo_commits_follow_target_and_mean_length_closed_form():
     from scipy import stats
