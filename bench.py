@@ -49,20 +49,30 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="override the workload's sampling temperature (0: greedy verification)")
     return ap.parse_args()
+
+
+def _workload(args):
+    import workloads
+    w = workloads.WORKLOADS[args.workload]
+    return w if args.temperature is None else w.with_(temperature=args.temperature)
 
 
 # ------------------------------------------------------------------------ CPU side
 def _oracle_sample(job):
     """Runs the oracle on `n` freshly generated single-request copies of the workload
     (same shapes and distributions) and returns (tokens, seconds)."""
-    name, first_seed, n, deadline = job
+    name, first_seed, n, deadline, temperature = job
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     import torch
     torch.set_num_threads(1)
     import oracle
     import workloads
     w = workloads.WORKLOADS[name]
+    if temperature is not None:
+        w = w.with_(temperature=temperature)
     tokens, spent = 0, 0.0
     for i in range(n):
         if time.time() > deadline and i > 0:
@@ -97,7 +107,7 @@ def _oracle_pool(cores):
     return mp.get_context("spawn").Pool(cores)
 
 
-def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000):
+def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000, temperature=None):
     """tokens/s of the oracle over all host cores (one single-threaded worker per core,
     each timing only its own oracle calls; input generation is not timed)."""
     cores = cores or len(os.sched_getaffinity(0))
@@ -106,7 +116,7 @@ def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000)
         pool = _oracle_pool(cores)
     try:
         deadline = time.time() + seconds
-        jobs = [(name, first_seed + 10000 * c, 10 ** 6, deadline) for c in range(cores)]
+        jobs = [(name, first_seed + 10000 * c, 10 ** 6, deadline, temperature) for c in range(cores)]
         t0 = time.perf_counter()
         res = pool.map(_oracle_sample, jobs)
         wall = time.perf_counter() - t0
@@ -133,15 +143,15 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import workloads
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
     cores = len(os.sched_getaffinity(0))
     per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     vals = []
     t0 = time.perf_counter()
     with _oracle_pool(cores) as pool:
         for k in range(args.warmup + args.steps):
-            v = cpu_oracle_throughput(args.workload, per_step, cores, pool, 1000 + 97 * k)
+            v = cpu_oracle_throughput(args.workload, per_step, cores, pool, 1000 + 97 * k,
+                                      args.temperature)
             if k >= args.warmup:
                 vals.append(v)
     elapsed = time.perf_counter() - t0
@@ -409,7 +419,7 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
 
     from diffusion_speculative_verify_gb300 import _build
     if rank == 0 or not os.path.exists(pkg.LIB_PATH):
@@ -524,7 +534,7 @@ def run_ours(args):
     # ---- CPU baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds)
+        cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds, temperature=args.temperature)
 
     # layout; attention (the tensor-core kernel and its split merge, or the fp32 / D 64
     # kernel alone); accept_stats and accept_finish

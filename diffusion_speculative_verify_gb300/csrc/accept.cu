@@ -53,9 +53,10 @@ int resident_finish_ctas();
 // whose items fill the warps' last round to at least 97 % (the kernel's time is set by the
 // warps that take the most items), else the best fill; chunks stay at least 512 entries.
 // K3b takes one wave of CTAs, nchunk_b per request.
-AcceptPlan make_plan(int batch, int gamma, int V) {
+// `models` = 2 (target and draft rows: sampling) or 1 (target rows only: greedy).
+AcceptPlan make_plan(int batch, int gamma, int V, int models = 2) {
   AcceptPlan p;
-  const long rows = (long)batch * gamma * 2;
+  const long rows = (long)batch * gamma * models;
   const long W = std::max(1, resident_stat_warps());
   const long ncmax = std::max<long>(1, (V + 511) / 512);
   long best_nc = 1;
@@ -80,7 +81,7 @@ AcceptPlan make_plan(int batch, int gamma, int V) {
   p.chunk_b = (int)(((V + nb - 1) / nb + 3) / 4 * 4);
   size_t off = 0;
   p.off_stats = off;
-  off = align_up(off + (size_t)batch * gamma * 2 * p.nchunk_a * sizeof(float2), 256);
+  off = align_up(off + (size_t)batch * gamma * models * p.nchunk_a * sizeof(float2), 256);
   p.off_winners = off;
   off = align_up(off + (size_t)batch * 2 * sizeof(unsigned long long), 256);
   p.off_ticket = off;
@@ -541,6 +542,169 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   }
 }
 
+// ------------------------------------------------------------------ greedy (T = 0)
+// Greedy verification (SPOT page, Algorithm 2, verification at T = 0): the target's own
+// choice at a slot is its first largest logit; a step is accepted iff the draft token is
+// that choice, and at the first mismatch the choice is committed. Two launches: an argmax
+// pass over the verified target rows (one warp per (row, chunk) item, (max, first index)
+// per chunk) and a finish kernel with one warp per request.
+constexpr int kArgmaxThreads = 256;
+constexpr int kNoIndex = 0x7fffffff;
+
+// (value, index) of the first maximum: a larger value wins, an equal one the smaller index.
+__device__ __forceinline__ void argmax_merge(float& m, int& i, float m2, int i2) {
+  if (i2 == kNoIndex) return;
+  if (i == kNoIndex || m2 > m || (m2 == m && i2 < i)) {
+    m = m2;
+    i = i2;
+  }
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
+    const float* __restrict__ target, const uint8_t* __restrict__ labels, int batch, int B,
+    int gamma, int V, AcceptPlan plan, AcceptWs ws) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long warp_global = (long)blockIdx.x * (kArgmaxThreads / 32) + (threadIdx.x >> 5);
+  const long nwarps = (long)gridDim.x * (kArgmaxThreads / 32);
+  const int nchunk = plan.nchunk_a;
+  const long items = (long)batch * gamma * nchunk;
+  const bool vec_ok = (V & 3) == 0 && (((uintptr_t)target) & 15) == 0;
+  for (long item = warp_global; item < items; item += nwarps) {
+    const int chunk = (int)(item % nchunk);
+    const long row = item / nchunk;
+    const int step = (int)(row % gamma);
+    const int r = (int)(row / gamma);
+    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
+    float m = -INFINITY;
+    int mi = kNoIndex;
+    const int c0 = chunk * plan.chunk_a;
+    const int len = min(plan.chunk_a, V - c0);
+    if (hit && len > 0) {
+      const float* rowp = target + ((size_t)r * B + (__ffs(hit) - 1)) * (size_t)V + c0;
+      // a lane visits its entries in increasing index, so a strict '>' keeps the first
+      // maximum (the first non-NaN entry starts the scan, even at -inf)
+      if (vec_ok) {  // batches of 16 float4 loads per lane in flight
+        constexpr int kPerA = 16;
+        const float4* src = reinterpret_cast<const float4*>(rowp);
+        const int n4 = len >> 2;
+        for (int base = 0; base < n4; base += 32 * kPerA) {
+          float4 x[kPerA];
+#pragma unroll
+          for (int u = 0; u < kPerA; ++u) {
+            const int i4 = base + lane + 32 * u;
+            x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+#pragma unroll
+          for (int u = 0; u < kPerA; ++u) {
+            const int i4 = base + lane + 32 * u;
+            if (i4 >= n4) break;
+            const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (xv[j] > m || (mi == kNoIndex && xv[j] == xv[j])) {
+                m = xv[j];
+                mi = c0 + 4 * i4 + j;
+              }
+          }
+        }
+      } else {
+        for (int v = lane; v < len; v += 32) {
+          const float x = rowp[v];
+          if (x > m || (mi == kNoIndex && x == x)) {
+            m = x;
+            mi = c0 + v;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, mi, o);
+      argmax_merge(m, mi, m2, i2);
+    }
+    if (lane == 0) ws.stats[item] = make_float2(m, __int_as_float(mi));
+  }
+}
+
+// One warp per request; launched as a programmatic dependent of the argmax pass.
+__global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
+    const int32_t* __restrict__ tokens, const uint8_t* __restrict__ labels, int batch, int B,
+    int gamma, int V, AcceptPlan plan, AcceptWs ws, int32_t* __restrict__ accepted_len,
+    int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_pos,
+    int32_t* __restrict__ n_commit, uint32_t* __restrict__ dev_err) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int r = blockIdx.x * 8 + w;
+  __shared__ int s_order[8][kMaxB];
+  // labels, order and draft tokens before the grid dependency wait (they are not the
+  // argmax pass's results)
+  int bad = 0, k = 0, x = 0;
+  if (r < batch) {
+    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : 0;
+    const int tau = lb & 0x7F;
+    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau >= 1 && tau <= B);
+    const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
+    const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
+    const unsigned full = B == 32 ? 0xffffffffu : ((1u << B) - 1u);
+    const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
+    if (perm && lane < B) s_order[w][tau - 1] = lane;
+    __syncwarp();
+    bad = perm ? 0 : (int)SIMSD_DEVERR_TAU;
+    if (perm && lane < gamma) {
+      k = s_order[w][lane];
+      x = tokens[(size_t)r * B + k];
+    }
+    if (__any_sync(0xffffffffu, perm && lane < gamma && (x < 0 || x >= V))) bad |= (int)SIMSD_DEVERR_TOKEN;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (r >= batch) return;  // warp-uniform
+  if (bad) {
+    if (lane == 0) {
+      atomicOr(dev_err, (uint32_t)bad);
+      accepted_len[r] = -1;
+      n_commit[r] = 0;
+    }
+    if (lane < B) {
+      out_tokens[(size_t)r * B + lane] = -1;
+      out_pos[(size_t)r * B + lane] = -1;
+    }
+    return;
+  }
+  // lane t < gamma: the target's choice at step t, merged over the row's chunks
+  float m = -INFINITY;
+  int choice = kNoIndex;
+  if (lane < gamma) {
+    const float2* src = ws.stats + ((size_t)r * gamma + lane) * plan.nchunk_a;
+    for (int c = 0; c < plan.nchunk_a; ++c) {
+      const float2 v = src[c];
+      argmax_merge(m, choice, v.x, __float_as_int(v.y));
+    }
+    if (choice == kNoIndex) choice = 0;  // a row of NaNs only
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && x != choice);
+  const int a = rej ? (__ffs(rej) - 1) : gamma;
+  const int choice_a = __shfl_sync(0xffffffffu, choice, a < gamma ? a : 0);
+  if (lane < B) {
+    int tok = -1, pos = -1;
+    if (lane < a) {
+      pos = s_order[w][lane];
+      tok = tokens[(size_t)r * B + pos];
+    } else if (lane == a && a < gamma) {
+      pos = s_order[w][a];
+      tok = choice_a;
+    }
+    out_tokens[(size_t)r * B + lane] = tok;
+    out_pos[(size_t)r * B + lane] = pos;
+  }
+  if (lane == 0) {
+    accepted_len[r] = a;
+    n_commit[r] = a + (a < gamma ? 1 : 0);
+  }
+}
+
 // Resident blocks per SM of `kernel` x SMs of the current device, cached per device.
 template <typename K>
 int resident_blocks(K kernel, int threads, int* cache) {
@@ -573,7 +737,8 @@ int resident_finish_ctas() {
 
 SIMSD_API size_t simsd_accept_workspace(int batch, int B, int gamma, int V) {
   if (batch < 0 || B < 1 || gamma < 1 || gamma > B || V < 1) return 0;
-  return simsd::make_plan(batch, gamma, V).bytes;
+  // enough for both the sampling path and the greedy one
+  return std::max(simsd::make_plan(batch, gamma, V, 2).bytes, simsd::make_plan(batch, gamma, V, 1).bytes);
 }
 
 SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
@@ -587,13 +752,13 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;
   if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
-  if (temperature == 0.f) return SIMSD_ERR_UNSUPPORTED;
   if (batch == 0) return SIMSD_OK;
   if (!target_logits || !draft_logits || !draft_tokens || !labels || !accepted_len ||
       !out_tokens || !out_pos || !n_commit || !dev_err)
     return SIMSD_ERR_INVALID_ARG;
   if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
-  const AcceptPlan plan = make_plan(batch, gamma, V);
+  const bool greedy = temperature == 0.f;
+  const AcceptPlan plan = make_plan(batch, gamma, V, greedy ? 1 : 2);
   if (!workspace || workspace_bytes < plan.bytes || (((uintptr_t)workspace) & 255))
     return SIMSD_ERR_WORKSPACE;
   char* base = (char*)workspace;
@@ -605,6 +770,32 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   const long grid_b = (long)batch * plan.nchunk_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
+  if (greedy) {  // argmax pass over the verified target rows, then one warp per request
+    const long warps_g = (long)batch * gamma * plan.nchunk_a;
+    const long max_g = std::max(1, resident_stat_warps() / (kStatThreads / 32));
+    const long grid_g = std::max<long>(1, std::min<long>((warps_g + kArgmaxThreads / 32 - 1) / (kArgmaxThreads / 32), max_g));
+    accept_argmax_kernel<<<(unsigned)grid_g, kArgmaxThreads, 0, s>>>(target_logits, labels, batch, B, gamma,
+                                                                     V, plan, ws);
+    simsd_status st = last_launch_status();
+    if (st != SIMSD_OK) return st;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)((batch + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_greedy_finish_kernel, draft_tokens, labels, batch,
+                                             B, gamma, V, plan, ws, accepted_len, out_tokens, out_pos,
+                                             n_commit, dev_err);
+    if (e != cudaSuccess) {
+      record_cuda_error("cudaLaunchKernelEx(accept_greedy_finish_kernel)", e);
+      return SIMSD_ERR_CUDA;
+    }
+    return last_launch_status();
+  }
   // persistent grid: as many stats CTAs as can be resident at once (fewer if the items are
   // fewer than the resident warps)
   const long max_ctas = std::max(1, resident_stat_warps() / (kStatThreads / 32));
@@ -689,7 +880,7 @@ SIMSD_API simsd_status simsd_accept_noalloc(const float* target_logits, const fl
   using namespace simsd;
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;
-  if (batch > 0 && make_plan(batch, gamma, V).bytes > kNoAllocScratchBytes)
+  if (batch > 0 && make_plan(batch, gamma, V, temperature == 0.f ? 1 : 2).bytes > kNoAllocScratchBytes)
     return SIMSD_ERR_WORKSPACE;  // these sizes need more scratch than the fixed array holds
   void* scratch = nullptr;
   if (batch > 0) {

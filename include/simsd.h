@@ -183,8 +183,11 @@ simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
  *   n_commit                     int32 [batch]     a + (a < gamma), or 0
  *   out_tokens                   int32 [batch, B]  committed tokens in step order, -1 after
  *   out_pos                      int32 [batch, B]  their slot indices, -1 after
- * Requires 1 <= gamma <= B <= 32, V >= 1, temperature > 0 (T = 0 is
- * SIMSD_ERR_UNSUPPORTED). Data errors: labels not a permutation (SIMSD_DEVERR_TAU) or a
+ * temperature = 0 is greedy verification [SPOT-G] (the SPOT page's Algorithm 2, which
+ * verifies at T = 0 against the target's own deterministic commit): step t is accepted iff
+ * x_t is the first index of the largest target logit at o_t, and at the first mismatch
+ * that index is committed; draft logits, seed and offset are unused.
+ * Requires 1 <= gamma <= B <= 32, V >= 1, temperature >= 0. Data errors: labels not a permutation (SIMSD_DEVERR_TAU) or a
  * verified token outside [0, V) (SIMSD_DEVERR_TOKEN) -> accepted_len = -1, n_commit = 0,
  * out_tokens = out_pos = -1 for that request.
  * --------------------------------------------------------------------------------- */

@@ -303,6 +303,49 @@ def _accept_outputs(path, tl, dl, toks, labels, gamma, T, seed, ws=None):
     return {k: v.cpu().numpy() for k, v in out.items()}, int(err.item())
 
 
+def _slot_order(labels_row, B):
+    tau = [int(x) & 0x7F for x in labels_row[:B]]
+    return [tau.index(t) for t in range(1, B + 1)]
+
+
+@pytest.mark.parametrize("path", ["workspace", "fixed"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "gqa8b_bf16", "large_block_bf16"])
+def test_accept_greedy_bit_exact(name, path):
+    """Greedy verification (temperature 0) against the oracle, bit-exact: draft tokens
+    agree with the target's first-maximum choice on a prefix of every length 0..gamma, and
+    some rows hold an exact tie of their maximum at an index half the vocabulary away
+    (another chunk), so the first-index rule is exercised across the chunk merge."""
+    w = W[name]
+    inputs, meta = H.make_case(w, seed=31)
+    st = _step(w, inputs, meta, with_lse=False)
+    b, B, V = inputs["target_logits"].shape
+    tl = inputs["target_logits"].clone()
+    labels = H.to_np(st.labels)
+    tl_cpu = tl.cpu().numpy()
+    for r in range(0, b, 3):                      # ties: the maximum copied elsewhere
+        for k in range(B):
+            c = int(np.argmax(tl_cpu[r, k]))
+            far = (c + V // 2) % V
+            tl_cpu[r, k, far] = tl_cpu[r, k, c]
+    tl.copy_(torch.from_numpy(tl_cpu))
+    toks = inputs["draft_tokens"].cpu().clone()
+    for r in range(b):
+        order = _slot_order(labels[r], B)
+        L = r % (w.gamma + 1)
+        for t in range(w.gamma):
+            k = order[t]
+            c = oracle.greedy_choice(tl_cpu[r, k])
+            toks[r, k] = c if t < L else (c + 1 + r) % V
+    toks = toks.cuda()
+    case = dict(inputs, target_logits=tl, draft_tokens=toks)
+    res = H.oracle_accept(case, st.labels, w.gamma, 0.0, meta["philox_seed"], 0)
+    got, err = _accept_outputs(path, tl, inputs["draft_logits"], toks, st.labels, w.gamma, 0.0,
+                               meta["philox_seed"])
+    assert err == 0
+    assert H.check_accept(res, got, list(range(b))) == 0
+    assert set(res["accepted_len"].tolist()) == set(range(min(b, w.gamma + 1)))
+
+
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 1.0), ("gqa8b_bf16", 1.0),
                                     ("gqa8b_bf16", 0.7)])
 def test_accept_fixed_scratch_entry_bit_exact(name, T):

@@ -60,9 +60,11 @@ def test_host_argument_errors_return_status(lib):
     assert lib.simsd_build_layout(None, None, 4, 33, None, None, None, None) == 1
     assert lib.simsd_build_layout(None, None, 4, 4, None, None, None, None) == 1
     assert lib.simsd_build_layout(None, None, 0, 4, None, None, None, None) == 0
-    # temperature 0 (greedy) is not implemented; gamma > B is invalid
+    # temperature 0 (greedy) is accepted, a negative one is not; gamma > B is invalid
     args = [None] * 4 + [2, 4, 4, 100, 0.0, 0, 0] + [None] * 4 + [None, 0, None, None]
-    assert lib.simsd_accept(*args) == 2
+    assert lib.simsd_accept(*args) == 1          # null pointers
+    args[8] = -1.0
+    assert lib.simsd_accept(*args) == 1
     args[8] = 1.0
     args[6] = 5
     assert lib.simsd_accept(*args) == 1

@@ -148,17 +148,20 @@ def make_attention_inputs(w: Workload, prompt_len: torch.Tensor, seed: Optional[
 def make_accept_inputs(w: Workload, seed: Optional[int] = None, device="cpu",
                        V: Optional[int] = None):
     """Target / draft logits [b, B, V] fp32 (indexed by block slot k), draft tokens
-    [b, B] int32 drawn from the draft distribution at temperature T, and a Philox
-    (seed, offset) pair for the acceptance uniforms."""
+    [b, B] int32 drawn from the draft distribution at temperature T (its argmax at T = 0),
+    and a Philox (seed, offset) pair for the acceptance uniforms."""
     seed = w.seed if seed is None else seed
     V = w.V if V is None else V
     g = _gen(seed + 2, device)
     b, B = w.batch, w.B
     target = torch.randn(b, B, V, generator=g, device=device) * w.logit_std
     draft = target + torch.randn(b, B, V, generator=g, device=device) * w.draft_noise_std
-    probs = torch.softmax(draft.reshape(b * B, V) / w.temperature, dim=-1)
-    tokens = torch.multinomial(probs, 1, generator=g).reshape(b, B).to(torch.int32)
-    del probs
+    if w.temperature == 0:   # a greedy drafter proposes its own first maximum
+        tokens = torch.argmax(draft, dim=-1).to(torch.int32)
+    else:
+        probs = torch.softmax(draft.reshape(b * B, V) / w.temperature, dim=-1)
+        tokens = torch.multinomial(probs, 1, generator=g).reshape(b, B).to(torch.int32)
+        del probs
     return {"target_logits": target, "draft_logits": draft, "draft_tokens": tokens,
             "philox_seed": 0x5EED0000 + int(seed), "philox_offset": 0}
 
@@ -166,13 +169,14 @@ def make_accept_inputs(w: Workload, seed: Optional[int] = None, device="cpu",
 def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor) -> dict:
     """Minimum HBM bytes of one verification step: each input read once, each
     output written once (per request: the prompt K/V, the 2B-row Q/K/V/O, and the
-    target+draft logit rows of the gamma verified slots)."""
+    target+draft logit rows of the gamma verified slots; the target rows only at
+    temperature 0, where greedy verification reads no draft logits)."""
     esz = 4 if w.dtype == "fp32" else 2
     P_sum = int(prompt_len.to(torch.int64).sum())
     b, B, D = w.batch, w.B, w.D
     kv_prompt = 2 * P_sum * w.Hkv * D * esz
     resp = b * 2 * B * D * esz * (2 * w.Hq + 2 * w.Hkv)   # q + out, k + v
-    accept = b * w.gamma * 2 * w.V * 4
+    accept = b * w.gamma * (1 if w.temperature == 0 else 2) * w.V * 4
     flops = 0
     for P in prompt_len.tolist():
         flops += 4 * 2 * B * w.Hq * (P + B) * D
