@@ -10,7 +10,10 @@ Each function restates a definition from the pages, in their notation:
 * layout    -- SimSD notes, "关键设计" items 1 and 3 (paired data/mask layout; RoPE copy);
                gist.science SimSD summary, sections 1 and 3.
 * mask      -- SimSD notes, item 2, the four-case equation for A_ij; step labels tau are
-               a permutation of 1..B (gist.science summary, section 2, "Mapa de Passo").
+               a permutation of 1..B (gist.science summary, section 2, "Mapa de Passo");
+               in a later round of the same block, slots committed earlier carry tau = 0
+               like the prompt, and the R remaining positions (SimSD notes, item 4) a
+               permutation of 1..R.
 * attention -- one softmax-attention layer over [prompt | D | D~] under A_ij, with the
                RoPE ids of D~_k copied from D_k (SimSD notes items 2-3).
 * accept    -- SimSD notes item 4, equation for alpha_r = min(1, p_theta / p_phi), walked in
@@ -23,7 +26,9 @@ Readings taken where the pages are silent (all listed in the design notes):
   prompt tokens carry tau = 0 and are visible to every response row; RoPE pairs are
   half-split (d, d + D/2) with omega_d = theta^(-2d/D); the prompt keys arrive already
   rotated; softmax scale 1/sqrt(D); q-head h uses kv-head h // G; every slot of D and
-  D~ is computed; no bonus token when all gamma drafts are accepted.
+  D~ is computed; no bonus token when all gamma drafts are accepted; a request with
+  R < gamma remaining positions (which the SimSD notes hand to the regular denoising path)
+  verifies its R steps.
 """
 from __future__ import annotations
 
@@ -49,9 +54,11 @@ def build_layout(tau, prompt_len):
 
     Position ids: prompt token j -> j (implicit); D_k -> P + k; D~_k copies D_k's id
     (0-based k). Labels: one byte per response slot, (segment << 7) | tau, segment 0
-    for D and 1 for D~. A request whose tau is not a permutation of 1..B, or whose
-    prompt length is negative, gets pos = -1 and labels = 0xFF on all 2B slots and
-    raises the matching error bit.
+    for D and 1 for D~. tau = 0 marks a slot committed in an earlier round of the same
+    block (its token is known, like the prompt's); the other slots' labels must be a
+    permutation of 1..R, R = their count (R = B in a block's first round). A request
+    breaking this, or with a negative prompt length, gets pos = -1 and labels = 0xFF on
+    all 2B slots and raises the matching error bit.
     """
     tau = np.asarray(tau, dtype=np.int64)
     prompt_len = np.asarray(prompt_len, dtype=np.int64)
@@ -62,7 +69,8 @@ def build_layout(tau, prompt_len):
     for r in range(b):
         P = int(prompt_len[r])
         bad = 0
-        if sorted(tau[r].tolist()) != list(range(1, B + 1)):
+        open_steps = sorted(t for t in tau[r].tolist() if t != 0)
+        if any(t < 0 or t > B for t in tau[r].tolist()) or open_steps != list(range(1, len(open_steps) + 1)):
             bad |= ERR_TAU
         if P < 0:
             bad |= ERR_PROMPT_LEN
@@ -187,16 +195,18 @@ def softmax(logits, temperature):
 
 
 def _order_from_labels(labels_row, B):
-    """o_r = the slot whose step label is r (r = 1..B), or None if the D half is not a
-    permutation of 1..B."""
+    """o_r = the slot whose step label is r (r = 1..R, R = the slots not committed in an
+    earlier round), or None if those labels are not a permutation of 1..R."""
     if int(labels_row[0]) == INVALID_LABEL:
         return None
     tau = [int(x) & 0x7F for x in labels_row[:B]]
-    if sorted(tau) != list(range(1, B + 1)):
+    open_steps = sorted(t for t in tau if t != 0)
+    if open_steps != list(range(1, len(open_steps) + 1)):
         return None
-    order = [0] * B
+    order = [0] * len(open_steps)
     for k, t in enumerate(tau):
-        order[t - 1] = k
+        if t:
+            order[t - 1] = k
     return order
 
 
@@ -210,6 +220,9 @@ def greedy_choice(logits):
 def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
            seed, offset, requests=None, request_ids=None):
     """Speculative acceptance along the draft's time order, then residual resampling.
+
+    A request verifies gamma_r = min(gamma, R) steps, R = its slots not committed in an
+    earlier round (tau != 0); n_commit = a + [a < gamma_r].
 
     temperature == 0 is greedy verification (SPOT page, Algorithm 2 and its verification
     paragraph: at T = 0 the target's own next commit is the deterministic Phi_0; an edge is
@@ -259,11 +272,11 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
             for step in range(a):
                 out_tokens[r, step] = int(toks[r, steps[step]])
                 out_pos[r, step] = steps[step]
-            if a < gamma:
+            if a < len(steps):
                 out_tokens[r, a] = greedy_choice(tl[r, steps[a]])
                 out_pos[r, a] = steps[a]
             acc_len[r] = a
-            n_commit[r] = a + (1 if a < gamma else 0)
+            n_commit[r] = a + (1 if a < len(steps) else 0)
             diag[r] = {"margins": [], "race_top2": None}
             continue
         u = philox.accept_uniforms(seed, offset, rid, gamma)
@@ -284,7 +297,7 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
             out_tokens[r, step] = int(toks[r, steps[step]])
             out_pos[r, step] = steps[step]
         race = None
-        if a < gamma:
+        if a < len(steps):
             k = steps[a]
             p = softmax(tl[r, k], temperature)
             q = softmax(dl[r, k], temperature)
@@ -299,7 +312,7 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
             out_tokens[r, a] = y
             out_pos[r, a] = k
         acc_len[r] = a
-        n_commit[r] = a + (1 if a < gamma else 0)
+        n_commit[r] = a + (1 if a < len(steps) else 0)
         diag[r] = {"margins": margins, "race_top2": race}
     return {"accepted_len": acc_len, "n_commit": n_commit, "out_tokens": out_tokens,
             "out_pos": out_pos, "err": err, "diag": diag}

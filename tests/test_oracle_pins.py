@@ -163,6 +163,99 @@ def test_single_forward_equals_explicit_denoising_states(B):
                     np.testing.assert_allclose(out[0, i, hq], ref, rtol=0, atol=1e-12)
 
 
+def _partial_label_sets(B):
+    """Every label vector of a later round of a B-slot block: a set of committed slots
+    (tau = 0) and a permutation of 1..R on the others."""
+    for committed in itertools.product([False, True], repeat=B):
+        open_slots = [k for k in range(B) if not committed[k]]
+        for perm in itertools.permutations(range(1, len(open_slots) + 1)):
+            tau = [0] * B
+            for k, t in zip(open_slots, perm):
+                tau[k] = t
+            yield tau
+
+
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_later_rounds_equal_explicit_denoising_states(B):
+    # a slot committed in an earlier round (tau = 0) holds its token in every state, like
+    # the prompt: the brute-force rebuild below marks it decided for every row of step >= 1
+    rng = np.random.default_rng(40 + B)
+    Hq, Hkv, D, P, theta = 2, 1, 8, 3, 100.0
+    scale = 1.0 / math.sqrt(D)
+    n = 0
+    for tau in _partial_label_sets(B):
+        if all(t == 0 for t in tau) or all(t != 0 for t in tau):
+            continue
+        n += 1
+        case = _random_case(rng, 1, B, Hq, Hkv, D, [P], taus=np.array([tau]))
+        out, _ = _run(case, theta)
+        q_rot = _complex_rope(case["q"][0], np.array(case["pos_ids"][0], float), theta)
+        pos_slot = (P + np.arange(B)).astype(float)
+        kD = _complex_rope(case["k_resp"][0, :B], pos_slot, theta)
+        kM = _complex_rope(case["k_resp"][0, B:], pos_slot, theta)
+        vD, vM = case["v_resp"][0, :B], case["v_resp"][0, B:]
+        for i in range(2 * B):
+            t = tau[i % B]
+            if t == 0:
+                continue          # rows of committed slots are not predictions
+            decided = [(tau[k] < t) if i >= B else (tau[k] <= t) for k in range(B)]
+            K = np.concatenate([case["k_cache"][:P, 0],
+                                np.stack([kD[k, 0] if decided[k] else kM[k, 0] for k in range(B)])])
+            Vv = np.concatenate([case["v_cache"][:P, 0],
+                                 np.stack([vD[k, 0] if decided[k] else vM[k, 0] for k in range(B)])])
+            for hq in range(Hq):
+                ref = _softmax_attend(q_rot[i, hq], K, Vv, scale)
+                np.testing.assert_allclose(out[0, i, hq], ref, rtol=0, atol=1e-12)
+    assert n > 0
+
+
+def test_layout_of_later_rounds():
+    taus = np.array([[0, 2, 0, 1], [0, 0, 0, 0], [3, 0, 1, 2], [0, 2, 3, 0], [1, 1, 0, 2], [5, 0, 1, 2]])
+    pos, labels, err = oracle.build_layout(taus, np.array([4, 4, 4, 4, 4, 4]))
+    assert err == oracle.ERR_TAU                 # rows 3 (gap), 4 (duplicate), 5 (> B)
+    assert labels[0].tolist() == [0, 2, 0, 1, 128, 130, 128, 129]
+    assert labels[1].tolist() == [0, 0, 0, 0, 128, 128, 128, 128]
+    assert pos[0].tolist() == [4, 5, 6, 7, 4, 5, 6, 7]
+    for r in (3, 4, 5):
+        assert (labels[r] == oracle.INVALID_LABEL).all() and (pos[r] == -1).all()
+
+
+def test_later_round_accepts_like_the_block_of_its_open_slots():
+    # committed slots take no part in acceptance: the block with committed slots and the
+    # smaller block made of its open slots alone (same step labels, same request ids, so
+    # the same uniforms) give the same decisions and commits
+    rng = np.random.default_rng(12)
+    b, B, V = 5, 6, 40
+    tl = rng.standard_normal((b, B, V)) * 2
+    dl = tl + rng.standard_normal((b, B, V)) * 0.7
+    toks = rng.integers(0, V, (b, B))
+    taus, subs = [], []
+    for r in range(b):
+        open_slots = sorted(rng.choice(B, size=int(rng.integers(1, B + 1)), replace=False).tolist())
+        perm = rng.permutation(len(open_slots)) + 1
+        tau = [0] * B
+        for k, t in zip(open_slots, perm):
+            tau[k] = int(t)
+        taus.append(tau)
+        subs.append(open_slots)
+    for T in (1.0, 0.0):
+        gamma = B
+        full = _accept_case(tl, dl, toks, taus, gamma, seed=4, T=T)
+        for r in range(b):
+            sl = subs[r]
+            R = len(sl)
+            _, lab, err = oracle.build_layout(np.array([[taus[r][k] for k in sl]]), np.zeros(1, int))
+            assert err == 0
+            sub = oracle.accept(tl[r:r + 1, sl], dl[r:r + 1, sl], toks[r:r + 1, sl], lab, R, T, 4, 0,
+                                request_ids=[r])
+            assert full["accepted_len"][r] == sub["accepted_len"][0] <= R
+            assert full["n_commit"][r] == sub["n_commit"][0]
+            n = int(sub["n_commit"][0])
+            assert full["out_tokens"][r, :n].tolist() == sub["out_tokens"][0, :n].tolist()
+            assert full["out_pos"][r, :n].tolist() == [sl[k] for k in sub["out_pos"][0, :n]]
+            assert (full["out_pos"][r, n:] == -1).all()
+
+
 # ------------------------------------------------------ P2: perturbation invariance
 def test_perturbing_invisible_slots_leaves_prediction_rows_unchanged():
     rng = np.random.default_rng(2)
