@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   const bool unit_T = (T == 1.f);
 
   __shared__ int s_order[kMaxB];
-  __shared__ int s_a, s_bad;
+  __shared__ int s_a, s_bad, s_gr;
   __shared__ float s_mt, s_st, s_md, s_sd;
   __shared__ float2 s_rowstat[2 * kMaxB];  // merged (max, sum exp) per (step, model)
 
@@ -356,26 +356,30 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   // it overlaps K3a's last items: warp 0 checks the step labels, orders the steps, and loads
   // each verified step's draft token, the two logits at that token and its uniform.
   int bad_w = 0, k_w = 0, x_w = 0;  // warp 0: error bits, slot and token of step `lane`
+  int gr_w = gamma;                 // warp 0: steps verified, min(gamma, R)
   float tx = 0.f, dx = 0.f, u = 0.f;
   if (w == 0) {
     // step labels of the data half -> order o_t; validity of the permutation
+    // labels 1..R of the open slots (0: committed in an earlier round) -> order o_t
     const uint8_t lb = lane < B ? lab[lane] : 0;
     const int tau = lb & 0x7F;
-    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau >= 1 && tau <= B);
+    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau <= B);
+    const int R = __popc(__ballot_sync(0xffffffffu, lane < B && tau != 0));
     const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
     const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
-    const unsigned full = B == 32 ? 0xffffffffu : ((1u << B) - 1u);
+    const unsigned full = R == 32 ? 0xffffffffu : ((1u << R) - 1u);
     const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
-    if (perm && lane < B) s_order[tau - 1] = lane;
+    if (perm && lane < B && tau != 0) s_order[tau - 1] = lane;
     __syncwarp();
     bad_w = perm ? 0 : (int)SIMSD_DEVERR_TAU;
-    if (perm && lane < gamma) {
+    gr_w = min(gamma, R);
+    if (perm && lane < gr_w) {
       k_w = s_order[lane];
       x_w = tokens[(size_t)r * B + k_w];
     }
-    const bool tok_bad = perm && lane < gamma && (x_w < 0 || x_w >= V);
+    const bool tok_bad = perm && lane < gr_w && (x_w < 0 || x_w >= V);
     if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
-    if (!bad_w && lane < gamma) {
+    if (!bad_w && lane < gr_w) {
       const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
       tx = scale_logit(target[rowoff], T, unit_T);
       dx = scale_logit(draft[rowoff], T, unit_T);
@@ -426,11 +430,11 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __syncthreads();
 
   if (w == 0) {
-    int a = gamma;
+    int a = gr_w;
     if (!bad_w) {
       bool acc = true;
       float mt = 0.f, st = 0.f, md = 0.f, sd = 0.f;
-      if (lane < gamma) {
+      if (lane < gr_w) {
         const float2 rt = s_rowstat[2 * lane], rd = s_rowstat[2 * lane + 1];
         mt = rt.x;
         st = rt.y;
@@ -440,9 +444,9 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
         const float qx = __fdiv_rn(expf(dx - md), sd);
         acc = (px >= qx) || (u * qx < px);
       }
-      const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && !acc);
-      a = rej ? (__ffs(rej) - 1) : gamma;
-      if (a < gamma && lane == a) {
+      const unsigned rej = __ballot_sync(0xffffffffu, lane < gr_w && !acc);
+      a = rej ? (__ffs(rej) - 1) : gr_w;
+      if (a < gr_w && lane == a) {
         s_mt = mt;
         s_st = st;
         s_md = md;
@@ -452,11 +456,13 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     if (lane == 0) {
       s_a = a;
       s_bad = bad_w;
+      s_gr = gr_w;
     }
   }
   __syncthreads();
   const int a = s_a;
   const int bad = s_bad;
+  const int gr = s_gr;  // steps this request verifies
   if (bad) {
     if (chunk == 0) {
       if (tid == 0) {
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     return;
   }
 
-  if (a < gamma) {
+  if (a < gr) {
     // exponential race over this CTA's chunk of the rejected slot's vocabulary
     const int k = s_order[a];
     const float mt = s_mt, st = s_st, md = s_md, sd = s_sd;
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   __shared__ unsigned long long s_win;
   if (tid == 0) s_win = atomicAdd(&ws.winners[2 * r], 0ull);
   __syncthreads();
-  if (a < gamma && s_win == 0ull) {
+  if (a < gr && s_win == 0ull) {
     // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
     // over the whole row, done here by the last CTA (never on typical inputs)
     const int k = s_order[a];
@@ -529,7 +535,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     if (tid < a) {
       pos = s_order[tid];
       tok = tokens[(size_t)r * B + pos];
-    } else if (tid == a && a < gamma) {
+    } else if (tid == a && a < gr) {
       pos = s_order[a];
       tok = unpack_token(s_win);
     }
@@ -538,7 +544,7 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
   }
   if (tid == 0) {
     accepted_len[r] = a;
-    n_commit[r] = a + (a < gamma ? 1 : 0);
+    n_commit[r] = a + (a < gr ? 1 : 0);
   }
 }
 
@@ -641,23 +647,26 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
   __shared__ int s_order[8][kMaxB];
   // labels, order and draft tokens before the grid dependency wait (they are not the
   // argmax pass's results)
-  int bad = 0, k = 0, x = 0;
+  int bad = 0, k = 0, x = 0, gr = gamma;  // gr: steps verified, min(gamma, R)
   if (r < batch) {
+    // labels 1..R of the open slots (0: committed in an earlier round) -> order o_t
     const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : 0;
     const int tau = lb & 0x7F;
-    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau >= 1 && tau <= B);
+    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau <= B);
+    const int R = __popc(__ballot_sync(0xffffffffu, lane < B && tau != 0));
     const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
     const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
-    const unsigned full = B == 32 ? 0xffffffffu : ((1u << B) - 1u);
+    const unsigned full = R == 32 ? 0xffffffffu : ((1u << R) - 1u);
     const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
-    if (perm && lane < B) s_order[w][tau - 1] = lane;
+    if (perm && lane < B && tau != 0) s_order[w][tau - 1] = lane;
     __syncwarp();
     bad = perm ? 0 : (int)SIMSD_DEVERR_TAU;
-    if (perm && lane < gamma) {
+    gr = min(gamma, R);
+    if (perm && lane < gr) {
       k = s_order[w][lane];
       x = tokens[(size_t)r * B + k];
     }
-    if (__any_sync(0xffffffffu, perm && lane < gamma && (x < 0 || x >= V))) bad |= (int)SIMSD_DEVERR_TOKEN;
+    if (__any_sync(0xffffffffu, perm && lane < gr && (x < 0 || x >= V))) bad |= (int)SIMSD_DEVERR_TOKEN;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (r >= batch) return;  // warp-uniform
@@ -676,7 +685,7 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
   // lane t < gamma: the target's choice at step t, merged over the row's chunks
   float m = -INFINITY;
   int choice = kNoIndex;
-  if (lane < gamma) {
+  if (lane < gr) {
     const float2* src = ws.stats + ((size_t)r * gamma + lane) * plan.nchunk_a;
     for (int c = 0; c < plan.nchunk_a; ++c) {
       const float2 v = src[c];
@@ -684,15 +693,15 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
     }
     if (choice == kNoIndex) choice = 0;  // a row of NaNs only
   }
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && x != choice);
-  const int a = rej ? (__ffs(rej) - 1) : gamma;
-  const int choice_a = __shfl_sync(0xffffffffu, choice, a < gamma ? a : 0);
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < gr && x != choice);
+  const int a = rej ? (__ffs(rej) - 1) : gr;
+  const int choice_a = __shfl_sync(0xffffffffu, choice, a < gr ? a : 0);
   if (lane < B) {
     int tok = -1, pos = -1;
     if (lane < a) {
       pos = s_order[w][lane];
       tok = tokens[(size_t)r * B + pos];
-    } else if (lane == a && a < gamma) {
+    } else if (lane == a && a < gr) {
       pos = s_order[w][a];
       tok = choice_a;
     }
@@ -701,7 +710,7 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
   }
   if (lane == 0) {
     accepted_len[r] = a;
-    n_commit[r] = a + (a < gamma ? 1 : 0);
+    n_commit[r] = a + (a < gr ? 1 : 0);
   }
 }
 

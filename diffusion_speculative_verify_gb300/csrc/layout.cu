@@ -3,7 +3,9 @@
 // SimSD notes (papernotes.org), "关键设计" items 1-3: the response part of the input is
 // [D_1..D_B | D~_1..D~_B]; D_k holds the draft token, D~_k is the [MASK] prediction slot
 // bound to it; every response slot carries a step label tau in 1..B (a permutation, per
-// the gist.science summary, section 2), and D~_k reuses the position id of D_k.
+// the gist.science summary, section 2), and D~_k reuses the position id of D_k. In a later
+// round of the same block the slots committed earlier carry tau = 0, like the prompt
+// (item 2), and the R remaining positions (item 4) a permutation of 1..R.
 // No mask is materialised: labels are enough to evaluate A_ij on the fly.
 #include "common.cuh"
 
@@ -19,12 +21,14 @@ __global__ void __launch_bounds__(128) build_layout_kernel(
   const bool active = lane < B;
   const int t = active ? tau[(size_t)r * B + lane] : 0;
   const int P = prompt_len[r];
-  // tau is a permutation of 1..B  <=>  every value lies in 1..B and the B values cover
-  // all of 1..B (B values, B distinct bits set).
-  const bool in_range = !active || (t >= 1 && t <= B);
+  // tau = 0 marks a slot committed in an earlier round of the block; the R other labels
+  // must be a permutation of 1..R  <=>  every value lies in 0..B and the R nonzero values
+  // set R distinct bits, the bits of 1..R.
+  const bool in_range = !active || (t >= 0 && t <= B);
+  const int R = __popc(__ballot_sync(0xffffffffu, active && t != 0));
   const unsigned bit = (active && t >= 1 && t <= B) ? (1u << (t - 1)) : 0u;
   const unsigned covered = __reduce_or_sync(0xffffffffu, bit);
-  const unsigned full = (B == 32) ? 0xffffffffu : ((1u << B) - 1u);
+  const unsigned full = (R == 32) ? 0xffffffffu : ((1u << R) - 1u);
   const bool perm_ok = __all_sync(0xffffffffu, in_range) && covered == full;
   uint32_t bad = 0;
   if (!perm_ok) bad |= SIMSD_DEVERR_TAU;

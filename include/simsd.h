@@ -59,7 +59,7 @@ typedef enum {
 } simsd_status;
 
 /* Bits of the device error word. */
-#define SIMSD_DEVERR_TAU 1u        /* tau of a request is not a permutation of 1..B     */
+#define SIMSD_DEVERR_TAU 1u        /* tau of a request: open labels not 1..R, or > B    */
 #define SIMSD_DEVERR_PROMPT_LEN 2u /* prompt length < 0                                 */
 #define SIMSD_DEVERR_TOKEN 4u      /* a verified draft token id is outside [0, V)       */
 #define SIMSD_DEVERR_TIMEOUT 8u    /* a bounded wait inside a kernel gave up            */
@@ -95,12 +95,16 @@ const char* simsd_last_cuda_error(void);
  *   labels[r][B + k]  = 0x80 | tau[r][k]     (segment 1, mask)
  * Prompt tokens have tau = 0 and positions 0..P_r-1 implicitly; no mask is stored.
  *
- *   tau        int32 [batch, B]   step label of each slot; must be a permutation of 1..B
+ *   tau        int32 [batch, B]   step label of each slot: a permutation of 1..B in a
+ *                                 block's first round; in a later round 0 marks a slot
+ *                                 committed earlier (seen like the prompt, [SimSD-2]) and
+ *                                 the R open slots carry a permutation of 1..R ([SimSD-4]:
+ *                                 the remaining positions)
  *   prompt_len int32 [batch]      prompt length P_r >= 0
  *   pos_ids    int32 [batch, 2B]  output
  *   labels     uint8 [batch, 2B]  output
  *   dev_err    uint32 [1]         error word, bits OR-ed in (never cleared here)
- * Data errors: a request whose tau is not a permutation of 1..B (SIMSD_DEVERR_TAU) or
+ * Data errors: a request whose tau breaks that rule (SIMSD_DEVERR_TAU) or
  * whose P_r < 0 (SIMSD_DEVERR_PROMPT_LEN) gets pos_ids = -1 and labels = 0xFF.
  * Returns SIMSD_ERR_INVALID_ARG for null pointers, batch < 0, B < 1 or B > 32.
  * --------------------------------------------------------------------------------- */
@@ -163,11 +167,12 @@ simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
  * simsd_accept  [SimSD-4], [SimSD-P] section 4, [S2D2-5], [SPOT-G].
  *
  * For each request r, with o_t = the slot whose step label is t (from labels' data
- * half) and x_t = draft_tokens[r][o_t], for t = 1..gamma:
+ * half) and x_t = draft_tokens[r][o_t], for t = 1..gamma_r, gamma_r = min(gamma, R_r)
+ * (R_r = the request's open slots, B in a block's first round):
  *   p = softmax(target_logits[r][o_t] / T), q = softmax(draft_logits[r][o_t] / T)
  *   accept step t iff p[x_t] >= q[x_t] or u_t * q[x_t] < p[x_t]; stop at the first
  *   rejection. accepted_len = a (number of leading accepted steps).
- * If a < gamma, slot o_{a+1} is resampled from the normalised residual max(0, p - q)
+ * If a < gamma_r, slot o_{a+1} is resampled from the normalised residual max(0, p - q)
  * by the exponential race y = argmax_v r_v / E_v, E_v = -ln(u_v) (ties -> smallest v;
  * if the residual is zero everywhere the race runs on p). No extra token is drawn when
  * all gamma steps are accepted.
@@ -180,7 +185,7 @@ simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
  *   draft_tokens                 int32 [batch, B], token of data slot k
  *   labels                       uint8 [batch, 2B] from simsd_build_layout
  *   accepted_len                 int32 [batch]     a, or -1 for a rejected request
- *   n_commit                     int32 [batch]     a + (a < gamma), or 0
+ *   n_commit                     int32 [batch]     a + (a < gamma_r), or 0
  *   out_tokens                   int32 [batch, B]  committed tokens in step order, -1 after
  *   out_pos                      int32 [batch, B]  their slot indices, -1 after
  * temperature = 0 is greedy verification [SPOT-G] (the SPOT page's Algorithm 2, which

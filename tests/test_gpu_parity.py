@@ -66,7 +66,7 @@ def test_layout_invalid_requests_and_block_32():
     rng = np.random.default_rng(0)
     tau = np.stack([rng.permutation(B) + 1 for _ in range(5)])
     tau[1, 3] = tau[1, 4]          # duplicate
-    tau[2, 0] = 0                  # out of range
+    tau[2, 0] = 0                  # a committed slot: valid only if 1..31 remain
     tau[3, 7] = 33
     plen = np.array([10, 20, 30, 40, -5])
     pos = torch.empty(5, 2 * B, dtype=torch.int32, device="cuda")
@@ -78,6 +78,38 @@ def test_layout_invalid_requests_and_block_32():
     assert np.array_equal(pos.cpu().numpy(), rp)
     assert np.array_equal(lab.cpu().numpy(), rl)
     assert int(err.item()) == re_ == (oracle.ERR_TAU | oracle.ERR_PROMPT_LEN)
+
+
+def _later_round_taus(rng, b, B, invalid_every=0):
+    """Label vectors of later rounds: a random set of committed slots (tau = 0) and a
+    permutation of 1..R on the rest; every `invalid_every`-th one gets a gap (invalid)."""
+    taus = []
+    for r in range(b):
+        n_open = int(rng.integers(1, B + 1))
+        open_slots = rng.choice(B, size=n_open, replace=False)
+        tau = np.zeros(B, dtype=np.int64)
+        tau[open_slots] = rng.permutation(n_open) + 1
+        if invalid_every and r % invalid_every == invalid_every - 1 and n_open < B:
+            tau[tau == n_open] = n_open + 1          # labels 1..R-1, R+1: a gap
+        taus.append(tau)
+    return np.stack(taus)
+
+
+@pytest.mark.parametrize("B", [4, 8, 32])
+def test_layout_later_rounds_bit_exact(B):
+    rng = np.random.default_rng(B)
+    b = 64
+    tau = _later_round_taus(rng, b, B, invalid_every=5)
+    plen = rng.integers(0, 500, b)
+    pos = torch.empty(b, 2 * B, dtype=torch.int32, device="cuda")
+    lab = torch.empty(b, 2 * B, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _pkg().simsd_build_layout(torch.tensor(tau, dtype=torch.int32).cuda(),
+                              torch.tensor(plen, dtype=torch.int32).cuda(), pos, lab, err)
+    rp, rl, re_ = oracle.build_layout(tau, plen)
+    assert np.array_equal(pos.cpu().numpy(), rp)
+    assert np.array_equal(lab.cpu().numpy(), rl)
+    assert int(err.item()) == re_ == oracle.ERR_TAU
 
 
 # -------------------------------------------------------------------------- attention
@@ -151,6 +183,44 @@ def test_attention_bf16_cluster_partial_second_block(Hq, Hkv, B):
     st = _step(w, inputs, meta)
     _attention_parity(w, inputs, meta, st)
     assert int(st.dev_err.item()) == 0
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_attention_bf16_later_rounds(B):
+    # committed slots (tau = 0) are seen by every open row through their data slot and by
+    # none through their mask slot
+    w = MEDIUM.with_(B=B, gamma=B)
+    tau = _later_round_taus(np.random.default_rng(50 + B), w.batch, B)
+    inputs, meta = H.make_case(w, seed=B, prompt_len=[0, 61, 128, 1000 + 37], tau=tau)
+    st = _step(w, inputs, meta)
+    assert int(st.dev_err.item()) == 0
+    _attention_parity(w, inputs, meta, st)
+
+
+def test_attention_fp32_later_rounds():
+    w = W["tiny_fp32"].with_(batch=3, Hq=4, Hkv=2, D=128, B=8, gamma=8, rope_theta=1e6)
+    tau = _later_round_taus(np.random.default_rng(7), 3, 8)
+    inputs, meta = H.make_case(w, seed=9, prompt_len=[0, 33, 777], tau=tau)
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_accept_later_rounds_bit_exact(T):
+    """Later rounds verify min(gamma, R) steps of their R open slots (gamma = B here, so
+    most requests verify fewer than gamma)."""
+    w = W["gqa8b_bf16"].with_(B=8, gamma=8, batch=24, temperature=T)
+    tau = _later_round_taus(np.random.default_rng(11), w.batch, w.B)
+    inputs, meta = H.make_case(w, seed=13, tau=tau)
+    st = _step(w, inputs, meta, with_lse=False)
+    res = H.oracle_accept(inputs, st.labels, w.gamma, T, meta["philox_seed"], 0)
+    got, err = _accept_outputs("workspace", inputs["target_logits"], inputs["draft_logits"],
+                               inputs["draft_tokens"], st.labels, w.gamma, T, meta["philox_seed"])
+    assert err == 0
+    reqs = list(range(w.batch))
+    assert H.check_accept(res, got, reqs) <= 1
+    R = (tau != 0).sum(axis=1)
+    assert (got["accepted_len"] <= R).all() and (got["n_commit"] <= R).all()
 
 
 def test_attention_bf16_identity_tau_and_d64():
