@@ -5,6 +5,6 @@ may import this package. It is independent of the CUDA library: the two share no
 code, and neither imports the other.
 """
 from .simsd import (ERR_PROMPT_LEN, ERR_TAU, ERR_TOKEN, INVALID_LABEL, SEG_DATA,  # noqa: F401
-                    SEG_MASK, accept, build_layout, greedy_choice, rope, softmax,
-                    temporal_causal_mask, verify_attention)
+                    SEG_MASK, accept, accept_coupled, build_layout, coupled_choice,
+                    greedy_choice, rope, softmax, temporal_causal_mask, verify_attention)
 from . import philox  # noqa: F401

@@ -16,6 +16,8 @@ give only the distributions):
   key      = (seed & 0xffffffff, seed >> 32)
   accept   counter = (request, offset_lo, offset_hi, j)          words 0..3 -> steps 4j..4j+3
   resample counter = (request, offset_lo, offset_hi, 0x80000000 | (v >> 2))  word v & 3 -> token v
+  noise    counter = (request, position, offset_lo, 0x40000000 | (v >> 2))  word v & 3 -> the
+           shared Gumbel noise of token v at absolute output position `position`
   uniform  u = (2 * (w >> 9) + 1) * 2**-24, an odd multiple of 2**-24 in (0, 1); exactly
            representable in fp32 and fp64, so both sides see the same value.
 """
@@ -29,6 +31,7 @@ W0 = 0x9E3779B9
 W1 = 0xBB67AE85
 MASK32 = 0xFFFFFFFF
 RESAMPLE_TAG = 0x80000000
+NOISE_TAG = 0x40000000
 
 
 def philox4x32_10(counter, key):
@@ -101,5 +104,19 @@ def resample_uniforms(seed, offset, request, V):
     ctr[:, 1] = offset & MASK32
     ctr[:, 2] = offset >> 32
     ctr[:, 3] = RESAMPLE_TAG | np.arange(calls, dtype=np.uint32)
+    words = philox4x32_10(ctr, _key(seed)).reshape(-1)[:V]
+    return word_to_uniform(words)
+
+
+def noise_uniforms(seed, offset, request, position, V):
+    """Uniforms u_{a,v}, v = 0..V-1, behind the shared Gumbel noise of one request at
+    absolute output position a (only the low 32 bits of the offset enter)."""
+    offset = int(offset) & 0xFFFFFFFFFFFFFFFF
+    calls = (V + 3) // 4
+    ctr = np.zeros((calls, 4), dtype=np.uint32)
+    ctr[:, 0] = request
+    ctr[:, 1] = int(position) & MASK32
+    ctr[:, 2] = offset & MASK32
+    ctr[:, 3] = NOISE_TAG | np.arange(calls, dtype=np.uint32)
     words = philox4x32_10(ctr, _key(seed)).reshape(-1)[:V]
     return word_to_uniform(words)

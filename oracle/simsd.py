@@ -217,6 +217,75 @@ def greedy_choice(logits):
     return int(np.argmax(np.asarray(logits, dtype=np.float64)))
 
 
+def coupled_choice(logits, temperature, seed, offset, request, position):
+    """The target's own transition under the shared noise table (SPOT page, "Gumbel-Max
+    技巧与随机耦合" and the coupled-noise verification of Algorithm 2): with p =
+    softmax(logits / T) and Gumbel noise G_{a,v} = -ln(-ln u_{a,v}) indexed by the
+    absolute output position a, Phi_G = argmax_v (log p_v + G_{a,v}), which by the
+    Gumbel-max identity is a sample of p. log p_v differs from logits_v / T by a constant,
+    so the keys are logits_v / T + G_{a,v}. Returns (token, gap between the two largest
+    keys). T = 0 is Phi_0, the first maximum of the logits (gap: of the logits)."""
+    z = np.asarray(logits, dtype=np.float64)
+    if float(temperature) == 0.0:
+        keys = z
+    else:
+        u = philox.noise_uniforms(seed, offset, request, position, z.shape[-1])
+        keys = z / float(temperature) - np.log(-np.log(u))
+    y = int(np.argmax(keys))          # first maximum
+    top2 = np.sort(keys)[-2:] if keys.shape[-1] > 1 else np.array([-np.inf, keys[0]])
+    return y, float(top2[1] - top2[0])
+
+
+def accept_coupled(target_logits, draft_tokens, labels, pos_ids, gamma, temperature, seed,
+                   offset, requests=None, request_ids=None):
+    """Coupled-noise verification (SPOT page, Algorithm 2 and the coupled-noise
+    verification paragraph): the drafter and the target share the Gumbel noise table,
+    conditioned on which the target's transition Phi_G is deterministic; step r (slot
+    k = o_r, absolute position a = pos_ids[k]) is accepted iff the draft token equals
+    Phi_G at k, and at the first mismatch the target's own Phi_G is committed. Verifies
+    min(gamma, R) steps like `accept`. No draft logits are read."""
+    tl = np.asarray(target_logits)
+    toks = np.asarray(draft_tokens)
+    labels = np.asarray(labels)
+    pos_ids = np.asarray(pos_ids)
+    b, B, V = tl.shape
+    acc_len = np.full(b, -1, dtype=np.int32)
+    n_commit = np.zeros(b, dtype=np.int32)
+    out_tokens = np.full((b, B), -1, dtype=np.int32)
+    out_pos = np.full((b, B), -1, dtype=np.int32)
+    err = 0
+    diag = {}
+    req_list = range(b) if requests is None else requests
+    for r in req_list:
+        order = _order_from_labels(labels[r], B)
+        if order is None:
+            err |= ERR_TAU
+            continue
+        steps = order[:gamma]
+        if any(not (0 <= int(toks[r, k]) < V) for k in steps):
+            err |= ERR_TOKEN
+            continue
+        rid = r if request_ids is None else int(request_ids[r])
+        a, gaps, choice = 0, [], None
+        for k in steps:
+            choice, gap = coupled_choice(tl[r, k], temperature, seed, offset, rid, int(pos_ids[r, k]))
+            gaps.append(gap)
+            if int(toks[r, k]) != choice:
+                break
+            a += 1
+        for step in range(a):
+            out_tokens[r, step] = int(toks[r, steps[step]])
+            out_pos[r, step] = steps[step]
+        if a < len(steps):
+            out_tokens[r, a] = choice
+            out_pos[r, a] = steps[a]
+        acc_len[r] = a
+        n_commit[r] = a + (1 if a < len(steps) else 0)
+        diag[r] = {"key_gaps": gaps}
+    return {"accepted_len": acc_len, "n_commit": n_commit, "out_tokens": out_tokens,
+            "out_pos": out_pos, "err": err, "diag": diag}
+
+
 def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
            seed, offset, requests=None, request_ids=None):
     """Speculative acceptance along the draft's time order, then residual resampling.

@@ -498,6 +498,62 @@ def test_greedy_ignores_draft_logits_and_seed_and_takes_the_first_maximum():
         np.testing.assert_array_equal(base[key], other[key])
 
 
+# ------------------------------------------ coupled-noise verification (SPOT page)
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_coupled_choice_is_a_sample_of_p(T):
+    # Gumbel-max identity (SPOT page, "Gumbel-Max 技巧与随机耦合"): over independent noise
+    # rows (one per absolute position) argmax_v (log p_v + G_v) follows p
+    z = np.array([1.2, -0.3, 0.4, 2.0, -1.1, 0.0])
+    p = oracle.softmax(z, T)
+    n = 20000
+    counts = np.zeros(len(z))
+    for a in range(n):
+        counts[oracle.coupled_choice(z, T, 7, 3, 0, a)[0]] += 1
+    sigma = np.sqrt(p * (1 - p) / n)
+    assert np.all(np.abs(counts / n - p) < 4.5 * sigma + 1e-4)
+
+
+def test_coupled_drafter_agreement_meets_the_total_variation_bound():
+    # SPOT page, same section: under shared noise two samplers of p and q agree with
+    # probability at least (1 - delta) / (1 + delta), delta = TV(p, q)
+    rng = np.random.default_rng(4)
+    V, n = 12, 6000
+    zt = rng.standard_normal(V) * 1.5
+    zd = zt + rng.standard_normal(V) * 0.8
+    p, q = oracle.softmax(zt, 1.0), oracle.softmax(zd, 1.0)
+    delta = 0.5 * np.abs(p - q).sum()
+    agree = sum(oracle.coupled_choice(zt, 1.0, 5, 0, 2, a)[0] == oracle.coupled_choice(zd, 1.0, 5, 0, 2, a)[0]
+                for a in range(n))
+    bound = (1 - delta) / (1 + delta)
+    assert agree / n >= bound - 4.0 * math.sqrt(bound * (1 - bound) / n)
+    assert agree / n <= 1.0 - delta + 4.0 * math.sqrt(delta * (1 - delta) / n)   # never above 1 - TV
+
+
+def test_coupled_verification_at_small_temperature_is_greedy():
+    tl, dl, toks, tau = _greedy_case(3)
+    b, B, V = tl.shape
+    pos, labels, err = oracle.build_layout(np.array(tau), np.full(b, 9))
+    assert err == 0
+    cold = oracle.accept_coupled(tl, toks, labels, pos, B, 1e-3, 11, 0)
+    greedy = oracle.accept(tl, dl, toks, labels, B, 0.0, 11, 0)
+    for key in ("accepted_len", "n_commit", "out_tokens", "out_pos"):
+        np.testing.assert_array_equal(cold[key], greedy[key])
+
+
+def test_coupled_verification_with_the_target_as_drafter_accepts_everything():
+    rng = np.random.default_rng(6)
+    b, B, V = 4, 5, 30
+    tl = rng.standard_normal((b, B, V)) * 2
+    tau = [list(rng.permutation(B) + 1) for _ in range(b)]
+    pos, labels, _ = oracle.build_layout(np.array(tau), np.array([0, 3, 17, 40]))
+    toks = np.array([[oracle.coupled_choice(tl[r, k], 0.8, 9, 1, r, pos[r, k])[0] for k in range(B)]
+                     for r in range(b)])
+    res = oracle.accept_coupled(tl, toks, labels, pos, B, 0.8, 9, 1)
+    assert res["accepted_len"].tolist() == [B] * b
+    other = oracle.accept_coupled(tl, toks, labels, pos, B, 0.8, 10, 1)   # other noise
+    assert other["accepted_len"].sum() < B * b
+
+
 # ----------------------------------------------- P8: Monte Carlo, lossless accept
 def test_monte_carlo_commits_follow_target_and_mean_length_closed_form():
     from scipy import stats
