@@ -51,6 +51,8 @@ def _args():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--temperature", type=float, default=None,
                     help="override the workload's sampling temperature (0: greedy verification)")
+    ap.add_argument("--coupled", action="store_true",
+                    help="coupled-noise verification (simsd_accept_coupled) instead of rejection sampling")
     return ap.parse_args()
 
 
@@ -183,6 +185,8 @@ def _config(w, args, launch):
     else:
         cfg["P_range"] = list(w.prompt_len_range)
     cfg["launch"] = launch
+    cfg["verification"] = "coupled noise" if getattr(args, "coupled", False) else (
+        "greedy" if w.temperature == 0 else "rejection sampling")
     return cfg
 
 
@@ -434,8 +438,9 @@ def run_ours(args):
     sets = _make_sets(w, args, device, n_sets, rank)
     steps = [pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
                             temperature=w.temperature, cache_layout=args.cache_layout,
-                            philox_seed=s["_seed"]) for s in sets]
-    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"]) for s in sets]
+                            philox_seed=s["_seed"], coupled=args.coupled) for s in sets]
+    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled)
+            for s in sets]
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()
 
@@ -514,8 +519,11 @@ def run_ours(args):
         call_bytes = {"attention": mean_alg["attn_bytes"], "accept": mean_alg["accept_bytes"]}
         dom = max(call_bytes, key=lambda k: per_call[k])
         achieved = call_bytes[dom] / per_call[dom] / 1e9
-        roofline = {"bound": "hbm", "kernel": "simsd_accept (accept_stats + accept_finish)"
-                    if dom == "accept" else "simsd_verify_attention",
+        accept_kernels = ("simsd_accept_coupled (accept_argmax with coupled noise + accept_greedy_finish)"
+                          if args.coupled else
+                          "simsd_accept (accept_argmax + accept_greedy_finish)" if w.temperature == 0 else
+                          "simsd_accept (accept_stats + accept_finish)")
+        roofline = {"bound": "hbm", "kernel": accept_kernels if dom == "accept" else "simsd_verify_attention",
                     "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": _traffic(w.name, dom),
                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",

@@ -11,13 +11,14 @@ import torch
 
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
                        DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, LIB_PATH, AttnParams,
-                       SimsdError, load_library, make_attn_params, simsd_accept,
+                       SimsdError, load_library, make_attn_params, simsd_accept, simsd_accept_coupled,
                        simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
                        simsd_accept_workspace, simsd_build_layout, simsd_last_cuda_error, simsd_status_str,
                        simsd_verify_attention, simsd_verify_attention_workspace,
                        simsd_version)
 
 __all__ = ["VerifyStep", "simsd_build_layout", "simsd_verify_attention", "simsd_accept",
+           "simsd_accept_coupled",
            "simsd_verify_attention_workspace", "simsd_accept_workspace", "make_attn_params",
            "load_library", "SimsdError"]
 
@@ -33,7 +34,7 @@ class VerifyStep:
 
     def __init__(self, inputs: dict, gamma: int, rope_theta: float, temperature: float = 1.0,
                  cache_layout: str = "NHD", softmax_scale: float = 0.0, with_lse: bool = True,
-                 philox_seed: int = 0, philox_offset: int = 0):
+                 philox_seed: int = 0, philox_offset: int = 0, coupled: bool = False):
         load_library()
         dev = inputs["q"].device
         b, twoB, Hq, D = inputs["q"].shape
@@ -41,6 +42,7 @@ class VerifyStep:
         V = inputs["target_logits"].shape[-1]
         self.b, self.B, self.V, self.gamma = b, B, V, gamma
         self.temperature = temperature
+        self.coupled = coupled  # coupled-noise verification instead of rejection sampling
         self.seed, self.offset = philox_seed, philox_offset
         self.inputs = inputs
         self.pos_ids = torch.empty(b, twoB, dtype=torch.int32, device=dev)
@@ -75,6 +77,12 @@ class VerifyStep:
 
     def accept(self, stream=None):
         i = self.inputs
+        if self.coupled:
+            simsd_accept_coupled(i["target_logits"], i["draft_tokens"], self.labels, self.pos_ids,
+                                 self.gamma, self.temperature, self.seed, self.offset,
+                                 self.accepted_len, self.out_tokens, self.out_pos, self.n_commit,
+                                 self.ws_accept, self.dev_err, stream)
+            return
         simsd_accept(i["target_logits"], i["draft_logits"], i["draft_tokens"], self.labels,
                      self.gamma, self.temperature, self.seed, self.offset, self.accepted_len,
                      self.out_tokens, self.out_pos, self.n_commit, self.ws_accept,

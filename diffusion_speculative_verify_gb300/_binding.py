@@ -24,8 +24,8 @@ CACHE_NHD, CACHE_HND = 0, 1
 
 EXPORTED = ["simsd_status_str", "simsd_version", "simsd_last_cuda_error", "simsd_build_layout",
             "simsd_verify_attention_workspace", "simsd_verify_attention",
-            "simsd_accept_workspace", "simsd_accept", "simsd_accept_noalloc",
-            "simsd_accept_noalloc_max_scratch"]
+            "simsd_accept_workspace", "simsd_accept", "simsd_accept_coupled",
+            "simsd_accept_noalloc", "simsd_accept_noalloc_max_scratch"]
 
 
 class SimsdError(RuntimeError):
@@ -80,6 +80,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.simsd_accept.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                  vp, vp, vp, vp, vp, sz, vp, vp]
     lib.simsd_accept.restype = i32
+    lib.simsd_accept_coupled.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
+                                         vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.simsd_accept_coupled.restype = i32
     lib.simsd_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                          vp, vp, vp, vp, vp, vp]
     lib.simsd_accept_noalloc.restype = i32
@@ -208,6 +211,28 @@ def simsd_accept(target_logits, draft_logits, draft_tokens, labels, gamma, tempe
         _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream(stream))
     _raise(st, "simsd_accept")
+
+
+def simsd_accept_coupled(target_logits, draft_tokens, labels, pos_ids, gamma, temperature,
+                         seed, offset, accepted_len, out_tokens, out_pos, n_commit, workspace,
+                         dev_err, stream=None):
+    """Coupled-noise verification: target logits, draft tokens and the layout's labels and
+    position ids in, the same outputs as simsd_accept."""
+    _check(target_logits, "target_logits", torch.float32)
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(labels, "labels", torch.uint8)
+    _check(pos_ids, "pos_ids", torch.int32)
+    for t, n in ((accepted_len, "accepted_len"), (out_tokens, "out_tokens"),
+                 (out_pos, "out_pos"), (n_commit, "n_commit"), (dev_err, "dev_err")):
+        _check(t, n, torch.int32)
+    _check(workspace, "workspace", torch.uint8)
+    b, B, V = target_logits.shape
+    st = load_library().simsd_accept_coupled(
+        _ptr(target_logits), _ptr(draft_tokens), _ptr(labels), _ptr(pos_ids), b, B,
+        int(gamma), V, float(temperature), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+        _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(stream))
+    _raise(st, "simsd_accept_coupled")
 
 
 def simsd_accept_noalloc_max_scratch() -> int:

@@ -566,9 +566,27 @@ __device__ __forceinline__ void argmax_merge(float& m, int& i, float m2, int i2)
   }
 }
 
+// Key of entry v: the logit at T = 0 (greedy); with `noise`, the coupled-noise key
+// logit / T + G_{a,v}, G = -ln(-ln u) with u from the counter (request, absolute position
+// a, offset lo, kNoiseTag | v/4), word v % 4 (SPOT page, Gumbel-max and coupling section).
+struct NoiseKey {
+  bool on;
+  float inv_T;  // 1 / T
+  uint32_t key0, key1, off_lo;
+};
+
+// logit / T - ln(E), E = -ln(u): -ln(u) to a few ulp relative (the winners sit at u near
+// 1, E small), its logarithm and the 1 / T scaling to about 1e-6 absolute; keys closer
+// than that are near-ties.
+__device__ __forceinline__ float noise_key(float logit, float inv_T, uint32_t word) {
+  const float E = neg_log_uniform(word_to_uniform(word));
+  return fmaf(logit, inv_T, -__logf(E));
+}
+
 __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
-    const float* __restrict__ target, const uint8_t* __restrict__ labels, int batch, int B,
-    int gamma, int V, AcceptPlan plan, AcceptWs ws) {
+    const float* __restrict__ target, const uint8_t* __restrict__ labels,
+    const int32_t* __restrict__ pos_ids, int batch, int B, int gamma, int V, AcceptPlan plan,
+    AcceptWs ws, NoiseKey nk) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long warp_global = (long)blockIdx.x * (kArgmaxThreads / 32) + (threadIdx.x >> 5);
@@ -588,7 +606,9 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
     const int c0 = chunk * plan.chunk_a;
     const int len = min(plan.chunk_a, V - c0);
     if (hit && len > 0) {
-      const float* rowp = target + ((size_t)r * B + (__ffs(hit) - 1)) * (size_t)V + c0;
+      const int slot = __ffs(hit) - 1;
+      const float* rowp = target + ((size_t)r * B + slot) * (size_t)V + c0;
+      const uint32_t apos = nk.on ? (uint32_t)pos_ids[(size_t)r * 2 * B + slot] : 0u;
       // a lane visits its entries in increasing index, so a strict '>' keeps the first
       // maximum (the first non-NaN entry starts the scan, even at -inf)
       if (vec_ok) {  // batches of 16 float4 loads per lane in flight
@@ -607,7 +627,13 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
           for (int u = 0; u < kPerA; ++u) {
             const int i4 = base + lane + 32 * u;
             if (i4 >= n4) break;
-            const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            if (nk.on) {  // one counter block per 4 entries (c0 is a multiple of 4)
+              Philox4 c4 = {(uint32_t)r, apos, nk.off_lo, kNoiseTag | (uint32_t)((c0 >> 2) + i4)};
+              const Philox4 rnd = philox4x32_10(c4, nk.key0, nk.key1);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) xv[j] = noise_key(xv[j], nk.inv_T, philox_word(rnd, j));
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               if (xv[j] > m || (mi == kNoIndex && xv[j] == xv[j])) {
@@ -618,7 +644,12 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
         }
       } else {
         for (int v = lane; v < len; v += 32) {
-          const float x = rowp[v];
+          float x = rowp[v];
+          if (nk.on) {
+            const int gv = c0 + v;
+            Philox4 c4 = {(uint32_t)r, apos, nk.off_lo, kNoiseTag | (uint32_t)(gv >> 2)};
+            x = noise_key(x, nk.inv_T, philox_word(philox4x32_10(c4, nk.key0, nk.key1), gv & 3));
+          }
           if (x > m || (mi == kNoIndex && x == x)) {
             m = x;
             mi = c0 + v;
@@ -740,6 +771,40 @@ int resident_finish_ctas() {
   return resident_blocks(accept_finish_kernel, kFinishThreads, cache);
 }
 
+// Argmax pass (greedy keys, or coupled-noise keys with nk.on) over the verified target
+// rows, then the one-warp-per-request finish kernel as its programmatic dependent.
+simsd_status launch_argmax_verify(const float* target_logits, const int32_t* draft_tokens,
+                                  const uint8_t* labels, const int32_t* pos_ids, int batch, int B,
+                                  int gamma, int V, const AcceptPlan& plan, const AcceptWs& ws,
+                                  const NoiseKey& nk, int32_t* accepted_len, int32_t* out_tokens,
+                                  int32_t* out_pos, int32_t* n_commit, uint32_t* dev_err,
+                                  cudaStream_t s) {
+  const long warps_g = (long)batch * gamma * plan.nchunk_a;
+  const long max_g = std::max(1, resident_stat_warps() / (kStatThreads / 32));
+  const long grid_g = std::max<long>(1, std::min<long>((warps_g + kArgmaxThreads / 32 - 1) / (kArgmaxThreads / 32), max_g));
+  accept_argmax_kernel<<<(unsigned)grid_g, kArgmaxThreads, 0, s>>>(target_logits, labels, pos_ids, batch, B,
+                                                                   gamma, V, plan, ws, nk);
+  simsd_status st = last_launch_status();
+  if (st != SIMSD_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)((batch + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_greedy_finish_kernel, draft_tokens, labels, batch, B,
+                                           gamma, V, plan, ws, accepted_len, out_tokens, out_pos, n_commit,
+                                           dev_err);
+  if (e != cudaSuccess) {
+    record_cuda_error("cudaLaunchKernelEx(accept_greedy_finish_kernel)", e);
+    return SIMSD_ERR_CUDA;
+  }
+  return last_launch_status();
+}
+
 }  // namespace
 
 }  // namespace simsd
@@ -780,30 +845,9 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   if (greedy) {  // argmax pass over the verified target rows, then one warp per request
-    const long warps_g = (long)batch * gamma * plan.nchunk_a;
-    const long max_g = std::max(1, resident_stat_warps() / (kStatThreads / 32));
-    const long grid_g = std::max<long>(1, std::min<long>((warps_g + kArgmaxThreads / 32 - 1) / (kArgmaxThreads / 32), max_g));
-    accept_argmax_kernel<<<(unsigned)grid_g, kArgmaxThreads, 0, s>>>(target_logits, labels, batch, B, gamma,
-                                                                     V, plan, ws);
-    simsd_status st = last_launch_status();
-    if (st != SIMSD_OK) return st;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)((batch + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.stream = s;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_greedy_finish_kernel, draft_tokens, labels, batch,
-                                             B, gamma, V, plan, ws, accepted_len, out_tokens, out_pos,
-                                             n_commit, dev_err);
-    if (e != cudaSuccess) {
-      record_cuda_error("cudaLaunchKernelEx(accept_greedy_finish_kernel)", e);
-      return SIMSD_ERR_CUDA;
-    }
-    return last_launch_status();
+    const NoiseKey nk = {false, 0.f, 0u, 0u, 0u};
+    return launch_argmax_verify(target_logits, draft_tokens, labels, nullptr, batch, B, gamma, V,
+                                plan, ws, nk, accepted_len, out_tokens, out_pos, n_commit, dev_err, s);
   }
   // persistent grid: as many stats CTAs as can be resident at once (fewer if the items are
   // fewer than the resident warps)
@@ -835,6 +879,37 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
     return SIMSD_ERR_CUDA;
   }
   return last_launch_status();
+}
+
+SIMSD_API simsd_status simsd_accept_coupled(const float* target_logits, const int32_t* draft_tokens,
+                                            const uint8_t* labels, const int32_t* pos_ids, int batch,
+                                            int B, int gamma, int V, float temperature, uint64_t seed,
+                                            uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
+                                            int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                            size_t workspace_bytes, uint32_t* dev_err,
+                                            simsd_stream_t stream) {
+  using namespace simsd;
+  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
+    return SIMSD_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
+  if (batch == 0) return SIMSD_OK;
+  if (!target_logits || !draft_tokens || !labels || !pos_ids || !accepted_len || !out_tokens ||
+      !out_pos || !n_commit || !dev_err)
+    return SIMSD_ERR_INVALID_ARG;
+  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+  const AcceptPlan plan = make_plan(batch, gamma, V, 1);
+  if (!workspace || workspace_bytes < plan.bytes || (((uintptr_t)workspace) & 255))
+    return SIMSD_ERR_WORKSPACE;
+  if ((long)batch * gamma * plan.nchunk_a > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
+  char* base = (char*)workspace;
+  AcceptWs ws;
+  ws.stats = (float2*)(base + plan.off_stats);
+  ws.winners = (unsigned long long*)(base + plan.off_winners);
+  ws.ticket = (unsigned*)(base + plan.off_ticket);
+  const NoiseKey nk = {temperature > 0.f, temperature > 0.f ? 1.f / temperature : 0.f,
+                       (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), (uint32_t)(offset & 0xffffffffu)};
+  return launch_argmax_verify(target_logits, draft_tokens, labels, pos_ids, batch, B, gamma, V, plan, ws, nk,
+                              accepted_len, out_tokens, out_pos, n_commit, dev_err, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------------------------

@@ -77,5 +77,6 @@ __device__ __forceinline__ uint32_t philox_word(const Philox4& r, int i) {
 }
 
 constexpr uint32_t kResampleTag = 0x80000000u;
+constexpr uint32_t kNoiseTag = 0x40000000u;  // coupled-noise table: (request, position, offset lo, tag | v/4)
 
 }  // namespace simsd

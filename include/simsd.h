@@ -36,6 +36,10 @@
  *   [SimSD-P] gist.science SimSD summary, sections 1-4 (same method; tau is a permutation).
  *   [S2D2-5]  S2D2 page, "方法步骤详情" step (5): residual distribution (P_ver - P)^+.
  *   [SPOT-G]  SPOT page, "Gumbel-Max 技巧与随机耦合": argmax(log p + G) samples p.
+ *   [SPOT-C]  SPOT page, core-innovation and Algorithm 2 paragraphs: coupled-noise
+ *             verification, a Gumbel table G_{a,v} indexed by absolute output position
+ *             shared by drafter and target; the target's transition Phi_G is then
+ *             deterministic and an edge is accepted iff the states are equal.
  */
 #ifndef SIMSD_H
 #define SIMSD_H
@@ -207,6 +211,29 @@ simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
                           uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
                           int32_t* out_pos, int32_t* n_commit, void* workspace,
                           size_t workspace_bytes, uint32_t* dev_err, simsd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * simsd_accept_coupled  [SPOT-C], [SPOT-G]; steps and later rounds as simsd_accept.
+ *
+ * Coupled-noise verification: for t = 1..gamma_r, with a_t = pos_ids[r][o_t] (the absolute
+ * output position of slot o_t, from simsd_build_layout), the target's own transition is
+ *   y_t = argmax_v (target_logits[r][o_t][v] / T + G_{a_t, v}),  G = -ln(-ln u)
+ * (ties -> smallest v), a sample of softmax(logits / T) by the Gumbel-max identity. Step t
+ * is accepted iff x_t = y_t; at the first mismatch y_t is committed (same outputs as
+ * simsd_accept). A drafter that proposes argmax_v (draft_logits / T + G) with the same table
+ * is accepted with probability >= (1 - TV) / (1 + TV). T = 0 is the greedy verification of
+ * simsd_accept. No draft logits are read.
+ * Noise uniforms: Philox4x32-10, key = (seed lo, seed hi), counter (r, a, offset lo,
+ * 0x40000000 | v / 4), word v % 4, u = (2 * (word >> 9) + 1) * 2^-24.
+ *   pos_ids  int32 [batch, 2B] from simsd_build_layout; other arguments as simsd_accept.
+ * Workspace: simsd_accept_workspace(batch, B, gamma, V) bytes, 256-byte aligned.
+ * --------------------------------------------------------------------------------- */
+simsd_status simsd_accept_coupled(const float* target_logits, const int32_t* draft_tokens,
+                                  const uint8_t* labels, const int32_t* pos_ids, int batch, int B,
+                                  int gamma, int V, float temperature, uint64_t seed,
+                                  uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
+                                  int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                  size_t workspace_bytes, uint32_t* dev_err, simsd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * simsd_accept_noalloc -- the same operation as simsd_accept, for callers that cannot

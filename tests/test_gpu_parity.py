@@ -416,6 +416,60 @@ def test_accept_greedy_bit_exact(name, path):
     assert set(res["accepted_len"].tolist()) == set(range(min(b, w.gamma + 1)))
 
 
+def _coupled_outputs(tl, toks, labels, pos, gamma, T, seed):
+    pkg = _pkg()
+    b, B, V = tl.shape
+    out = {k: torch.full((b,), -7, dtype=torch.int32, device="cuda")
+           for k in ("accepted_len", "n_commit")}
+    out |= {k: torch.full((b, B), -7, dtype=torch.int32, device="cuda")
+            for k in ("out_tokens", "out_pos")}
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(pkg.simsd_accept_workspace(b, B, gamma, V), dtype=torch.uint8, device="cuda")
+    pkg.simsd_accept_coupled(tl, toks, labels, pos, gamma, T, seed, 0, out["accepted_len"],
+                             out["out_tokens"], out["out_pos"], out["n_commit"], ws, err)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}, int(err.item())
+
+
+@pytest.mark.parametrize("name,T,later", [("tiny_fp32", 1.0, False), ("gqa8b_bf16", 1.0, False),
+                                          ("gqa8b_bf16", 0.8, True), ("gqa8b_bf16", 0.0, False)])
+def test_accept_coupled_bit_exact(name, T, later):
+    """Coupled-noise verification against the oracle. Half of the requests propose the
+    drafter's coupled choice (draft logits, same noise), the others the target's own (all
+    accepted); bit-exact except where the oracle's two best keys are within 1e-4."""
+    w = W[name].with_(temperature=T if T > 0 else 1.0)
+    tau = _later_round_taus(np.random.default_rng(23), w.batch, w.B) if later else None
+    inputs, meta = H.make_case(w, seed=41, tau=tau)
+    st = _step(w, inputs, meta, with_lse=False)
+    b, B, V = inputs["target_logits"].shape
+    seed = meta["philox_seed"]
+    labels = H.to_np(st.labels)
+    pos = H.to_np(st.pos_ids)
+    tl_cpu = H.to_np(inputs["target_logits"])
+    dl_cpu = H.to_np(inputs["draft_logits"])
+    toks = inputs["draft_tokens"].cpu().clone()
+    for r in range(b):
+        src = tl_cpu if r % 2 else dl_cpu
+        for k in range(B):
+            if int(labels[r, k]) & 0x7F:
+                toks[r, k] = oracle.coupled_choice(src[r, k], T, seed, 0, r, int(pos[r, k]))[0]
+    toks = toks.cuda()
+    res = oracle.accept_coupled(tl_cpu, toks.cpu().numpy(), labels, pos, w.gamma, T, seed, 0)
+    got, err = _coupled_outputs(inputs["target_logits"], toks, st.labels, st.pos_ids, w.gamma, T, seed)
+    assert err == 0
+    ties = 0
+    for r in range(b):
+        same = all(np.array_equal(got[k][r], res[k][r])
+                   for k in ("accepted_len", "n_commit", "out_tokens", "out_pos"))
+        if not same:
+            assert min(res["diag"][r]["key_gaps"]) < 1e-4, (r, got["accepted_len"][r], res["accepted_len"][r])
+            ties += 1
+    assert ties <= max(1, b // 16)
+    for r in range(1, b, 2):   # the target as its own drafter: everything open is accepted
+        R = int(sum(1 for k in range(B) if int(labels[r, k]) & 0x7F))
+        assert res["accepted_len"][r] == min(w.gamma, R)
+
+
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 1.0), ("gqa8b_bf16", 1.0),
                                     ("gqa8b_bf16", 0.7)])
 def test_accept_fixed_scratch_entry_bit_exact(name, T):

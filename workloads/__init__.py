@@ -166,17 +166,18 @@ def make_accept_inputs(w: Workload, seed: Optional[int] = None, device="cpu",
             "philox_seed": 0x5EED0000 + int(seed), "philox_offset": 0}
 
 
-def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor) -> dict:
+def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor, target_only: bool = False) -> dict:
     """Minimum HBM bytes of one verification step: each input read once, each
     output written once (per request: the prompt K/V, the 2B-row Q/K/V/O, and the
     target+draft logit rows of the gamma verified slots; the target rows only at
-    temperature 0, where greedy verification reads no draft logits)."""
+    temperature 0, where greedy verification reads no draft logits, or with `target_only`
+    for coupled-noise verification)."""
     esz = 4 if w.dtype == "fp32" else 2
     P_sum = int(prompt_len.to(torch.int64).sum())
     b, B, D = w.batch, w.B, w.D
     kv_prompt = 2 * P_sum * w.Hkv * D * esz
     resp = b * 2 * B * D * esz * (2 * w.Hq + 2 * w.Hkv)   # q + out, k + v
-    accept = b * w.gamma * (1 if w.temperature == 0 else 2) * w.V * 4
+    accept = b * w.gamma * (1 if (w.temperature == 0 or target_only) else 2) * w.V * 4
     flops = 0
     for P in prompt_len.tolist():
         flops += 4 * 2 * B * w.Hq * (P + B) * D
