@@ -53,28 +53,41 @@ def _args():
                     help="override the workload's sampling temperature (0: greedy verification)")
     ap.add_argument("--coupled", action="store_true",
                     help="coupled-noise verification (simsd_accept_coupled) instead of rejection sampling")
+    ap.add_argument("--logit-dtype", choices=["fp32", "bf16"], default=None,
+                    help="element type of the target / draft logits (default: the workload's, fp32)")
     return ap.parse_args()
+
+
+def _overrides(args):
+    """Workload fields and the verification mode the command line changes."""
+    ov = {"coupled": bool(getattr(args, "coupled", False))}
+    if args.temperature is not None:
+        ov["temperature"] = args.temperature
+    if getattr(args, "logit_dtype", None) is not None:
+        ov["logit_dtype"] = args.logit_dtype
+    return ov
+
+
+def _apply(w, ov):
+    return w.with_(**{k: v for k, v in ov.items() if k != "coupled"})
 
 
 def _workload(args):
     import workloads
-    w = workloads.WORKLOADS[args.workload]
-    return w if args.temperature is None else w.with_(temperature=args.temperature)
+    return _apply(workloads.WORKLOADS[args.workload], _overrides(args))
 
 
 # ------------------------------------------------------------------------ CPU side
 def _oracle_sample(job):
     """Runs the oracle on `n` freshly generated single-request copies of the workload
     (same shapes and distributions) and returns (tokens, seconds)."""
-    name, first_seed, n, deadline, temperature = job
+    name, first_seed, n, deadline, ov = job
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     import torch
     torch.set_num_threads(1)
     import oracle
     import workloads
-    w = workloads.WORKLOADS[name]
-    if temperature is not None:
-        w = w.with_(temperature=temperature)
+    w = _apply(workloads.WORKLOADS[name], ov)
     tokens, spent = 0, 0.0
     for i in range(n):
         if time.time() > deadline and i > 0:
@@ -95,9 +108,13 @@ def _oracle_sample(job):
                                 f(att["k_cache"]), f(att["v_cache"]),
                                 att["cache_offsets"].numpy(), lay["prompt_len"].numpy(), pos,
                                 labels, one.rope_theta)
-        oracle.accept(acc["target_logits"].numpy(), acc["draft_logits"].numpy(),
-                      acc["draft_tokens"].numpy(), labels, one.gamma, one.temperature,
-                      acc["philox_seed"], 0)
+        if ov.get("coupled"):
+            oracle.accept_coupled(f(acc["target_logits"]), acc["draft_tokens"].numpy(), labels,
+                                  pos, one.gamma, one.temperature, acc["philox_seed"], 0)
+        else:
+            oracle.accept(f(acc["target_logits"]), f(acc["draft_logits"]),
+                          acc["draft_tokens"].numpy(), labels, one.gamma, one.temperature,
+                          acc["philox_seed"], 0)
         spent += time.perf_counter() - t0
         tokens += one.gamma
     return tokens, spent
@@ -109,7 +126,7 @@ def _oracle_pool(cores):
     return mp.get_context("spawn").Pool(cores)
 
 
-def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000, temperature=None):
+def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000, ov=None):
     """tokens/s of the oracle over all host cores (one single-threaded worker per core,
     each timing only its own oracle calls; input generation is not timed)."""
     cores = cores or len(os.sched_getaffinity(0))
@@ -118,7 +135,7 @@ def cpu_oracle_throughput(name, seconds, cores=None, pool=None, first_seed=1000,
         pool = _oracle_pool(cores)
     try:
         deadline = time.time() + seconds
-        jobs = [(name, first_seed + 10000 * c, 10 ** 6, deadline, temperature) for c in range(cores)]
+        jobs = [(name, first_seed + 10000 * c, 10 ** 6, deadline, ov or {}) for c in range(cores)]
         t0 = time.perf_counter()
         res = pool.map(_oracle_sample, jobs)
         wall = time.perf_counter() - t0
@@ -153,7 +170,7 @@ def run_reference(args):
     with _oracle_pool(cores) as pool:
         for k in range(args.warmup + args.steps):
             v = cpu_oracle_throughput(args.workload, per_step, cores, pool, 1000 + 97 * k,
-                                      args.temperature)
+                                      _overrides(args))
             if k >= args.warmup:
                 vals.append(v)
     elapsed = time.perf_counter() - t0
@@ -178,7 +195,8 @@ def run_reference(args):
 def _config(w, args, launch):
     cfg = {"workload": w.name, "batch": w.batch, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
            "D": w.D, "gamma": w.gamma, "V": w.V, "rope_theta": w.rope_theta,
-           "temperature": w.temperature, "cache_layout": args.cache_layout,
+           "temperature": w.temperature, "logit_dtype": w.logit_dtype,
+           "cache_layout": args.cache_layout,
            "parallelism": f"dp{args.gpus} (independent requests per rank)"}
     if w.prompt_len is not None:
         cfg["P"] = w.prompt_len
@@ -542,7 +560,7 @@ def run_ours(args):
     # ---- CPU baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds, temperature=args.temperature)
+        cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds, ov=_overrides(args))
 
     # layout; attention (the tensor-core kernel and its split merge, or the fp32 / D 64
     # kernel alone); accept_stats and accept_finish

@@ -12,13 +12,13 @@ import torch
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
                        DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, LIB_PATH, AttnParams,
                        SimsdError, load_library, make_attn_params, simsd_accept, simsd_accept_coupled,
-                       simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
+                       simsd_accept_coupled_ex, simsd_accept_ex, simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
                        simsd_accept_workspace, simsd_build_layout, simsd_last_cuda_error, simsd_status_str,
                        simsd_verify_attention, simsd_verify_attention_workspace,
                        simsd_version)
 
 __all__ = ["VerifyStep", "simsd_build_layout", "simsd_verify_attention", "simsd_accept",
-           "simsd_accept_coupled",
+           "simsd_accept_coupled", "simsd_accept_ex", "simsd_accept_coupled_ex",
            "simsd_verify_attention_workspace", "simsd_accept_workspace", "make_attn_params",
            "load_library", "SimsdError"]
 
@@ -27,7 +27,8 @@ class VerifyStep:
     """One verification step (layout -> verify attention -> accept) over fixed inputs.
 
     ``inputs`` holds device tensors: tau, prompt_len, q, k_resp, v_resp, k_cache, v_cache,
-    cache_start (int64 [b]), target_logits, draft_logits, draft_tokens. Outputs live in
+    cache_start (int64 [b]), target_logits, draft_logits (both fp32 or both bf16),
+    draft_tokens. Outputs live in
     this object (``pos_ids``, ``labels``, ``out``, ``lse``, ``accepted_len``, ``n_commit``,
     ``out_tokens``, ``out_pos``, ``dev_err``) and are overwritten by every ``run``.
     """
@@ -78,15 +79,15 @@ class VerifyStep:
     def accept(self, stream=None):
         i = self.inputs
         if self.coupled:
-            simsd_accept_coupled(i["target_logits"], i["draft_tokens"], self.labels, self.pos_ids,
-                                 self.gamma, self.temperature, self.seed, self.offset,
-                                 self.accepted_len, self.out_tokens, self.out_pos, self.n_commit,
-                                 self.ws_accept, self.dev_err, stream)
+            simsd_accept_coupled_ex(i["target_logits"], i["draft_tokens"], self.labels, self.pos_ids,
+                                    self.gamma, self.temperature, self.seed, self.offset,
+                                    self.accepted_len, self.out_tokens, self.out_pos,
+                                    self.n_commit, self.ws_accept, self.dev_err, stream)
             return
-        simsd_accept(i["target_logits"], i["draft_logits"], i["draft_tokens"], self.labels,
-                     self.gamma, self.temperature, self.seed, self.offset, self.accepted_len,
-                     self.out_tokens, self.out_pos, self.n_commit, self.ws_accept,
-                     self.dev_err, stream)
+        simsd_accept_ex(i["target_logits"], i["draft_logits"], i["draft_tokens"], self.labels,
+                        self.gamma, self.temperature, self.seed, self.offset,
+                        self.accepted_len, self.out_tokens, self.out_pos, self.n_commit,
+                        self.ws_accept, self.dev_err, stream)
 
     def run(self, stream=None):
         self.layout(stream)

@@ -25,6 +25,7 @@ CACHE_NHD, CACHE_HND = 0, 1
 EXPORTED = ["simsd_status_str", "simsd_version", "simsd_last_cuda_error", "simsd_build_layout",
             "simsd_verify_attention_workspace", "simsd_verify_attention",
             "simsd_accept_workspace", "simsd_accept", "simsd_accept_coupled",
+            "simsd_accept_ex", "simsd_accept_coupled_ex",
             "simsd_accept_noalloc", "simsd_accept_noalloc_max_scratch"]
 
 
@@ -83,6 +84,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.simsd_accept_coupled.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                          vp, vp, vp, vp, vp, sz, vp, vp]
     lib.simsd_accept_coupled.restype = i32
+    lib.simsd_accept_ex.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, f32, u64, u64,
+                                    vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.simsd_accept_ex.restype = i32
+    lib.simsd_accept_coupled_ex.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64,
+                                            u64, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.simsd_accept_coupled_ex.restype = i32
     lib.simsd_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                          vp, vp, vp, vp, vp, vp]
     lib.simsd_accept_noalloc.restype = i32
@@ -233,6 +240,60 @@ def simsd_accept_coupled(target_logits, draft_tokens, labels, pos_ids, gamma, te
         _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream(stream))
     _raise(st, "simsd_accept_coupled")
+
+
+_LOGIT_DTYPES = {torch.float32: DTYPE_FP32, torch.bfloat16: DTYPE_BF16}
+
+
+def _logit_dtype(t, name):
+    if t.dtype not in _LOGIT_DTYPES:
+        raise ValueError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+    return _LOGIT_DTYPES[t.dtype]
+
+
+def simsd_accept_ex(target_logits, draft_logits, draft_tokens, labels, gamma, temperature,
+                    seed, offset, accepted_len, out_tokens, out_pos, n_commit, workspace,
+                    dev_err, stream=None):
+    """simsd_accept for fp32 or bf16 logits (both arrays of one type, passed to the library
+    as its logit_dtype argument)."""
+    dt = _logit_dtype(target_logits, "target_logits")
+    _check(target_logits, "target_logits")
+    _check(draft_logits, "draft_logits", target_logits.dtype)
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(labels, "labels", torch.uint8)
+    for t, n in ((accepted_len, "accepted_len"), (out_tokens, "out_tokens"),
+                 (out_pos, "out_pos"), (n_commit, "n_commit"), (dev_err, "dev_err")):
+        _check(t, n, torch.int32)
+    _check(workspace, "workspace", torch.uint8)
+    b, B, V = target_logits.shape
+    st = load_library().simsd_accept_ex(
+        _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(labels), b, B,
+        int(gamma), V, float(temperature), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+        _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(stream))
+    _raise(st, "simsd_accept_ex")
+
+
+def simsd_accept_coupled_ex(target_logits, draft_tokens, labels, pos_ids, gamma, temperature,
+                            seed, offset, accepted_len, out_tokens, out_pos, n_commit,
+                            workspace, dev_err, stream=None):
+    """simsd_accept_coupled for fp32 or bf16 target logits."""
+    dt = _logit_dtype(target_logits, "target_logits")
+    _check(target_logits, "target_logits")
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(labels, "labels", torch.uint8)
+    _check(pos_ids, "pos_ids", torch.int32)
+    for t, n in ((accepted_len, "accepted_len"), (out_tokens, "out_tokens"),
+                 (out_pos, "out_pos"), (n_commit, "n_commit"), (dev_err, "dev_err")):
+        _check(t, n, torch.int32)
+    _check(workspace, "workspace", torch.uint8)
+    b, B, V = target_logits.shape
+    st = load_library().simsd_accept_coupled_ex(
+        _ptr(target_logits), dt, _ptr(draft_tokens), _ptr(labels), _ptr(pos_ids), b, B,
+        int(gamma), V, float(temperature), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+        _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(stream))
+    _raise(st, "simsd_accept_coupled_ex")
 
 
 def simsd_accept_noalloc_max_scratch() -> int:

@@ -38,7 +38,7 @@ struct AcceptWs {
 };
 
 struct AcceptPlan {
-  int nchunk_a, chunk_a;  // K3a: chunks per row, elements per chunk (multiple of 4)
+  int nchunk_a, chunk_a;  // K3a: chunks per row, elements per chunk (multiple of 8)
   int nchunk_b, chunk_b;  // K3b: chunks per request, elements per chunk (multiple of 4)
   size_t off_stats, off_winners, off_ticket, bytes;
 };
@@ -71,7 +71,7 @@ AcceptPlan make_plan(int batch, int gamma, int V, int models = 2) {
     }
     if (fill >= 0.97) break;
   }
-  p.chunk_a = (int)(((V + best_nc - 1) / best_nc + 3) / 4 * 4);
+  p.chunk_a = (int)(((V + best_nc - 1) / best_nc + 7) / 8 * 8);  // 16-byte loads of bf16
   p.nchunk_a = (V + p.chunk_a - 1) / p.chunk_a;
   long nb = batch > 0 ? std::max(1, resident_finish_ctas()) / batch : 1;
   const long max_nb = (V + 1023) / 1024;
@@ -96,6 +96,82 @@ __device__ __forceinline__ float4 ld_stream4(const float* p) {
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p));
   return v;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
+  return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
+}
+
+// Logit element types: fp32, or bf16 widened exactly to fp32 (its 16 bits are the top half
+// of the fp32 pattern). The streaming passes read kVec consecutive entries per 16-byte load
+// (4 fp32 or 8 bf16, so a lane keeps as many bytes in flight for either type) and widen
+// each with `entry`; the race reads 4 entries per load (`ldg4`, kAlign bytes).
+template <typename LT>
+struct LogitIO;
+template <>
+struct LogitIO<float> {
+  static constexpr int kVec = 4;
+  static constexpr int kAlign = 16;
+  static constexpr uint32_t kNegInfWord = 0xff800000u;  // one -inf entry
+  static __device__ __forceinline__ float entry(const uint4& w, int j) { return __uint_as_float(word_of(w, j)); }
+  // running maximum over whole loads
+  using MaxAcc = float;
+  static __device__ __forceinline__ MaxAcc max_init() { return -INFINITY; }
+  static __device__ __forceinline__ MaxAcc max_acc(MaxAcc a, const uint4& w) {
+    return fmaxf(a, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                          fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+  }
+  static __device__ __forceinline__ float max_value(MaxAcc a) { return a; }
+  static __device__ __forceinline__ float4 ldg4(const float* row, int i) {
+    return __ldg(reinterpret_cast<const float4*>(row) + i);
+  }
+  static __device__ __forceinline__ float ld1(const float* p) { return __ldg(p); }
+};
+template <>
+struct LogitIO<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  static constexpr int kAlign = 8;
+  static constexpr uint32_t kNegInfWord = 0xff80ff80u;  // two -inf entries
+  static __device__ __forceinline__ float lo(uint32_t x) { return __uint_as_float(x << 16); }
+  static __device__ __forceinline__ float hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+  static __device__ __forceinline__ float entry(const uint4& w, int j) {
+    const uint32_t x = word_of(w, j >> 1);
+    return (j & 1) ? hi(x) : lo(x);
+  }
+  // running maximum on the packed pairs (widening is exact and monotone, so the maximum of
+  // the bf16 values widens to the maximum of the widened values; a NaN operand is skipped)
+  using MaxAcc = uint32_t;
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ MaxAcc max_init() { return kNegInfWord; }
+  static __device__ __forceinline__ MaxAcc max_acc(MaxAcc a, const uint4& w) {
+    return max2(a, max2(max2(w.x, w.y), max2(w.z, w.w)));
+  }
+  static __device__ __forceinline__ float max_value(MaxAcc a) { return fmaxf(lo(a), hi(a)); }
+  static __device__ __forceinline__ float4 ldg4(const __nv_bfloat16* row, int i) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(row) + i);
+    return make_float4(lo(w.x), hi(w.x), lo(w.y), hi(w.y));
+  }
+  static __device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p)) << 16);
+  }
+};
+
+// Rows can be streamed with 16-byte loads: V a multiple of kVec and both bases aligned.
+template <typename LT>
+__device__ __forceinline__ bool stream_ok(int V, const LT* a, const LT* b) {
+  return V % LogitIO<LT>::kVec == 0 && ((((uintptr_t)a) | ((uintptr_t)b)) & 15) == 0;
 }
 
 __device__ __forceinline__ float scale_logit(float x, float T, bool unit_T) {
@@ -132,8 +208,11 @@ __device__ __forceinline__ float exp_shifted(float x, float m) {
   return y;
 }
 
-__global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft,
+template <typename LT>
+// Two CTAs per SM: each lane holds 16 16-byte loads in flight (64 registers), and a third
+// CTA would force spills.
+__global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
+    const LT* __restrict__ target, const LT* __restrict__ draft,
     const uint8_t* __restrict__ labels, int batch, int B, int gamma, int V, float T,
     AcceptPlan plan, AcceptWs ws) {
   // K3b may be scheduled as SMs free up; it waits for this grid before it reads anything
@@ -151,7 +230,10 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     }
   }
   const bool unit_T = (T == 1.f);
-  const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+  const bool vec_ok = stream_ok(V, target, draft);
+  constexpr int E = LogitIO<LT>::kVec;
+  const uint4 neg_inf = make_uint4(LogitIO<LT>::kNegInfWord, LogitIO<LT>::kNegInfWord,
+                                   LogitIO<LT>::kNegInfWord, LogitIO<LT>::kNegInfWord);
   for (long item = warp_global; item < items; item += nwarps) {
     const int chunk = (int)(item % nchunk);
     const long row = item / nchunk;
@@ -165,29 +247,22 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     const int len = min(plan.chunk_a, V - c0);
     if (hit && len > 0) {
       const int k = __ffs(hit) - 1;
-      const float* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
-      if (vec_ok) {
-        const float4* src = reinterpret_cast<const float4*>(rowp + c0);
-        const int n4 = len >> 2;
-        for (int base = 0; base < n4; base += 32 * kPer) {
-          float4 x[kPer];
+      const LT* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
+      if (vec_ok) {  // batches of kPer 16-byte loads per lane in flight (c0 is a multiple of 8)
+        const LT* src = rowp + c0;
+        const int nv = len / E;
+        for (int base = 0; base < nv; base += 32 * kPer) {
+          uint4 x[kPer];
 #pragma unroll
           for (int u = 0; u < kPer; ++u) {
-            const int i4 = base + lane + 32 * u;
-            x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const int i = base + lane + 32 * u;
+            x[u] = i < nv ? ld_stream16(src + (size_t)E * i) : neg_inf;
           }
-          float mb = -INFINITY;
+          // x / T rounded is monotone in x (T > 0), so the batch maximum is scaled once
+          typename LogitIO<LT>::MaxAcc acc = LogitIO<LT>::max_init();
 #pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            if (!unit_T) {
-              x[u].x = scale_logit(x[u].x, T, false);
-              x[u].y = scale_logit(x[u].y, T, false);
-              x[u].z = scale_logit(x[u].z, T, false);
-              x[u].w = scale_logit(x[u].w, T, false);
-            }
-            mb = fmaxf(mb, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
-          }
+          for (int u = 0; u < kPer; ++u) acc = LogitIO<LT>::max_acc(acc, x[u]);
+          const float mb = scale_logit(LogitIO<LT>::max_value(acc), T, unit_T);
           if (mb > m) {  // rescale what was summed so far to the new maximum
             sum = (m == -INFINITY) ? 0.f : sum * exp_shifted(m, mb);
             m = mb;
@@ -195,16 +270,18 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
           if (m != -INFINITY) {
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              s0 += exp_shifted(x[u].x, m) + exp_shifted(x[u].y, m);
-              s1 += exp_shifted(x[u].z, m) + exp_shifted(x[u].w, m);
-            }
+            for (int u = 0; u < kPer; ++u)
+#pragma unroll
+              for (int j = 0; j < E; j += 2) {
+                s0 += exp_shifted(scale_logit(LogitIO<LT>::entry(x[u], j), T, unit_T), m);
+                s1 += exp_shifted(scale_logit(LogitIO<LT>::entry(x[u], j + 1), T, unit_T), m);
+              }
             sum += s0 + s1;
           }
         }
       } else {
         for (int v = lane; v < len; v += 32) {
-          const float z = scale_logit(rowp[c0 + v], T, unit_T);
+          const float z = scale_logit(LogitIO<LT>::ld1(rowp + c0 + v), T, unit_T);
           if (z > m) {
             sum = (m == -INFINITY) ? 0.f : sum * exp_shifted(m, z);
             m = z;
@@ -294,7 +371,8 @@ __device__ __forceinline__ void race_group(int g, int end, const float (&t)[4], 
 // Race over entries [c0, c1) (c0 a multiple of 4) of one target row (and draft row unless
 // `on_p`), by `nthreads` threads with thread index `t`: four counter groups' loads in
 // flight per thread at a time.
-__device__ __forceinline__ void race_range(const float* __restrict__ trow, const float* __restrict__ drow,
+template <typename LT>
+__device__ __forceinline__ void race_range(const LT* __restrict__ trow, const LT* __restrict__ drow,
                                            int c0, int c1, int t, int nthreads, bool vec_ok,
                                            float T, bool unit_T, float mt, float inv_st, float md,
                                            float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
@@ -308,18 +386,18 @@ __device__ __forceinline__ void race_range(const float* __restrict__ trow, const
       const int g = gb + u * nthreads;
       if (g < g1) {
         if (vec_ok) {
-          const float4 t4 = __ldg(reinterpret_cast<const float4*>(trow) + g);
+          const float4 t4 = LogitIO<LT>::ldg4(trow, g);
           tv[u][0] = t4.x; tv[u][1] = t4.y; tv[u][2] = t4.z; tv[u][3] = t4.w;
           if (!on_p) {
-            const float4 d4 = __ldg(reinterpret_cast<const float4*>(drow) + g);
+            const float4 d4 = LogitIO<LT>::ldg4(drow, g);
             dv[u][0] = d4.x; dv[u][1] = d4.y; dv[u][2] = d4.z; dv[u][3] = d4.w;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int v = 4 * g + j;
-            tv[u][j] = v < c1 ? __ldg(trow + v) : 0.f;
-            dv[u][j] = (v < c1 && !on_p) ? __ldg(drow + v) : 0.f;
+            tv[u][j] = v < c1 ? LogitIO<LT>::ld1(trow + v) : 0.f;
+            dv[u][j] = (v < c1 && !on_p) ? LogitIO<LT>::ld1(drow + v) : 0.f;
           }
         }
       }
@@ -334,8 +412,9 @@ __device__ __forceinline__ void race_range(const float* __restrict__ trow, const
   }
 }
 
+template <typename LT>
 __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft,
+    const LT* __restrict__ target, const LT* __restrict__ draft,
     const int32_t* __restrict__ tokens, const uint8_t* __restrict__ labels, int batch, int B,
     int gamma, int V, float T, uint32_t key0, uint32_t key1, uint32_t off_lo, uint32_t off_hi,
     AcceptPlan plan, AcceptWs ws, int32_t* __restrict__ accepted_len,
@@ -381,8 +460,8 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
     if (!bad_w && lane < gr_w) {
       const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
-      tx = scale_logit(target[rowoff], T, unit_T);
-      dx = scale_logit(draft[rowoff], T, unit_T);
+      tx = scale_logit(LogitIO<LT>::ld1(target + rowoff), T, unit_T);
+      dx = scale_logit(LogitIO<LT>::ld1(draft + rowoff), T, unit_T);
       Philox4 c4 = {(uint32_t)r, off_lo, off_hi, (uint32_t)(lane >> 2)};
       const Philox4 rnd = philox4x32_10(c4, key0, key1);
       u = word_to_uniform(philox_word(rnd, lane & 3));
@@ -482,12 +561,12 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     // exponential race over this CTA's chunk of the rejected slot's vocabulary
     const int k = s_order[a];
     const float mt = s_mt, st = s_st, md = s_md, sd = s_sd;
-    const float* trow = target + ((size_t)r * B + k) * (size_t)V;
-    const float* drow = draft + ((size_t)r * B + k) * (size_t)V;
+    const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
+    const LT* drow = draft + ((size_t)r * B + k) * (size_t)V;
     const int c0 = chunk * plan.chunk_b;
     const int c1 = min(V, c0 + plan.chunk_b);
     unsigned long long best_res = 0ull;
-    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
     race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
                1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
 #pragma unroll
@@ -517,9 +596,9 @@ __global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
     // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
     // over the whole row, done here by the last CTA (never on typical inputs)
     const int k = s_order[a];
-    const float* trow = target + ((size_t)r * B + k) * (size_t)V;
+    const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
     unsigned long long best = 0ull;
-    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & 15) == 0;
+    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
     race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
                1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
 #pragma unroll
@@ -583,8 +662,9 @@ __device__ __forceinline__ float noise_key(float logit, float inv_T, uint32_t wo
   return fmaf(logit, inv_T, -__logf(E));
 }
 
+template <typename LT>
 __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
-    const float* __restrict__ target, const uint8_t* __restrict__ labels,
+    const LT* __restrict__ target, const uint8_t* __restrict__ labels,
     const int32_t* __restrict__ pos_ids, int batch, int B, int gamma, int V, AcceptPlan plan,
     AcceptWs ws, NoiseKey nk) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -593,7 +673,10 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
   const long nwarps = (long)gridDim.x * (kArgmaxThreads / 32);
   const int nchunk = plan.nchunk_a;
   const long items = (long)batch * gamma * nchunk;
-  const bool vec_ok = (V & 3) == 0 && (((uintptr_t)target) & 15) == 0;
+  const bool vec_ok = stream_ok(V, target, target);
+  constexpr int E = LogitIO<LT>::kVec;
+  const uint4 neg_inf = make_uint4(LogitIO<LT>::kNegInfWord, LogitIO<LT>::kNegInfWord,
+                                   LogitIO<LT>::kNegInfWord, LogitIO<LT>::kNegInfWord);
   for (long item = warp_global; item < items; item += nwarps) {
     const int chunk = (int)(item % nchunk);
     const long row = item / nchunk;
@@ -607,44 +690,72 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
     const int len = min(plan.chunk_a, V - c0);
     if (hit && len > 0) {
       const int slot = __ffs(hit) - 1;
-      const float* rowp = target + ((size_t)r * B + slot) * (size_t)V + c0;
+      const LT* rowp = target + ((size_t)r * B + slot) * (size_t)V + c0;
       const uint32_t apos = nk.on ? (uint32_t)pos_ids[(size_t)r * 2 * B + slot] : 0u;
       // a lane visits its entries in increasing index, so a strict '>' keeps the first
       // maximum (the first non-NaN entry starts the scan, even at -inf)
-      if (vec_ok) {  // batches of 16 float4 loads per lane in flight
+      if (vec_ok) {  // batches of 16 16-byte loads per lane in flight (c0 is a multiple of 8)
         constexpr int kPerA = 16;
-        const float4* src = reinterpret_cast<const float4*>(rowp);
-        const int n4 = len >> 2;
-        for (int base = 0; base < n4; base += 32 * kPerA) {
-          float4 x[kPerA];
+        const int nv = len / E;
+        for (int base = 0; base < nv; base += 32 * kPerA) {
+          uint4 x[kPerA];
 #pragma unroll
           for (int u = 0; u < kPerA; ++u) {
-            const int i4 = base + lane + 32 * u;
-            x[u] = i4 < n4 ? ld_stream4(reinterpret_cast<const float*>(src + i4))
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const int i = base + lane + 32 * u;
+            x[u] = i < nv ? ld_stream16(rowp + (size_t)E * i) : neg_inf;
+          }
+          if (!nk.on) {
+            // greedy keys: the batch maximum first (padding is -inf); the first index of it
+            // is looked up only when it raises the running maximum (or starts the scan),
+            // which keeps the first maximum as the per-entry scan does
+            typename LogitIO<LT>::MaxAcc acc = LogitIO<LT>::max_init();
+#pragma unroll
+            for (int u = 0; u < kPerA; ++u) acc = LogitIO<LT>::max_acc(acc, x[u]);
+            const float mb = LogitIO<LT>::max_value(acc);
+            if (mb > m || (mi == kNoIndex && mb == mb)) {
+              int first = kNoIndex;
+#pragma unroll
+              for (int u = kPerA - 1; u >= 0; --u) {  // backwards: the last hit is the first index
+                const int i = base + lane + 32 * u;
+#pragma unroll
+                for (int j = E - 1; j >= 0; --j)
+                  if (i < nv && LogitIO<LT>::entry(x[u], j) == mb) first = c0 + E * i + j;
+              }
+              if (first != kNoIndex) {
+                m = mb;
+                mi = first;
+              }
+            }
+            continue;
           }
 #pragma unroll
           for (int u = 0; u < kPerA; ++u) {
-            const int i4 = base + lane + 32 * u;
-            if (i4 >= n4) break;
-            float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-            if (nk.on) {  // one counter block per 4 entries (c0 is a multiple of 4)
-              Philox4 c4 = {(uint32_t)r, apos, nk.off_lo, kNoiseTag | (uint32_t)((c0 >> 2) + i4)};
-              const Philox4 rnd = philox4x32_10(c4, nk.key0, nk.key1);
+            const int i = base + lane + 32 * u;
+            if (i >= nv) break;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) xv[j] = noise_key(xv[j], nk.inv_T, philox_word(rnd, j));
-            }
+            for (int g = 0; g < E / 4; ++g) {  // groups of 4 entries: one counter block each
+              const int v0 = c0 + E * i + 4 * g;
+              float xv[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (xv[j] > m || (mi == kNoIndex && xv[j] == xv[j])) {
-                m = xv[j];
-                mi = c0 + 4 * i4 + j;
+              for (int j = 0; j < 4; ++j) xv[j] = LogitIO<LT>::entry(x[u], 4 * g + j);
+              if (nk.on) {
+                Philox4 c4 = {(uint32_t)r, apos, nk.off_lo, kNoiseTag | (uint32_t)(v0 >> 2)};
+                const Philox4 rnd = philox4x32_10(c4, nk.key0, nk.key1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xv[j] = noise_key(xv[j], nk.inv_T, philox_word(rnd, j));
               }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (xv[j] > m || (mi == kNoIndex && xv[j] == xv[j])) {
+                  m = xv[j];
+                  mi = v0 + j;
+                }
+            }
           }
         }
       } else {
         for (int v = lane; v < len; v += 32) {
-          float x = rowp[v];
+          float x = LogitIO<LT>::ld1(rowp + v);
           if (nk.on) {
             const int gv = c0 + v;
             Philox4 c4 = {(uint32_t)r, apos, nk.off_lo, kNoiseTag | (uint32_t)(gv >> 2)};
@@ -761,28 +872,40 @@ int resident_blocks(K kernel, int threads, int* cache) {
   return cache[dev];
 }
 
+// The work split (and so the workspace size) does not depend on the logit type: both
+// instantiations of a kernel are counted and the smaller residency is taken.
 int resident_stat_warps() {
-  static int cache[64];
-  return resident_blocks(accept_stats_kernel, kStatThreads, cache) * (kStatThreads / 32);
+  static int cache_f[64], cache_h[64];
+  return std::min(resident_blocks(accept_stats_kernel<float>, kStatThreads, cache_f),
+                  resident_blocks(accept_stats_kernel<__nv_bfloat16>, kStatThreads, cache_h)) *
+         (kStatThreads / 32);
+}
+
+int resident_argmax_ctas() {
+  static int cache_f[64], cache_h[64];
+  return std::min(resident_blocks(accept_argmax_kernel<float>, kArgmaxThreads, cache_f),
+                  resident_blocks(accept_argmax_kernel<__nv_bfloat16>, kArgmaxThreads, cache_h));
 }
 
 int resident_finish_ctas() {
-  static int cache[64];
-  return resident_blocks(accept_finish_kernel, kFinishThreads, cache);
+  static int cache_f[64], cache_h[64];
+  return std::min(resident_blocks(accept_finish_kernel<float>, kFinishThreads, cache_f),
+                  resident_blocks(accept_finish_kernel<__nv_bfloat16>, kFinishThreads, cache_h));
 }
 
 // Argmax pass (greedy keys, or coupled-noise keys with nk.on) over the verified target
 // rows, then the one-warp-per-request finish kernel as its programmatic dependent.
-simsd_status launch_argmax_verify(const float* target_logits, const int32_t* draft_tokens,
+template <typename LT>
+simsd_status launch_argmax_verify(const LT* target_logits, const int32_t* draft_tokens,
                                   const uint8_t* labels, const int32_t* pos_ids, int batch, int B,
                                   int gamma, int V, const AcceptPlan& plan, const AcceptWs& ws,
                                   const NoiseKey& nk, int32_t* accepted_len, int32_t* out_tokens,
                                   int32_t* out_pos, int32_t* n_commit, uint32_t* dev_err,
                                   cudaStream_t s) {
   const long warps_g = (long)batch * gamma * plan.nchunk_a;
-  const long max_g = std::max(1, resident_stat_warps() / (kStatThreads / 32));
+  const long max_g = std::max(1, resident_argmax_ctas());
   const long grid_g = std::max<long>(1, std::min<long>((warps_g + kArgmaxThreads / 32 - 1) / (kArgmaxThreads / 32), max_g));
-  accept_argmax_kernel<<<(unsigned)grid_g, kArgmaxThreads, 0, s>>>(target_logits, labels, pos_ids, batch, B,
+  accept_argmax_kernel<LT><<<(unsigned)grid_g, kArgmaxThreads, 0, s>>>(target_logits, labels, pos_ids, batch, B,
                                                                    gamma, V, plan, ws, nk);
   simsd_status st = last_launch_status();
   if (st != SIMSD_OK) return st;
@@ -815,22 +938,15 @@ SIMSD_API size_t simsd_accept_workspace(int batch, int B, int gamma, int V) {
   return std::max(simsd::make_plan(batch, gamma, V, 2).bytes, simsd::make_plan(batch, gamma, V, 1).bytes);
 }
 
-SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
-                                    const int32_t* draft_tokens, const uint8_t* labels,
-                                    int batch, int B, int gamma, int V, float temperature,
-                                    uint64_t seed, uint64_t offset, int32_t* accepted_len,
-                                    int32_t* out_tokens, int32_t* out_pos, int32_t* n_commit,
-                                    void* workspace, size_t workspace_bytes, uint32_t* dev_err,
-                                    simsd_stream_t stream) {
-  using namespace simsd;
-  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
-    return SIMSD_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
-  if (batch == 0) return SIMSD_OK;
-  if (!target_logits || !draft_logits || !draft_tokens || !labels || !accepted_len ||
-      !out_tokens || !out_pos || !n_commit || !dev_err)
-    return SIMSD_ERR_INVALID_ARG;
-  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+namespace simsd {
+namespace {
+
+template <typename LT>
+simsd_status accept_impl(const LT* target_logits, const LT* draft_logits, const int32_t* draft_tokens,
+                         const uint8_t* labels, int batch, int B, int gamma, int V, float temperature,
+                         uint64_t seed, uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
+                         int32_t* out_pos, int32_t* n_commit, void* workspace, size_t workspace_bytes,
+                         uint32_t* dev_err, cudaStream_t s) {
   const bool greedy = temperature == 0.f;
   const AcceptPlan plan = make_plan(batch, gamma, V, greedy ? 1 : 2);
   if (!workspace || workspace_bytes < plan.bytes || (((uintptr_t)workspace) & 255))
@@ -843,11 +959,10 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   const long grid_a = (long)batch * gamma * 2 * plan.nchunk_a;
   const long grid_b = (long)batch * plan.nchunk_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
-  cudaStream_t s = (cudaStream_t)stream;
   if (greedy) {  // argmax pass over the verified target rows, then one warp per request
     const NoiseKey nk = {false, 0.f, 0u, 0u, 0u};
-    return launch_argmax_verify(target_logits, draft_tokens, labels, nullptr, batch, B, gamma, V,
-                                plan, ws, nk, accepted_len, out_tokens, out_pos, n_commit, dev_err, s);
+    return launch_argmax_verify<LT>(target_logits, draft_tokens, labels, nullptr, batch, B, gamma, V,
+                                    plan, ws, nk, accepted_len, out_tokens, out_pos, n_commit, dev_err, s);
   }
   // persistent grid: as many stats CTAs as can be resident at once (fewer if the items are
   // fewer than the resident warps)
@@ -855,7 +970,7 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   const long warps_needed = (long)batch * gamma * 2 * plan.nchunk_a;
   const long grid_stats = std::max<long>(1, std::min<long>((warps_needed + kStatThreads / 32 - 1) / (kStatThreads / 32),
                                                            max_ctas));
-  accept_stats_kernel<<<(unsigned)grid_stats, kStatThreads, 0, s>>>(
+  accept_stats_kernel<LT><<<(unsigned)grid_stats, kStatThreads, 0, s>>>(
       target_logits, draft_logits, labels, batch, B, gamma, V, temperature, plan, ws);
   simsd_status st = last_launch_status();
   if (st != SIMSD_OK) return st;
@@ -870,7 +985,7 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   cfg.attrs = at;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, accept_finish_kernel, target_logits, draft_logits, draft_tokens, labels, batch, B,
+      &cfg, accept_finish_kernel<LT>, target_logits, draft_logits, draft_tokens, labels, batch, B,
       gamma, V, temperature, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32),
       (uint32_t)(offset & 0xffffffffu), (uint32_t)(offset >> 32), plan, ws, accepted_len,
       out_tokens, out_pos, n_commit, dev_err);
@@ -881,22 +996,12 @@ SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* dra
   return last_launch_status();
 }
 
-SIMSD_API simsd_status simsd_accept_coupled(const float* target_logits, const int32_t* draft_tokens,
-                                            const uint8_t* labels, const int32_t* pos_ids, int batch,
-                                            int B, int gamma, int V, float temperature, uint64_t seed,
-                                            uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
-                                            int32_t* out_pos, int32_t* n_commit, void* workspace,
-                                            size_t workspace_bytes, uint32_t* dev_err,
-                                            simsd_stream_t stream) {
-  using namespace simsd;
-  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
-    return SIMSD_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
-  if (batch == 0) return SIMSD_OK;
-  if (!target_logits || !draft_tokens || !labels || !pos_ids || !accepted_len || !out_tokens ||
-      !out_pos || !n_commit || !dev_err)
-    return SIMSD_ERR_INVALID_ARG;
-  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+template <typename LT>
+simsd_status accept_coupled_impl(const LT* target_logits, const int32_t* draft_tokens, const uint8_t* labels,
+                                 const int32_t* pos_ids, int batch, int B, int gamma, int V,
+                                 float temperature, uint64_t seed, uint64_t offset, int32_t* accepted_len,
+                                 int32_t* out_tokens, int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                 size_t workspace_bytes, uint32_t* dev_err, cudaStream_t s) {
   const AcceptPlan plan = make_plan(batch, gamma, V, 1);
   if (!workspace || workspace_bytes < plan.bytes || (((uintptr_t)workspace) & 255))
     return SIMSD_ERR_WORKSPACE;
@@ -908,8 +1013,92 @@ SIMSD_API simsd_status simsd_accept_coupled(const float* target_logits, const in
   ws.ticket = (unsigned*)(base + plan.off_ticket);
   const NoiseKey nk = {temperature > 0.f, temperature > 0.f ? 1.f / temperature : 0.f,
                        (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), (uint32_t)(offset & 0xffffffffu)};
-  return launch_argmax_verify(target_logits, draft_tokens, labels, pos_ids, batch, B, gamma, V, plan, ws, nk,
-                              accepted_len, out_tokens, out_pos, n_commit, dev_err, (cudaStream_t)stream);
+  return launch_argmax_verify<LT>(target_logits, draft_tokens, labels, pos_ids, batch, B, gamma, V, plan, ws,
+                                  nk, accepted_len, out_tokens, out_pos, n_commit, dev_err, s);
+}
+
+}  // namespace
+}  // namespace simsd
+
+SIMSD_API simsd_status simsd_accept_ex(const void* target_logits, const void* draft_logits,
+                                       simsd_dtype logit_dtype, const int32_t* draft_tokens,
+                                       const uint8_t* labels, int batch, int B, int gamma, int V,
+                                       float temperature, uint64_t seed, uint64_t offset,
+                                       int32_t* accepted_len, int32_t* out_tokens, int32_t* out_pos,
+                                       int32_t* n_commit, void* workspace, size_t workspace_bytes,
+                                       uint32_t* dev_err, simsd_stream_t stream) {
+  using namespace simsd;
+  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
+    return SIMSD_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
+  if (logit_dtype != SIMSD_DTYPE_FP32 && logit_dtype != SIMSD_DTYPE_BF16) return SIMSD_ERR_INVALID_ARG;
+  if (batch == 0) return SIMSD_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !labels || !accepted_len ||
+      !out_tokens || !out_pos || !n_commit || !dev_err)
+    return SIMSD_ERR_INVALID_ARG;
+  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (logit_dtype == SIMSD_DTYPE_BF16)
+    return accept_impl<__nv_bfloat16>((const __nv_bfloat16*)target_logits, (const __nv_bfloat16*)draft_logits,
+                                      draft_tokens, labels, batch, B, gamma, V, temperature, seed, offset,
+                                      accepted_len, out_tokens, out_pos, n_commit, workspace,
+                                      workspace_bytes, dev_err, s);
+  return accept_impl<float>((const float*)target_logits, (const float*)draft_logits, draft_tokens, labels,
+                            batch, B, gamma, V, temperature, seed, offset, accepted_len, out_tokens,
+                            out_pos, n_commit, workspace, workspace_bytes, dev_err, s);
+}
+
+SIMSD_API simsd_status simsd_accept(const float* target_logits, const float* draft_logits,
+                                    const int32_t* draft_tokens, const uint8_t* labels,
+                                    int batch, int B, int gamma, int V, float temperature,
+                                    uint64_t seed, uint64_t offset, int32_t* accepted_len,
+                                    int32_t* out_tokens, int32_t* out_pos, int32_t* n_commit,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                    simsd_stream_t stream) {
+  return simsd_accept_ex(target_logits, draft_logits, SIMSD_DTYPE_FP32, draft_tokens, labels, batch, B,
+                         gamma, V, temperature, seed, offset, accepted_len, out_tokens, out_pos,
+                         n_commit, workspace, workspace_bytes, dev_err, stream);
+}
+
+SIMSD_API simsd_status simsd_accept_coupled_ex(const void* target_logits, simsd_dtype logit_dtype,
+                                               const int32_t* draft_tokens, const uint8_t* labels,
+                                               const int32_t* pos_ids, int batch, int B, int gamma, int V,
+                                               float temperature, uint64_t seed, uint64_t offset,
+                                               int32_t* accepted_len, int32_t* out_tokens,
+                                               int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                               size_t workspace_bytes, uint32_t* dev_err,
+                                               simsd_stream_t stream) {
+  using namespace simsd;
+  if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
+    return SIMSD_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
+  if (logit_dtype != SIMSD_DTYPE_FP32 && logit_dtype != SIMSD_DTYPE_BF16) return SIMSD_ERR_INVALID_ARG;
+  if (batch == 0) return SIMSD_OK;
+  if (!target_logits || !draft_tokens || !labels || !pos_ids || !accepted_len || !out_tokens ||
+      !out_pos || !n_commit || !dev_err)
+    return SIMSD_ERR_INVALID_ARG;
+  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (logit_dtype == SIMSD_DTYPE_BF16)
+    return accept_coupled_impl<__nv_bfloat16>((const __nv_bfloat16*)target_logits, draft_tokens, labels, pos_ids,
+                                              batch, B, gamma, V, temperature, seed, offset, accepted_len,
+                                              out_tokens, out_pos, n_commit, workspace, workspace_bytes,
+                                              dev_err, s);
+  return accept_coupled_impl<float>((const float*)target_logits, draft_tokens, labels, pos_ids, batch, B,
+                                    gamma, V, temperature, seed, offset, accepted_len, out_tokens, out_pos,
+                                    n_commit, workspace, workspace_bytes, dev_err, s);
+}
+
+SIMSD_API simsd_status simsd_accept_coupled(const float* target_logits, const int32_t* draft_tokens,
+                                            const uint8_t* labels, const int32_t* pos_ids, int batch,
+                                            int B, int gamma, int V, float temperature, uint64_t seed,
+                                            uint64_t offset, int32_t* accepted_len, int32_t* out_tokens,
+                                            int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                            size_t workspace_bytes, uint32_t* dev_err,
+                                            simsd_stream_t stream) {
+  return simsd_accept_coupled_ex(target_logits, SIMSD_DTYPE_FP32, draft_tokens, labels, pos_ids, batch, B,
+                                 gamma, V, temperature, seed, offset, accepted_len, out_tokens, out_pos,
+                                 n_commit, workspace, workspace_bytes, dev_err, stream);
 }
 
 // ------------------------------------------------------------------------------------

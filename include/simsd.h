@@ -236,6 +236,36 @@ simsd_status simsd_accept_coupled(const float* target_logits, const int32_t* dra
                                   size_t workspace_bytes, uint32_t* dev_err, simsd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * simsd_accept_ex, simsd_accept_coupled_ex -- simsd_accept and simsd_accept_coupled with
+ * the element type of the logits as an argument. (Library addition: a model head that
+ * emits bf16 logits is verified without a widening copy.)
+ *   logit_dtype  SIMSD_DTYPE_FP32: the logit arrays are float, exactly simsd_accept /
+ *                simsd_accept_coupled.
+ *                SIMSD_DTYPE_BF16: the logit arrays are bf16 [batch, B, V]; every entry is
+ *                widened exactly to fp32 on load and the operation proceeds on those fp32
+ *                values: the outputs equal those of the fp32 call on the widened arrays.
+ *                Other values return SIMSD_ERR_INVALID_ARG.
+ *   All other arguments, the workspace size (simsd_accept_workspace, the same for both
+ *   types), outputs, error bits and sentinels: as the fp32 calls.
+ * --------------------------------------------------------------------------------- */
+simsd_status simsd_accept_ex(const void* target_logits, const void* draft_logits,
+                             simsd_dtype logit_dtype, const int32_t* draft_tokens,
+                             const uint8_t* labels, int batch, int B, int gamma, int V,
+                             float temperature, uint64_t seed, uint64_t offset,
+                             int32_t* accepted_len, int32_t* out_tokens, int32_t* out_pos,
+                             int32_t* n_commit, void* workspace, size_t workspace_bytes,
+                             uint32_t* dev_err, simsd_stream_t stream);
+
+simsd_status simsd_accept_coupled_ex(const void* target_logits, simsd_dtype logit_dtype,
+                                     const int32_t* draft_tokens, const uint8_t* labels,
+                                     const int32_t* pos_ids, int batch, int B, int gamma, int V,
+                                     float temperature, uint64_t seed, uint64_t offset,
+                                     int32_t* accepted_len, int32_t* out_tokens,
+                                     int32_t* out_pos, int32_t* n_commit, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_err,
+                                     simsd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * simsd_accept_noalloc -- the same operation as simsd_accept, for callers that cannot
  * allocate device memory. (Library addition: the pages have no counterpart to this call.)
  *

@@ -323,6 +323,43 @@ def test_accept_temperatures_and_odd_vocab(T):
     assert (st.accepted_len.cpu().numpy() < w.gamma).any()
 
 
+BF16_ACCEPT_CASES = {
+    "tiny_fp32": dict(),
+    "tiny_odd_vocab": dict(base="tiny_fp32", batch=64, B=8, gamma=6, V=1001),
+    "gqa8b_bf16": dict(),
+    "gqa8b_t07": dict(base="gqa8b_bf16", temperature=0.7),
+    "large_block_bf16": dict(),
+    "ragged_bf16": dict(),
+}
+
+
+@pytest.mark.parametrize("case", list(BF16_ACCEPT_CASES))
+def test_accept_bf16_logits_bit_exact(case):
+    """bf16 target / draft logits through the step: against the oracle on their exactly
+    widened values, and identical to the fp32 call on those widened arrays (the kernels
+    widen each entry on load and change nothing else). Odd V takes the unvectorised loads."""
+    kw = dict(BF16_ACCEPT_CASES[case])
+    name = kw.pop("base", case)
+    w = W[name].with_(logit_dtype="bf16", **kw)
+    inputs, meta = H.make_case(w, seed=51)
+    assert inputs["target_logits"].dtype == torch.bfloat16
+    st = _step(w, inputs, meta, with_lse=False)
+    reqs = ACC_SAMPLE.get(name) or list(range(w.batch))
+    res = H.oracle_accept(inputs, st.labels, w.gamma, w.temperature, meta["philox_seed"],
+                          meta["philox_offset"], requests=reqs)
+    got = {k: getattr(st, k).cpu().numpy() for k in
+           ("accepted_len", "n_commit", "out_tokens", "out_pos")}
+    ties = H.check_accept(res, got, reqs)
+    assert ties <= max(1, len(reqs) // 100)
+    assert int(st.dev_err.item()) == 0
+    got32, err = _accept_outputs("workspace", inputs["target_logits"].float(),
+                                 inputs["draft_logits"].float(), inputs["draft_tokens"],
+                                 st.labels, w.gamma, w.temperature, meta["philox_seed"])
+    assert err == 0
+    for k in got:
+        assert np.array_equal(got[k], got32[k]), k
+
+
 def test_accept_invalid_labels_and_tokens():
     pkg = _pkg()
     B, V = 4, 100
@@ -352,7 +389,8 @@ def test_accept_invalid_labels_and_tokens():
 
 def _accept_outputs(path, tl, dl, toks, labels, gamma, T, seed, ws=None):
     """Runs one acceptance entry point: "workspace" (simsd_accept on a caller workspace,
-    `ws` or a fresh zeroed one) or "fixed" (simsd_accept_noalloc on the library's array)."""
+    `ws` or a fresh zeroed one), "bf16" (simsd_accept_ex on bf16 logits, same workspace
+    rule) or "fixed" (simsd_accept_noalloc on the library's array)."""
     pkg = _pkg()
     b, B, V = tl.shape
     out = {k: torch.full((b,), -7, dtype=torch.int32, device="cuda")
@@ -362,11 +400,11 @@ def _accept_outputs(path, tl, dl, toks, labels, gamma, T, seed, ws=None):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     args = (tl, dl, toks, labels, gamma, T, seed, 0, out["accepted_len"], out["out_tokens"],
             out["out_pos"], out["n_commit"])
-    if path == "workspace":
+    if path in ("workspace", "bf16"):
         if ws is None:
             ws = torch.zeros(pkg.simsd_accept_workspace(b, B, gamma, V), dtype=torch.uint8,
                              device="cuda")
-        pkg.simsd_accept(*args, ws, err)
+        (pkg.simsd_accept_ex if path == "bf16" else pkg.simsd_accept)(*args, ws, err)
     else:
         pkg.simsd_accept_noalloc(*args, err)
     torch.cuda.synchronize()
@@ -378,20 +416,24 @@ def _slot_order(labels_row, B):
     return [tau.index(t) for t in range(1, B + 1)]
 
 
-@pytest.mark.parametrize("path", ["workspace", "fixed"])
+@pytest.mark.parametrize("path", ["workspace", "fixed", "bf16"])
 @pytest.mark.parametrize("name", ["tiny_fp32", "gqa8b_bf16", "large_block_bf16"])
 def test_accept_greedy_bit_exact(name, path):
     """Greedy verification (temperature 0) against the oracle, bit-exact: draft tokens
     agree with the target's first-maximum choice on a prefix of every length 0..gamma, and
     some rows hold an exact tie of their maximum at an index half the vocabulary away
-    (another chunk), so the first-index rule is exercised across the chunk merge."""
+    (another chunk), so the first-index rule is exercised across the chunk merge. With
+    bf16 logits (8-bit mantissa) many rows also tie by rounding."""
     w = W[name]
     inputs, meta = H.make_case(w, seed=31)
     st = _step(w, inputs, meta, with_lse=False)
     b, B, V = inputs["target_logits"].shape
     tl = inputs["target_logits"].clone()
+    dl = inputs["draft_logits"]
+    if path == "bf16":
+        tl, dl = tl.to(torch.bfloat16), dl.to(torch.bfloat16)
     labels = H.to_np(st.labels)
-    tl_cpu = tl.cpu().numpy()
+    tl_cpu = H.to_np(tl)
     for r in range(0, b, 3):                      # ties: the maximum copied elsewhere
         for k in range(B):
             c = int(np.argmax(tl_cpu[r, k]))
@@ -409,11 +451,50 @@ def test_accept_greedy_bit_exact(name, path):
     toks = toks.cuda()
     case = dict(inputs, target_logits=tl, draft_tokens=toks)
     res = H.oracle_accept(case, st.labels, w.gamma, 0.0, meta["philox_seed"], 0)
-    got, err = _accept_outputs(path, tl, inputs["draft_logits"], toks, st.labels, w.gamma, 0.0,
-                               meta["philox_seed"])
+    got, err = _accept_outputs(path, tl, dl, toks, st.labels, w.gamma, 0.0, meta["philox_seed"])
     assert err == 0
     assert H.check_accept(res, got, list(range(b))) == 0
     assert set(res["accepted_len"].tolist()) == set(range(min(b, w.gamma + 1)))
+
+
+@pytest.mark.parametrize("ldt", ["fp32", "bf16"])
+@pytest.mark.parametrize("V", [5000, 5001])
+def test_accept_greedy_masked_rows(V, ldt):
+    """Greedy verification on masked vocabularies (-inf entries): a fully masked row (its
+    first index is the choice), rows masked except a few entries, the maximum at the first
+    or the last entry, and a maximum repeated across chunks; V = 5001 takes the unvectorised
+    loads. Bit-exact against the oracle."""
+    b, B, gamma = 12, 4, 4
+    g = torch.Generator(device="cpu").manual_seed(61)
+    tl = torch.randn(b, B, V, generator=g) * 2
+    tl[0] = -math.inf                                   # every row of request 0 fully masked
+    keep = torch.rand(b, B, V, generator=g) < 0.01
+    tl[1][~keep[1]] = -math.inf                         # request 1: 1 % of the entries left
+    tl[2, :, 0] = 50.0                                  # maximum at the first entry
+    tl[3, :, V - 1] = 50.0                              # ... at the last entry
+    tl[4, :, 7] = 40.0
+    tl[4, :, V - 3] = 40.0                              # repeated far apart: the first wins
+    tl[5, :, : V // 2] = -math.inf                      # first half masked
+    if ldt == "bf16":
+        tl = tl.to(torch.bfloat16)
+    tl_cpu = H.to_np(tl)
+    tau = torch.stack([torch.randperm(B, generator=g) + 1 for _ in range(b)]).to(torch.int32)
+    labels = torch.cat([tau, tau + 128], 1).to(torch.uint8)
+    toks = torch.zeros(b, B, dtype=torch.int32)
+    for r in range(b):
+        order = _slot_order(labels[r].numpy(), B)
+        L = r % (gamma + 1)
+        for t in range(gamma):
+            k = order[t]
+            c = oracle.greedy_choice(tl_cpu[r, k])
+            toks[r, k] = c if t < L else (c + 1) % V
+    res = oracle.accept(tl_cpu, tl_cpu, toks.numpy(), labels.numpy(), gamma, 0.0, 3, 0)
+    path = "bf16" if ldt == "bf16" else "workspace"
+    got, err = _accept_outputs(path, tl.cuda(), tl.cuda(), toks.cuda(), labels.cuda(), gamma,
+                               0.0, 3)
+    assert err == 0
+    assert H.check_accept(res, got, list(range(b))) == 0
+    assert res["accepted_len"][0] == 0 and 0 in res["out_tokens"][0].tolist()
 
 
 def _coupled_outputs(tl, toks, labels, pos, gamma, T, seed):
@@ -425,19 +506,23 @@ def _coupled_outputs(tl, toks, labels, pos, gamma, T, seed):
             for k in ("out_tokens", "out_pos")}
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(pkg.simsd_accept_workspace(b, B, gamma, V), dtype=torch.uint8, device="cuda")
-    pkg.simsd_accept_coupled(tl, toks, labels, pos, gamma, T, seed, 0, out["accepted_len"],
-                             out["out_tokens"], out["out_pos"], out["n_commit"], ws, err)
+    call = pkg.simsd_accept_coupled_ex if tl.dtype == torch.bfloat16 else pkg.simsd_accept_coupled
+    call(tl, toks, labels, pos, gamma, T, seed, 0, out["accepted_len"], out["out_tokens"],
+         out["out_pos"], out["n_commit"], ws, err)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}, int(err.item())
 
 
-@pytest.mark.parametrize("name,T,later", [("tiny_fp32", 1.0, False), ("gqa8b_bf16", 1.0, False),
-                                          ("gqa8b_bf16", 0.8, True), ("gqa8b_bf16", 0.0, False)])
-def test_accept_coupled_bit_exact(name, T, later):
+@pytest.mark.parametrize("name,T,later,ldt", [
+    ("tiny_fp32", 1.0, False, "fp32"), ("gqa8b_bf16", 1.0, False, "fp32"),
+    ("gqa8b_bf16", 0.8, True, "fp32"), ("gqa8b_bf16", 0.0, False, "fp32"),
+    ("gqa8b_bf16", 1.0, True, "bf16"), ("tiny_fp32", 0.0, False, "bf16")])
+def test_accept_coupled_bit_exact(name, T, later, ldt):
     """Coupled-noise verification against the oracle. Half of the requests propose the
     drafter's coupled choice (draft logits, same noise), the others the target's own (all
-    accepted); bit-exact except where the oracle's two best keys are within 1e-4."""
-    w = W[name].with_(temperature=T if T > 0 else 1.0)
+    accepted); bit-exact except where the oracle's two best keys are within 1e-4. With bf16
+    logits the oracle runs on their exactly widened values."""
+    w = W[name].with_(temperature=T if T > 0 else 1.0, logit_dtype=ldt)
     tau = _later_round_taus(np.random.default_rng(23), w.batch, w.B) if later else None
     inputs, meta = H.make_case(w, seed=41, tau=tau)
     st = _step(w, inputs, meta, with_lse=False)

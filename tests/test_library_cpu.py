@@ -72,6 +72,19 @@ def test_host_argument_errors_return_status(lib):
     assert lib.simsd_accept(*args) == 1          # null pointers
     assert lib.simsd_accept_workspace(2, 4, 4, 100) > 0
     assert lib.simsd_accept_workspace(2, 4, 5, 100) == 0
+    # the logit-type entries: an unknown type is invalid; batch 0 with a known one is a no-op
+    ex = [None, None, 1, None, None, 0, 4, 4, 100, 1.0, 0, 0] + [None] * 5 + [0, None, None]
+    assert lib.simsd_accept_ex(*ex) == 0
+    ex[2] = 2
+    assert lib.simsd_accept_ex(*ex) == 1
+    ex[2], ex[5] = 1, 2
+    assert lib.simsd_accept_ex(*ex) == 1          # null pointers
+    cx = [None, 1, None, None, None, 0, 4, 4, 100, 1.0, 0, 0] + [None] * 5 + [0, None, None]
+    assert lib.simsd_accept_coupled_ex(*cx) == 0
+    cx[1] = 7
+    assert lib.simsd_accept_coupled_ex(*cx) == 1
+    cx[1], cx[5] = 0, 2
+    assert lib.simsd_accept_coupled_ex(*cx) == 1  # null pointers
 
 
 def test_attention_parameter_checks(lib):

@@ -39,6 +39,7 @@ class Workload:
     draft_noise_std: float = math.sqrt(0.5)
     temperature: float = 1.0
     identity_tau_frac: float = 0.0   # share of requests whose step labels are 1..B in order
+    logit_dtype: str = "fp32"        # "fp32" or "bf16" target / draft logits
     seed: int = 0
 
     @property
@@ -147,19 +148,24 @@ def make_attention_inputs(w: Workload, prompt_len: torch.Tensor, seed: Optional[
 
 def make_accept_inputs(w: Workload, seed: Optional[int] = None, device="cpu",
                        V: Optional[int] = None):
-    """Target / draft logits [b, B, V] fp32 (indexed by block slot k), draft tokens
-    [b, B] int32 drawn from the draft distribution at temperature T (its argmax at T = 0),
-    and a Philox (seed, offset) pair for the acceptance uniforms."""
+    """Target / draft logits [b, B, V] (indexed by block slot k) in `w.logit_dtype` (bf16:
+    the fp32 draws rounded to nearest), draft tokens [b, B] int32 drawn from the draft
+    distribution of those logits at temperature T (its argmax at T = 0), and a Philox
+    (seed, offset) pair for the acceptance uniforms."""
     seed = w.seed if seed is None else seed
     V = w.V if V is None else V
     g = _gen(seed + 2, device)
     b, B = w.batch, w.B
     target = torch.randn(b, B, V, generator=g, device=device) * w.logit_std
     draft = target + torch.randn(b, B, V, generator=g, device=device) * w.draft_noise_std
+    if w.logit_dtype == "bf16":
+        target, draft = target.to(torch.bfloat16), draft.to(torch.bfloat16)
+    elif w.logit_dtype != "fp32":
+        raise ValueError(w.logit_dtype)
     if w.temperature == 0:   # a greedy drafter proposes its own first maximum
         tokens = torch.argmax(draft, dim=-1).to(torch.int32)
     else:
-        probs = torch.softmax(draft.reshape(b * B, V) / w.temperature, dim=-1)
+        probs = torch.softmax(draft.float().reshape(b * B, V) / w.temperature, dim=-1)
         tokens = torch.multinomial(probs, 1, generator=g).reshape(b, B).to(torch.int32)
         del probs
     return {"target_logits": target, "draft_logits": draft, "draft_tokens": tokens,
@@ -177,7 +183,8 @@ def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor, target_only: bool =
     b, B, D = w.batch, w.B, w.D
     kv_prompt = 2 * P_sum * w.Hkv * D * esz
     resp = b * 2 * B * D * esz * (2 * w.Hq + 2 * w.Hkv)   # q + out, k + v
-    accept = b * w.gamma * (1 if (w.temperature == 0 or target_only) else 2) * w.V * 4
+    lsz = 2 if w.logit_dtype == "bf16" else 4
+    accept = b * w.gamma * (1 if (w.temperature == 0 or target_only) else 2) * w.V * lsz
     flops = 0
     for P in prompt_len.tolist():
         flops += 4 * 2 * B * w.Hq * (P + B) * D
