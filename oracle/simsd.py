@@ -21,6 +21,10 @@ Each function restates a definition from the pages, in their notation:
                normalised residual max(0, p - q) (S2D2 page, "方法步骤详情" step (5));
                the race draw is the Gumbel-max / exponential-race identity (SPOT page,
                "Gumbel-Max 技巧与随机耦合").
+* routing   -- S2D2 page, "方法步骤详情" step (4) (the score-threshold routing policy of
+               its Algorithm 4): the expected accepted-prefix length
+               K^ = sum_{k=1..L} prod_{i=1..k} alpha_i with a margin-based
+               alpha_i = 1[m_i >= tau_margin] or an entropy-based alpha_i = exp(-beta H~_i).
 
 Readings taken where the pages are silent (all listed in the design notes):
   prompt tokens carry tau = 0 and are visible to every response row; RoPE pairs are
@@ -46,6 +50,10 @@ INVALID_LABEL = 0xFF
 ERR_TAU = 1          # step labels are not a permutation of 1..B
 ERR_PROMPT_LEN = 2   # negative prompt length
 ERR_TOKEN = 4        # draft token id outside [0, V)
+
+# Estimators of the per-step acceptance alpha_i (same values as the C interface).
+KHAT_MARGIN = 0      # alpha_i = 1[m_i >= tau_margin]
+KHAT_ENTROPY = 1     # alpha_i = exp(-beta * H~_i)
 
 
 # ----------------------------------------------------------------------------- layout
@@ -385,3 +393,56 @@ def accept(target_logits, draft_logits, draft_tokens, labels, gamma, temperature
         diag[r] = {"margins": margins, "race_top2": race}
     return {"accepted_len": acc_len, "n_commit": n_commit, "out_tokens": out_tokens,
             "out_pos": out_pos, "err": err, "diag": diag}
+
+
+# ----------------------------------------------------------------------------- routing
+def draft_confidence(logits, temperature):
+    """Confidence of the draft at one position, from its distribution p = softmax(logits / T):
+    the margin m = p_(1) - p_(2) between its two largest probabilities, and the entropy
+    normalised by its largest possible value, H~ = H(p) / ln V (0 when V = 1). These are the
+    m_i and H~_i of the routing estimators (S2D2 page, "方法步骤详情" step (4))."""
+    p = softmax(logits, temperature)
+    V = p.shape[-1]
+    top = np.sort(p)[::-1]
+    margin = float(top[0] - (top[1] if V > 1 else 0.0))
+    nz = p[p > 0]                     # 0 log 0 = 0 (masked entries)
+    H = float(-np.sum(nz * np.log(nz)))
+    return margin, (H / math.log(V) if V > 1 else 0.0)
+
+
+def expected_prefix(draft_logits, labels, gamma, temperature, mode, tau_margin=0.0, beta=1.0,
+                    requests=None):
+    """Expected accepted-prefix length of every request (S2D2 page, "方法步骤详情" step (4)):
+
+        K^ = sum_{k=1..L} prod_{i=1..k} alpha_i
+
+    over the L = min(gamma, R) steps that verification would walk, in the draft's time order
+    (step i is the slot o_i labelled i; left to right when tau is the identity), with
+    alpha_i = 1[m_i >= tau_margin] (mode KHAT_MARGIN) or exp(-beta H~_i) (KHAT_ENTROPY), m_i
+    and H~_i from `draft_confidence` at temperature T > 0.
+
+    Returns khat [b] (-1 for a request whose labels are invalid, which also sets ERR_TAU),
+    alpha, margin and entropy [b, gamma] (step order; alpha 0 and margin / entropy NaN past
+    L or for an invalid request) and the error word."""
+    dl = np.asarray(draft_logits)
+    labels = np.asarray(labels)
+    b, B, V = dl.shape
+    khat = np.full(b, -1.0)
+    alpha = np.zeros((b, gamma))
+    margin = np.full((b, gamma), np.nan)
+    entropy = np.full((b, gamma), np.nan)
+    err = 0
+    for r in (range(b) if requests is None else requests):
+        order = _order_from_labels(labels[r], B)
+        if order is None:
+            err |= ERR_TAU
+            continue
+        for i, k in enumerate(order[:gamma]):
+            margin[r, i], entropy[r, i] = draft_confidence(dl[r, k], temperature)
+            if mode == KHAT_MARGIN:
+                alpha[r, i] = 1.0 if margin[r, i] >= tau_margin else 0.0
+            else:
+                alpha[r, i] = math.exp(-beta * entropy[r, i])
+        L = min(gamma, len(order))
+        khat[r] = sum(float(np.prod(alpha[r, : k + 1])) for k in range(L))
+    return {"khat": khat, "alpha": alpha, "margin": margin, "entropy": entropy, "err": err}

@@ -11,6 +11,10 @@
 * Acceptance: special cases, the closed form E[a] = sum_k prod_{r<=k} (1 - TV(p_r, q_r))
   (total-variation bound on the SPOT page), and Monte Carlo: committed tokens follow the
   target distribution (speculative decoding is lossless, S2D2 / SPOT pages).
+* Routing estimator K^ (S2D2 page, step (4)): the expectation of the accepted-prefix
+  length under independent acceptances, enumerated outcome by outcome; entropy against
+  scipy; closed forms for uniform and two-level distributions; a hand-worked margin case
+  in a permuted step order; later rounds.
 """
 import itertools
 import math
@@ -598,3 +602,121 @@ def test_monte_carlo_commits_follow_target_and_mean_length_closed_form():
     keep = exp_rej > 5
     chi2 = ((counts_rej[keep] - exp_rej[keep]) ** 2 / exp_rej[keep]).sum()
     assert stats.chi2.sf(chi2, keep.sum() - 1) > 1e-3
+
+
+# --------------------------------------------------------------------- routing estimator
+def _labels_from_tau(tau):
+    tau = np.asarray(tau, dtype=np.int64)
+    return np.concatenate([tau, tau + 128], axis=-1).astype(np.uint8)
+
+
+def _prefix_expectation_by_enumeration(alphas):
+    """E[number of leading accepts] when step i is accepted independently with
+    probability alphas[i]: every accept/reject pattern weighted by its probability."""
+    total = 0.0
+    for pattern in itertools.product([0, 1], repeat=len(alphas)):
+        w = 1.0
+        for a, x in zip(alphas, pattern):
+            w *= a if x else 1.0 - a
+        lead = 0
+        while lead < len(pattern) and pattern[lead]:
+            lead += 1
+        total += w * lead
+    return total
+
+
+@pytest.mark.parametrize("B,gamma", [(4, 4), (8, 6), (6, 6)])
+def test_khat_entropy_is_expected_prefix_of_independent_acceptances(B, gamma):
+    """Entropy estimator with a permuted step order: alpha_i = exp(-beta H(p_i) / ln V),
+    the entropies taken by scipy in the oracle's step order, then K^ against the
+    enumeration of every acceptance pattern."""
+    from scipy import stats
+    rng = np.random.default_rng(5)
+    V, T, beta = 50, 0.8, 1.7
+    dl = rng.normal(0, 2, (3, B, V))
+    tau = np.stack([rng.permutation(B) + 1 for _ in range(3)])
+    res = oracle.expected_prefix(dl, _labels_from_tau(tau), gamma, T, oracle.KHAT_ENTROPY,
+                                 beta=beta)
+    assert res["err"] == 0
+    for r in range(3):
+        slots = [int(np.where(tau[r] == i)[0][0]) for i in range(1, gamma + 1)]
+        alphas = []
+        for k in slots:
+            z = dl[r, k] / T
+            p = np.exp(z - z.max())
+            p /= p.sum()
+            alphas.append(math.exp(-beta * stats.entropy(p) / math.log(V)))
+        np.testing.assert_allclose(res["alpha"][r], alphas, rtol=1e-12)
+        assert abs(res["khat"][r] - _prefix_expectation_by_enumeration(alphas)) < 1e-12
+
+
+def test_khat_uniform_and_one_hot_closed_forms():
+    """Uniform draft logits: H~ = 1 and margin 0, so K^ = sum_{k=1..L} e^(-beta k) with the
+    entropy estimator and 0 with a positive margin threshold (L with threshold 0). A
+    near-one-hot distribution: H~ -> 0, margin -> 1, K^ -> L."""
+    B, V, beta = 5, 64, 0.9
+    tau = np.array([[2, 5, 1, 4, 3]])
+    lab = _labels_from_tau(tau)
+    uni = np.zeros((1, B, V))
+    e = oracle.expected_prefix(uni, lab, B, 1.0, oracle.KHAT_ENTROPY, beta=beta)
+    geo = math.exp(-beta) * (1 - math.exp(-beta * B)) / (1 - math.exp(-beta))
+    assert abs(e["khat"][0] - geo) < 1e-12
+    np.testing.assert_allclose(e["entropy"][0], 1.0, rtol=1e-12)
+    np.testing.assert_allclose(e["margin"][0], 0.0, atol=1e-15)
+    assert oracle.expected_prefix(uni, lab, B, 1.0, oracle.KHAT_MARGIN, tau_margin=0.01)["khat"][0] == 0
+    assert oracle.expected_prefix(uni, lab, B, 1.0, oracle.KHAT_MARGIN, tau_margin=0.0)["khat"][0] == B
+    hot = np.zeros((1, B, V))
+    hot[..., 7] = 60.0
+    h = oracle.expected_prefix(hot, lab, B, 1.0, oracle.KHAT_ENTROPY, beta=beta)
+    assert abs(h["khat"][0] - B) < 1e-12 and np.all(h["entropy"][0] < 1e-20)
+    np.testing.assert_allclose(h["margin"][0], 1.0, rtol=1e-20)
+
+
+@pytest.mark.parametrize("n_hi", [1, 2, 7])
+def test_khat_two_level_distribution(n_hi):
+    """n entries at logit a and V - n at logit c: p_hi = e^a / (n e^a + (V - n) e^c), and
+    the entropy and margin follow in closed form (margin 0 when the maximum is shared)."""
+    V, a, c, T = 40, 3.0, -1.0, 1.5
+    x = np.full(V, c)
+    x[[3 * i + 1 for i in range(n_hi)]] = a
+    ea, ec = math.exp(a / T), math.exp(c / T)
+    Z = n_hi * ea + (V - n_hi) * ec
+    ph, pl = ea / Z, ec / Z
+    H = -(n_hi * ph * math.log(ph) + (V - n_hi) * pl * math.log(pl))
+    m, hn = oracle.draft_confidence(x, T)
+    assert abs(hn - H / math.log(V)) < 1e-13
+    assert abs(m - ((ph - pl) if n_hi == 1 else 0.0)) < 1e-15
+
+
+def test_khat_margin_follows_the_step_order():
+    """Margin estimator, worked by hand. Slots 0 and 2 confident (margin near 1), slot 1
+    flat (margin 0). tau = (2, 3, 1): steps visit slots 2, 0, 1, so alpha = (1, 1, 0) and
+    K^ = 1 + 1 + 0 = 2; with tau = identity alpha = (1, 0, 1) and K^ = 1."""
+    V = 16
+    dl = np.zeros((2, 3, V))
+    dl[:, 0, 4] = dl[:, 2, 9] = 30.0
+    lab = _labels_from_tau([[2, 3, 1], [1, 2, 3]])
+    res = oracle.expected_prefix(dl, lab, 3, 1.0, oracle.KHAT_MARGIN, tau_margin=0.5)
+    assert res["alpha"].tolist() == [[1.0, 1.0, 0.0], [1.0, 0.0, 1.0]]
+    assert res["khat"].tolist() == [2.0, 1.0]
+
+
+def test_khat_later_rounds_temperature_and_invalid_labels():
+    """Committed slots (tau = 0) are skipped and L = min(gamma, R); logits / T at T = 1
+    equal logits at T; invalid labels give K^ = -1 and the tau error bit; masked (-inf)
+    entries hold no probability."""
+    rng = np.random.default_rng(9)
+    B, V, beta = 6, 30, 2.0
+    dl = rng.normal(0, 1.5, (3, B, V))
+    dl[0, :, :5] = -np.inf
+    lab = _labels_from_tau([[0, 2, 0, 1, 3, 0], [3, 1, 2, 4, 6, 5], [1, 1, 2, 3, 4, 5]])
+    res = oracle.expected_prefix(dl, lab, 4, 0.7, oracle.KHAT_ENTROPY, beta=beta)
+    assert res["err"] == oracle.ERR_TAU and res["khat"][2] == -1
+    slots0 = [3, 1, 4]                      # R = 3 < gamma: steps 1..3
+    a0 = [math.exp(-beta * oracle.draft_confidence(dl[0, k], 0.7)[1]) for k in slots0]
+    assert abs(res["khat"][0] - (a0[0] + a0[0] * a0[1] + a0[0] * a0[1] * a0[2])) < 1e-12
+    assert res["alpha"][0, 3] == 0 and np.isnan(res["entropy"][0, 3])
+    scaled = oracle.expected_prefix(dl / 0.7, lab, 4, 1.0, oracle.KHAT_ENTROPY, beta=beta)
+    np.testing.assert_allclose(scaled["khat"][:2], res["khat"][:2], rtol=1e-12)
+    p = oracle.softmax(dl[0, 0], 0.7)
+    assert np.all(p[:5] == 0) and abs(p.sum() - 1) < 1e-12
