@@ -53,6 +53,9 @@ def _args():
                     help="override the workload's sampling temperature (0: greedy verification)")
     ap.add_argument("--coupled", action="store_true",
                     help="coupled-noise verification (simsd_accept_coupled) instead of rejection sampling")
+    ap.add_argument("--khat", choices=["margin", "entropy"], default=None,
+                    help="also estimate the expected accepted-prefix length (simsd_expected_prefix) "
+                         "from the draft logits in every step")
     ap.add_argument("--logit-dtype", choices=["fp32", "bf16"], default=None,
                     help="element type of the target / draft logits (default: the workload's, fp32)")
     return ap.parse_args()
@@ -205,6 +208,8 @@ def _config(w, args, launch):
     cfg["launch"] = launch
     cfg["verification"] = "coupled noise" if getattr(args, "coupled", False) else (
         "greedy" if w.temperature == 0 else "rejection sampling")
+    if getattr(args, "khat", None):
+        cfg["expected_prefix"] = args.khat
     return cfg
 
 
@@ -454,17 +459,22 @@ def run_ours(args):
     alg = workloads.algorithmic_bytes(w, probe["prompt_len"])
     n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / max(1, alg["total_bytes"]))))
     sets = _make_sets(w, args, device, n_sets, rank)
+    khat_mode = {None: None, "margin": pkg.KHAT_MARGIN, "entropy": pkg.KHAT_ENTROPY}[args.khat]
     steps = [pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
                             temperature=w.temperature, cache_layout=args.cache_layout,
-                            philox_seed=s["_seed"], coupled=args.coupled) for s in sets]
-    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled)
-            for s in sets]
+                            philox_seed=s["_seed"], coupled=args.coupled, khat_mode=khat_mode,
+                            khat_temperature=w.temperature if w.temperature > 0 else 1.0)
+             for s in sets]
+    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled,
+                                        with_khat=khat_mode is not None) for s in sets]
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()
 
     # one CUDA graph per step (and per call, for the per-call roofline timing)
     use_graph = not args.no_graph
     g_step, g_calls = [], {"layout": [], "attention": [], "accept": []}
+    if khat_mode is not None:
+        g_calls["expected_prefix"] = []
     if use_graph:
         with torch.cuda.stream(stream):
             for st in steps:          # untimed eager pass: module loading, first launches
@@ -530,7 +540,7 @@ def run_ours(args):
             for name, gl in g_calls.items():
                 per_call[name] = _time_graphs(gl, reps, stream) / reps
     mean_alg = {k: statistics.mean(a[k] for a in algs)
-                for k in ("attn_bytes", "accept_bytes", "total_bytes", "attn_flops")}
+                for k in ("attn_bytes", "accept_bytes", "khat_bytes", "total_bytes", "attn_flops")}
     peak, peak_kind = _peaks()
     roofline = None
     if per_call:
@@ -548,6 +558,14 @@ def run_ours(args):
                     "algorithmic_bytes_per_launch": call_bytes[dom],
                     "avg_launch_us": per_call[dom] * 1e6,
                     "per_call_us": {k: v * 1e6 for k, v in per_call.items()}}
+    khat_line = None
+    if per_call and "expected_prefix" in per_call:
+        kb = mean_alg["khat_bytes"]
+        ka = kb / per_call["expected_prefix"] / 1e9
+        khat_line = {"bound": "hbm", "kernel": "simsd_expected_prefix (khat_stats + khat_finish)",
+                     "mode": args.khat, "achieved": ka, "peak": peak, "unit": "GB/s",
+                     "frac": ka / peak, "algorithmic_bytes_per_launch": kb,
+                     "avg_launch_us": per_call["expected_prefix"] * 1e6}
     step_s = elapsed / args.steps
     step_frac = mean_alg["total_bytes"] / step_s / 1e9 / peak
 
@@ -565,7 +583,7 @@ def run_ours(args):
     # layout; attention (the tensor-core kernel and its split merge, or the fp32 / D 64
     # kernel alone); accept_stats and accept_finish
     tc_path = w.dtype == "bf16" and w.D == 128 and 2 * w.B * (w.Hq // w.Hkv) <= 256
-    launches_per_step = 1 + (2 if tc_path else 1) + 2
+    launches_per_step = 1 + (2 if tc_path else 1) + 2 + (2 if khat_mode is not None else 0)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -576,6 +594,7 @@ def run_ours(args):
             "pct_hbm_roofline_step": 100.0 * step_frac,
             "algorithmic_bytes_per_step": mean_alg["total_bytes"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            **({"khat_roofline": khat_line} if khat_line else {}),
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
             "dev_err": errs, "wall_s_timed": wall}
     if rank == 0:

@@ -10,15 +10,18 @@ from __future__ import annotations
 import torch
 
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
-                       DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, LIB_PATH, AttnParams,
+                       DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, KHAT_ENTROPY, KHAT_MARGIN,
+                       LIB_PATH, AttnParams,
                        SimsdError, load_library, make_attn_params, simsd_accept, simsd_accept_coupled,
                        simsd_accept_coupled_ex, simsd_accept_ex, simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
-                       simsd_accept_workspace, simsd_build_layout, simsd_last_cuda_error, simsd_status_str,
+                       simsd_accept_workspace, simsd_build_layout, simsd_expected_prefix,
+                       simsd_expected_prefix_workspace, simsd_last_cuda_error, simsd_status_str,
                        simsd_verify_attention, simsd_verify_attention_workspace,
                        simsd_version)
 
 __all__ = ["VerifyStep", "simsd_build_layout", "simsd_verify_attention", "simsd_accept",
            "simsd_accept_coupled", "simsd_accept_ex", "simsd_accept_coupled_ex",
+           "simsd_expected_prefix", "simsd_expected_prefix_workspace",
            "simsd_verify_attention_workspace", "simsd_accept_workspace", "make_attn_params",
            "load_library", "SimsdError"]
 
@@ -28,14 +31,18 @@ class VerifyStep:
 
     ``inputs`` holds device tensors: tau, prompt_len, q, k_resp, v_resp, k_cache, v_cache,
     cache_start (int64 [b]), target_logits, draft_logits (both fp32 or both bf16),
-    draft_tokens. Outputs live in
+    draft_tokens. With ``khat_mode`` set (KHAT_MARGIN or KHAT_ENTROPY) the step also
+    estimates every request's expected accepted-prefix length from the draft logits
+    (``khat``, ``alpha``) between the layout and the attention. Outputs live in
     this object (``pos_ids``, ``labels``, ``out``, ``lse``, ``accepted_len``, ``n_commit``,
     ``out_tokens``, ``out_pos``, ``dev_err``) and are overwritten by every ``run``.
     """
 
     def __init__(self, inputs: dict, gamma: int, rope_theta: float, temperature: float = 1.0,
                  cache_layout: str = "NHD", softmax_scale: float = 0.0, with_lse: bool = True,
-                 philox_seed: int = 0, philox_offset: int = 0, coupled: bool = False):
+                 philox_seed: int = 0, philox_offset: int = 0, coupled: bool = False,
+                 khat_mode=None, tau_margin: float = 0.5, beta: float = 1.0,
+                 khat_temperature: float = 1.0):
         load_library()
         dev = inputs["q"].device
         b, twoB, Hq, D = inputs["q"].shape
@@ -68,10 +75,24 @@ class VerifyStep:
         if ws_acc == 0:
             raise SimsdError(1, "simsd_accept_workspace")
         self.ws_accept = torch.empty(ws_acc, dtype=torch.uint8, device=dev)
+        self.khat_mode = khat_mode
+        if khat_mode is not None:
+            self.khat_args = (khat_temperature, int(khat_mode), tau_margin, beta)
+            self.khat = torch.empty(b, dtype=torch.float32, device=dev)
+            self.alpha = torch.empty(b, gamma, dtype=torch.float32, device=dev)
+            ws_k = simsd_expected_prefix_workspace(b, B, gamma, V)
+            if ws_k == 0:
+                raise SimsdError(1, "simsd_expected_prefix_workspace")
+            self.ws_khat = torch.empty(ws_k, dtype=torch.uint8, device=dev)
 
     def layout(self, stream=None):
         simsd_build_layout(self.inputs["tau"], self.inputs["prompt_len"], self.pos_ids,
                            self.labels, self.dev_err, stream)
+
+    def expected_prefix(self, stream=None):
+        simsd_expected_prefix(self.inputs["draft_logits"], self.labels, self.gamma,
+                              *self.khat_args, self.khat, self.alpha, self.ws_khat,
+                              self.dev_err, stream)
 
     def attention(self, stream=None):
         simsd_verify_attention(self.params, self.ws_attn, stream)
@@ -91,5 +112,7 @@ class VerifyStep:
 
     def run(self, stream=None):
         self.layout(stream)
+        if self.khat_mode is not None:
+            self.expected_prefix(stream)
         self.attention(stream)
         self.accept(stream)

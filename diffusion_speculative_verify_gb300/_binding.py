@@ -20,12 +20,14 @@ STATUS_NAMES = {0: "SIMSD_OK", 1: "SIMSD_ERR_INVALID_ARG", 2: "SIMSD_ERR_UNSUPPO
                 3: "SIMSD_ERR_WORKSPACE", 4: "SIMSD_ERR_CUDA", 5: "SIMSD_ERR_TIMEOUT"}
 DEVERR_TAU, DEVERR_PROMPT_LEN, DEVERR_TOKEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DTYPE_FP32, DTYPE_BF16 = 0, 1
+KHAT_MARGIN, KHAT_ENTROPY = 0, 1
 CACHE_NHD, CACHE_HND = 0, 1
 
 EXPORTED = ["simsd_status_str", "simsd_version", "simsd_last_cuda_error", "simsd_build_layout",
             "simsd_verify_attention_workspace", "simsd_verify_attention",
             "simsd_accept_workspace", "simsd_accept", "simsd_accept_coupled",
             "simsd_accept_ex", "simsd_accept_coupled_ex",
+            "simsd_expected_prefix_workspace", "simsd_expected_prefix",
             "simsd_accept_noalloc", "simsd_accept_noalloc_max_scratch"]
 
 
@@ -90,6 +92,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.simsd_accept_coupled_ex.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64,
                                             u64, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.simsd_accept_coupled_ex.restype = i32
+    lib.simsd_expected_prefix_workspace.argtypes = [i32, i32, i32, i32]
+    lib.simsd_expected_prefix_workspace.restype = sz
+    lib.simsd_expected_prefix.argtypes = [vp, i32, vp, i32, i32, i32, i32, f32, i32, f32, f32,
+                                          vp, vp, vp, sz, vp, vp]
+    lib.simsd_expected_prefix.restype = i32
     lib.simsd_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                          vp, vp, vp, vp, vp, vp]
     lib.simsd_accept_noalloc.restype = i32
@@ -294,6 +301,30 @@ def simsd_accept_coupled_ex(target_logits, draft_tokens, labels, pos_ids, gamma,
         _ptr(accepted_len), _ptr(out_tokens), _ptr(out_pos), _ptr(n_commit), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream(stream))
     _raise(st, "simsd_accept_coupled_ex")
+
+
+def simsd_expected_prefix_workspace(batch: int, B: int, gamma: int, V: int) -> int:
+    return int(load_library().simsd_expected_prefix_workspace(batch, B, gamma, V))
+
+
+def simsd_expected_prefix(draft_logits, labels, gamma, temperature, mode, tau_margin, beta,
+                          khat, alpha, workspace, dev_err, stream=None):
+    """Expected accepted-prefix length of every request from its draft logits (fp32 or
+    bf16 [b, B, V]); `alpha` ([b, gamma] float32) may be None."""
+    dt = _logit_dtype(draft_logits, "draft_logits")
+    _check(draft_logits, "draft_logits")
+    _check(labels, "labels", torch.uint8)
+    _check(khat, "khat", torch.float32)
+    if alpha is not None:
+        _check(alpha, "alpha", torch.float32)
+    _check(workspace, "workspace", torch.uint8)
+    _check(dev_err, "dev_err", torch.int32)
+    b, B, V = draft_logits.shape
+    st = load_library().simsd_expected_prefix(
+        _ptr(draft_logits), dt, _ptr(labels), b, B, int(gamma), V, float(temperature),
+        int(mode), float(tau_margin), float(beta), _ptr(khat), _ptr(alpha), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(stream))
+    _raise(st, "simsd_expected_prefix")
 
 
 def simsd_accept_noalloc_max_scratch() -> int:

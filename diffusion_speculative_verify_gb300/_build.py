@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsimsd.so")
-SOURCES = ["layout.cu", "attn_simt.cu", "attn_tc.cu", "accept.cu", "api.cu"]
+SOURCES = ["layout.cu", "attn_simt.cu", "attn_tc.cu", "accept.cu", "route.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -10,6 +10,9 @@
  *   simsd_accept            min(1, p/q) prefix acceptance along the step order, then
  *                           residual resampling at the first rejected slot.
  *
+ * and, before the verify forward when a caller routes requests, simsd_expected_prefix
+ * (the expected accepted-prefix length K^ of every request from its draft logits).
+ *
  * Conventions shared by every call
  *   - All array pointers are DEVICE pointers owned by the caller; the library keeps no
  *     reference after the call returns. Every call is asynchronous on `stream` (a
@@ -36,6 +39,8 @@
  *   [SimSD-P] gist.science SimSD summary, sections 1-4 (same method; tau is a permutation).
  *   [S2D2-5]  S2D2 page, "方法步骤详情" step (5): residual distribution (P_ver - P)^+.
  *   [SPOT-G]  SPOT page, "Gumbel-Max 技巧与随机耦合": argmax(log p + G) samples p.
+ *   [S2D2-4]  S2D2 page, "方法步骤详情" step (4): routing by the expected accepted-prefix
+ *             length K^ = sum_k prod_{i<=k} alpha_i (margin- or entropy-based alpha_i).
  *   [SPOT-C]  SPOT page, core-innovation and Algorithm 2 paragraphs: coupled-noise
  *             verification, a Gumbel table G_{a,v} indexed by absolute output position
  *             shared by drafter and target; the target's transition Phi_G is then
@@ -73,6 +78,9 @@ typedef enum {
 #define SIMSD_LABEL_INVALID 0xFFu
 
 typedef enum { SIMSD_DTYPE_FP32 = 0, SIMSD_DTYPE_BF16 = 1 } simsd_dtype;
+
+/* Estimators of the per-step acceptance alpha_i of simsd_expected_prefix. */
+typedef enum { SIMSD_KHAT_MARGIN = 0, SIMSD_KHAT_ENTROPY = 1 } simsd_khat_mode;
 
 /* Cache layouts of the packed prompt K/V (keys stored already rotated at positions
  * 0..P-1 of their request):
@@ -264,6 +272,41 @@ simsd_status simsd_accept_coupled_ex(const void* target_logits, simsd_dtype logi
                                      int32_t* out_pos, int32_t* n_commit, void* workspace,
                                      size_t workspace_bytes, uint32_t* dev_err,
                                      simsd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * simsd_expected_prefix  [S2D2-4]; steps and later rounds as simsd_accept.
+ *
+ * Routing statistic, computed from the draft logits alone (before the verify forward):
+ * for every request r the expected accepted-prefix length
+ *   K^_r = sum_{k=1..L} prod_{i=1..k} alpha_i,   L = min(gamma, R_r),
+ * over the steps i = 1..L in the draft's time order (slot o_i, the slot labelled i), with
+ *   SIMSD_KHAT_MARGIN:  alpha_i = 1 if m_i >= tau_margin else 0,
+ *   SIMSD_KHAT_ENTROPY: alpha_i = exp(-beta * H~_i),
+ * where p = softmax(draft_logits[r][o_i] / T) (T > 0), m_i = p_(1) - p_(2) (its two
+ * largest probabilities; p_(2) = 0 when V = 1) and H~_i = H(p) / ln V (0 when V = 1).
+ *   draft_logits  [batch, B, V] of logit_dtype (fp32, or bf16 widened exactly), indexed by
+ *                 block slot; -inf entries hold no probability (every verified row needs a
+ *                 finite entry).
+ *   labels        uint8 [batch, 2B] from simsd_build_layout.
+ *   temperature   T > 0; tau_margin any float; beta >= 0.
+ *   khat          float [batch] out.
+ *   alpha         float [batch, gamma] out, or NULL: alpha_i of step i + 1 (0 past L).
+ * Numerics: fp32 with one pass over each row (top two values, sum of e^(z - m) and of
+ * e^(z - m)(z - m)); alpha_i of the entropy estimator is within 2e-5 of its exact value
+ * and K^ within L(L + 1)/2 * 2e-5; margin decisions are exact unless m_i is within a
+ * relative 1e-5 of tau_margin.
+ * Data errors: labels not a permutation (SIMSD_DEVERR_TAU) -> K^ = -1, alpha row 0.
+ * Workspace: simsd_expected_prefix_workspace(batch, B, gamma, V) bytes (on the current
+ * device), 256-byte aligned, no initialisation needed.
+ * --------------------------------------------------------------------------------- */
+size_t simsd_expected_prefix_workspace(int batch, int B, int gamma, int V);
+
+simsd_status simsd_expected_prefix(const void* draft_logits, simsd_dtype logit_dtype,
+                                   const uint8_t* labels, int batch, int B, int gamma, int V,
+                                   float temperature, simsd_khat_mode mode, float tau_margin,
+                                   float beta, float* khat, float* alpha, void* workspace,
+                                   size_t workspace_bytes, uint32_t* dev_err,
+                                   simsd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * simsd_accept_noalloc -- the same operation as simsd_accept, for callers that cannot

@@ -33,12 +33,12 @@ def _pkg():
     return pkg
 
 
-def _step(w, inputs, meta, with_lse=True):
+def _step(w, inputs, meta, with_lse=True, **kw):
     pkg = _pkg()
     st = pkg.VerifyStep(inputs, gamma=w.gamma, rope_theta=w.rope_theta,
                         temperature=w.temperature, cache_layout=meta["cache_layout"],
                         with_lse=with_lse, philox_seed=meta["philox_seed"],
-                        philox_offset=meta["philox_offset"])
+                        philox_offset=meta["philox_offset"], **kw)
     st.run()
     torch.cuda.synchronize()
     return st
@@ -667,3 +667,127 @@ def test_accept_monte_carlo_commits_follow_target():
     got = {"accepted_len": a, "n_commit": nc.cpu().numpy(), "out_tokens": ot,
            "out_pos": op.cpu().numpy()}
     H.check_accept(res, got, reqs)
+
+
+# ------------------------------------------------------------------ routing estimator (K^)
+ALPHA_TOL = 2e-5   # fp32 sums of e^(z - m) over a row: alpha of the entropy estimator
+
+
+def _khat_gpu(dl, labels, gamma, T, mode, tau_margin, beta, with_alpha=True):
+    pkg = _pkg()
+    b, B, V = dl.shape
+    khat = torch.full((b,), -7.0, device="cuda")
+    al = torch.full((b, gamma), -7.0, device="cuda") if with_alpha else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkg.simsd_expected_prefix_workspace(b, B, gamma, V), dtype=torch.uint8,
+                     device="cuda")
+    pkg.simsd_expected_prefix(dl, labels, gamma, T, mode, tau_margin, beta, khat, al, ws, err)
+    torch.cuda.synchronize()
+    return khat.cpu().numpy(), (al.cpu().numpy() if with_alpha else None), int(err.item())
+
+
+def _check_khat(res, khat, alpha, reqs, mode, tau_margin):
+    """Entropy estimator: alpha within ALPHA_TOL and K^ within L(L+1)/2 ALPHA_TOL (each
+    prefix product moves by at most the sum of its factors' errors). Margin estimator: the
+    decisions and K^ exact, except for a request with a margin within a relative 1e-5 of
+    tau_margin (counted and returned)."""
+    near = 0
+    for r in reqs:
+        L = int(np.sum(~np.isnan(res["margin"][r])))
+        if res["khat"][r] == -1:
+            assert khat[r] == -1 and (alpha is None or (alpha[r] == 0).all())
+            continue
+        if alpha is not None:
+            assert (alpha[r, L:] == 0).all()
+        if mode == oracle.KHAT_MARGIN:
+            close = np.abs(res["margin"][r, :L] - tau_margin) <= 1e-5 * abs(tau_margin) + 1e-12
+            if close.any():
+                near += 1
+                continue
+            if alpha is not None:
+                assert np.array_equal(alpha[r, :L], res["alpha"][r, :L]), r
+            assert khat[r] == res["khat"][r], (r, khat[r], res["khat"][r])
+        else:
+            if alpha is not None:
+                assert np.abs(alpha[r, :L] - res["alpha"][r, :L]).max(initial=0) <= ALPHA_TOL, r
+            assert abs(khat[r] - res["khat"][r]) <= L * (L + 1) / 2 * ALPHA_TOL, (r, khat[r], res["khat"][r])
+    return near
+
+
+def _spread_logits(b, B, V, seed):
+    """Rows from flat to peaked (logit scale 0.3 .. 40), so margins and entropies cover
+    (0, 1)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    scale = torch.exp(torch.linspace(math.log(0.3), math.log(40.0), b * B))
+    scale = scale[torch.randperm(b * B, generator=g)].reshape(b, B, 1)
+    return torch.randn(b, B, V, generator=g) * scale
+
+
+@pytest.mark.parametrize("ldt", ["fp32", "bf16"])
+@pytest.mark.parametrize("mode,T", [(0, 1.0), (0, 0.7), (1, 1.0), (1, 1.3)])
+def test_expected_prefix_spread_rows(mode, T, ldt):
+    """Margin and entropy estimators on rows from flat to peaked, first and later rounds
+    (committed slots skipped, R < gamma for some requests), against the oracle."""
+    b, B, gamma, V = 40, 8, 6, 32000
+    dl = _spread_logits(b, B, V, 71)
+    if ldt == "bf16":
+        dl = dl.to(torch.bfloat16)
+    labels = torch.from_numpy(oracle.build_layout(
+        _later_round_taus(np.random.default_rng(72), b, B), np.full(b, 100))[1])
+    tau_margin, beta = 0.3, 2.0
+    res = oracle.expected_prefix(H.to_np(dl), labels.numpy(), gamma, T, mode, tau_margin, beta)
+    khat, alpha, err = _khat_gpu(dl.cuda(), labels.cuda(), gamma, T, mode, tau_margin, beta)
+    assert err == 0
+    near = _check_khat(res, khat, alpha, range(b), mode, tau_margin)
+    assert near <= 2
+    assert len(set(np.round(res["khat"], 6))) > (5 if mode == oracle.KHAT_ENTROPY else 3)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "gqa8b_bf16", "large_block_bf16", "ragged_bf16"])
+def test_expected_prefix_in_the_step(name):
+    """The estimator inside VerifyStep (between the layout and the attention) on the
+    workloads' draft logits, entropy estimator at the workload's temperature; the ragged
+    workload is checked on a sample of its requests."""
+    w = W[name]
+    inputs, meta = H.make_case(w, seed=81)
+    st = _step(w, inputs, meta, with_lse=False, khat_mode=oracle.KHAT_ENTROPY, beta=1.5,
+               khat_temperature=w.temperature)
+    reqs = ACC_SAMPLE.get(name) or list(range(w.batch))
+    idx = torch.tensor(reqs, device="cuda")
+    res = oracle.expected_prefix(H.to_np(inputs["draft_logits"][idx]), H.to_np(st.labels[idx]),
+                                 w.gamma, w.temperature, oracle.KHAT_ENTROPY, beta=1.5)
+    khat = st.khat.cpu().numpy()[reqs]
+    alpha = st.alpha.cpu().numpy()[reqs]
+    _check_khat(res, khat, alpha, range(len(reqs)), oracle.KHAT_ENTROPY, 0.0)
+    assert int(st.dev_err.item()) == 0
+
+
+@pytest.mark.parametrize("ldt", ["fp32", "bf16"])
+def test_expected_prefix_edges(ldt):
+    """Odd V (unvectorised loads), masked entries, a request with invalid labels (K^ = -1,
+    tau error bit), one with every slot committed (K^ = 0), a peaked row per request, no
+    alpha output; and V = 1 (margin 1, entropy 0: K^ = L)."""
+    b, B, gamma, V = 6, 4, 4, 1001
+    dl = _spread_logits(b, B, V, 91)
+    dl[1, :, : V // 2] = -math.inf
+    dl[2, :, 5] = 40.0
+    if ldt == "bf16":
+        dl = dl.to(torch.bfloat16)
+    taus = np.array([[2, 1, 4, 3], [1, 2, 3, 4], [0, 0, 0, 0], [3, 0, 1, 2], [1, 1, 2, 3],
+                     [4, 3, 2, 1]])
+    pos, lab, lerr = oracle.build_layout(taus, np.full(b, 10))
+    assert lerr == oracle.ERR_TAU
+    for mode in (oracle.KHAT_MARGIN, oracle.KHAT_ENTROPY):
+        res = oracle.expected_prefix(H.to_np(dl), lab, gamma, 0.9, mode, 0.05, 0.8)
+        assert res["khat"][2] == 0 and res["khat"][4] == -1
+        for with_alpha in (True, False):
+            khat, alpha, err = _khat_gpu(dl.cuda(), torch.from_numpy(lab).cuda(), gamma, 0.9,
+                                         mode, 0.05, 0.8, with_alpha)
+            assert err == oracle.ERR_TAU
+            _check_khat(res, khat, alpha, range(b), mode, 0.05)
+    one = torch.randn(3, B, 1)
+    if ldt == "bf16":
+        one = one.to(torch.bfloat16)
+    khat, alpha, err = _khat_gpu(one.cuda(), torch.from_numpy(lab[:2]).cuda().repeat(2, 1)[:3],
+                                 gamma, 1.0, oracle.KHAT_ENTROPY, 0.0, 3.0)
+    assert err == 0 and khat.tolist() == [4.0, 4.0, 4.0] and (alpha == 1).all()

@@ -85,6 +85,17 @@ def test_host_argument_errors_return_status(lib):
     assert lib.simsd_accept_coupled_ex(*cx) == 1
     cx[1], cx[5] = 0, 2
     assert lib.simsd_accept_coupled_ex(*cx) == 1  # null pointers
+    # the expected accepted-prefix estimator: T > 0, beta >= 0, a known mode and type
+    kx = [None, 0, None, 0, 4, 4, 100, 1.0, 1, 0.5, 1.0, None, None, None, 0, None, None]
+    assert lib.simsd_expected_prefix(*kx) == 0    # batch 0: nothing to do
+    for i, bad in ((7, 0.0), (7, -1.0), (10, -0.5), (8, 2), (1, 3), (9, float("nan"))):
+        k2 = list(kx)
+        k2[i] = bad
+        assert lib.simsd_expected_prefix(*k2) == 1, (i, bad)
+    kx[3] = 2
+    assert lib.simsd_expected_prefix(*kx) == 1    # null pointers
+    assert lib.simsd_expected_prefix_workspace(2, 4, 4, 100) >= 256
+    assert lib.simsd_expected_prefix_workspace(2, 4, 5, 100) == 0
 
 
 def test_attention_parameter_checks(lib):

@@ -172,12 +172,14 @@ def make_accept_inputs(w: Workload, seed: Optional[int] = None, device="cpu",
             "philox_seed": 0x5EED0000 + int(seed), "philox_offset": 0}
 
 
-def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor, target_only: bool = False) -> dict:
+def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor, target_only: bool = False,
+                      with_khat: bool = False) -> dict:
     """Minimum HBM bytes of one verification step: each input read once, each
     output written once (per request: the prompt K/V, the 2B-row Q/K/V/O, and the
     target+draft logit rows of the gamma verified slots; the target rows only at
     temperature 0, where greedy verification reads no draft logits, or with `target_only`
-    for coupled-noise verification)."""
+    for coupled-noise verification). `khat_bytes` is the expected-prefix estimate's read of
+    the gamma draft rows, added to the total with `with_khat`."""
     esz = 4 if w.dtype == "fp32" else 2
     P_sum = int(prompt_len.to(torch.int64).sum())
     b, B, D = w.batch, w.B, w.D
@@ -188,6 +190,7 @@ def algorithmic_bytes(w: Workload, prompt_len: torch.Tensor, target_only: bool =
     flops = 0
     for P in prompt_len.tolist():
         flops += 4 * 2 * B * w.Hq * (P + B) * D
-    return {"attn_bytes": kv_prompt + resp, "accept_bytes": accept,
-            "total_bytes": kv_prompt + resp + accept, "attn_flops": flops,
-            "tokens": b * w.gamma}
+    khat = b * w.gamma * w.V * lsz
+    return {"attn_bytes": kv_prompt + resp, "accept_bytes": accept, "khat_bytes": khat,
+            "total_bytes": kv_prompt + resp + accept + (khat if with_khat else 0),
+            "attn_flops": flops, "tokens": b * w.gamma}
