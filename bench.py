@@ -56,6 +56,8 @@ def _args():
     ap.add_argument("--khat", choices=["margin", "entropy"], default=None,
                     help="also estimate the expected accepted-prefix length (simsd_expected_prefix) "
                          "from the draft logits in every step")
+    ap.add_argument("--physical-positions", action="store_true",
+                    help="ablation layout: mask slots at their own sequence index (no aligned RoPE)")
     ap.add_argument("--logit-dtype", choices=["fp32", "bf16"], default=None,
                     help="element type of the target / draft logits (default: the workload's, fp32)")
     return ap.parse_args()
@@ -210,6 +212,8 @@ def _config(w, args, launch):
         "greedy" if w.temperature == 0 else "rejection sampling")
     if getattr(args, "khat", None):
         cfg["expected_prefix"] = args.khat
+    if getattr(args, "physical_positions", False):
+        cfg["rope_positions"] = "physical (ablation: no aligned RoPE)"
     return cfg
 
 
@@ -463,7 +467,8 @@ def run_ours(args):
     steps = [pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
                             temperature=w.temperature, cache_layout=args.cache_layout,
                             philox_seed=s["_seed"], coupled=args.coupled, khat_mode=khat_mode,
-                            khat_temperature=w.temperature if w.temperature > 0 else 1.0)
+                            khat_temperature=w.temperature if w.temperature > 0 else 1.0,
+                            aligned_rope=not args.physical_positions)
              for s in sets]
     algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled,
                                         with_khat=khat_mode is not None) for s in sets]

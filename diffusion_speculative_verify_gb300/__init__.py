@@ -11,7 +11,7 @@ import torch
 
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
                        DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, KHAT_ENTROPY, KHAT_MARGIN,
-                       LIB_PATH, AttnParams,
+                       LAYOUT_PHYSICAL_POSITIONS, LIB_PATH, AttnParams,
                        SimsdError, load_library, make_attn_params, simsd_accept, simsd_accept_coupled,
                        simsd_accept_coupled_ex, simsd_accept_ex, simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,
                        simsd_accept_workspace, simsd_build_layout, simsd_expected_prefix,
@@ -42,7 +42,7 @@ class VerifyStep:
                  cache_layout: str = "NHD", softmax_scale: float = 0.0, with_lse: bool = True,
                  philox_seed: int = 0, philox_offset: int = 0, coupled: bool = False,
                  khat_mode=None, tau_margin: float = 0.5, beta: float = 1.0,
-                 khat_temperature: float = 1.0):
+                 khat_temperature: float = 1.0, aligned_rope: bool = True):
         load_library()
         dev = inputs["q"].device
         b, twoB, Hq, D = inputs["q"].shape
@@ -76,6 +76,8 @@ class VerifyStep:
             raise SimsdError(1, "simsd_accept_workspace")
         self.ws_accept = torch.empty(ws_acc, dtype=torch.uint8, device=dev)
         self.khat_mode = khat_mode
+        # aligned_rope=False: the mask slots keep their physical positions (ablation)
+        self.layout_flags = 0 if aligned_rope else LAYOUT_PHYSICAL_POSITIONS
         if khat_mode is not None:
             self.khat_args = (khat_temperature, int(khat_mode), tau_margin, beta)
             self.khat = torch.empty(b, dtype=torch.float32, device=dev)
@@ -87,7 +89,7 @@ class VerifyStep:
 
     def layout(self, stream=None):
         simsd_build_layout(self.inputs["tau"], self.inputs["prompt_len"], self.pos_ids,
-                           self.labels, self.dev_err, stream)
+                           self.labels, self.dev_err, stream, self.layout_flags)
 
     def expected_prefix(self, stream=None):
         simsd_expected_prefix(self.inputs["draft_logits"], self.labels, self.gamma,

@@ -23,7 +23,10 @@ DTYPE_FP32, DTYPE_BF16 = 0, 1
 KHAT_MARGIN, KHAT_ENTROPY = 0, 1
 CACHE_NHD, CACHE_HND = 0, 1
 
+LAYOUT_PHYSICAL_POSITIONS = 1
+
 EXPORTED = ["simsd_status_str", "simsd_version", "simsd_last_cuda_error", "simsd_build_layout",
+            "simsd_build_layout_ex",
             "simsd_verify_attention_workspace", "simsd_verify_attention",
             "simsd_accept_workspace", "simsd_accept", "simsd_accept_coupled",
             "simsd_accept_ex", "simsd_accept_coupled_ex",
@@ -74,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.simsd_last_cuda_error.restype = ctypes.c_char_p
     lib.simsd_build_layout.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
     lib.simsd_build_layout.restype = i32
+    lib.simsd_build_layout_ex.argtypes = [vp, vp, i32, i32, ctypes.c_uint32, vp, vp, vp, vp]
+    lib.simsd_build_layout_ex.restype = i32
     lib.simsd_verify_attention_workspace.argtypes = [ctypes.POINTER(AttnParams)]
     lib.simsd_verify_attention_workspace.restype = sz
     lib.simsd_verify_attention.argtypes = [ctypes.POINTER(AttnParams), vp, sz, vp]
@@ -143,14 +148,21 @@ def simsd_last_cuda_error() -> str:
     return load_library().simsd_last_cuda_error().decode()
 
 
-def simsd_build_layout(tau, prompt_len, pos_ids, labels, dev_err, stream=None):
-    """tau int32 [b, B], prompt_len int32 [b] -> pos_ids int32 [b, 2B], labels uint8 [b, 2B]."""
+def simsd_build_layout(tau, prompt_len, pos_ids, labels, dev_err, stream=None, flags=0):
+    """tau int32 [b, B], prompt_len int32 [b] -> pos_ids int32 [b, 2B], labels uint8 [b, 2B].
+    Nonzero `flags` (LAYOUT_PHYSICAL_POSITIONS) calls simsd_build_layout_ex."""
     _check(tau, "tau", torch.int32)
     _check(prompt_len, "prompt_len", torch.int32)
     _check(pos_ids, "pos_ids", torch.int32)
     _check(labels, "labels", torch.uint8)
     _check(dev_err, "dev_err", torch.int32)
     b, B = tau.shape
+    if flags:
+        st = load_library().simsd_build_layout_ex(_ptr(tau), _ptr(prompt_len), b, B, int(flags),
+                                                  _ptr(pos_ids), _ptr(labels), _ptr(dev_err),
+                                                  _stream(stream))
+        _raise(st, "simsd_build_layout_ex")
+        return
     st = load_library().simsd_build_layout(_ptr(tau), _ptr(prompt_len), b, B, _ptr(pos_ids),
                                            _ptr(labels), _ptr(dev_err), _stream(stream))
     _raise(st, "simsd_build_layout")

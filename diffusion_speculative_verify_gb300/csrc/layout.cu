@@ -7,6 +7,8 @@
 // round of the same block the slots committed earlier carry tau = 0, like the prompt
 // (item 2), and the R remaining positions (item 4) a permutation of 1..R.
 // No mask is materialised: labels are enough to evaluate A_ij on the fly.
+// With SIMSD_LAYOUT_PHYSICAL_POSITIONS the mask slots take their own sequence index instead
+// (the "Without Aligned RoPE" ablation of the SimSD notes' table), a negative control.
 #include "common.cuh"
 
 namespace simsd {
@@ -14,7 +16,8 @@ namespace simsd {
 // One warp per request; lane k handles slot k (B <= 32).
 __global__ void __launch_bounds__(128) build_layout_kernel(
     const int32_t* __restrict__ tau, const int32_t* __restrict__ prompt_len, int batch, int B,
-    int32_t* __restrict__ pos_ids, uint8_t* __restrict__ labels, uint32_t* __restrict__ dev_err) {
+    int mask_pos_offset, int32_t* __restrict__ pos_ids, uint8_t* __restrict__ labels,
+    uint32_t* __restrict__ dev_err) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= batch) return;
@@ -44,22 +47,31 @@ __global__ void __launch_bounds__(128) build_layout_kernel(
     return;
   }
   pos_ids[row + lane] = P + lane;      // D_k: next response position
-  pos_ids[row + B + lane] = P + lane;  // D~_k: copy of D_k's id
+  pos_ids[row + B + lane] = P + mask_pos_offset + lane;  // D~_k: D_k's id (offset 0) or its own
   labels[row + lane] = (uint8_t)t;
   labels[row + B + lane] = (uint8_t)(kSegMask | t);
 }
 
 }  // namespace simsd
 
-SIMSD_API simsd_status simsd_build_layout(const int32_t* tau, const int32_t* prompt_len,
-                                          int batch, int B, int32_t* pos_ids, uint8_t* labels,
-                                          uint32_t* dev_err, simsd_stream_t stream) {
+SIMSD_API simsd_status simsd_build_layout_ex(const int32_t* tau, const int32_t* prompt_len,
+                                             int batch, int B, uint32_t flags, int32_t* pos_ids,
+                                             uint8_t* labels, uint32_t* dev_err,
+                                             simsd_stream_t stream) {
   if (batch < 0 || B < 1 || B > simsd::kMaxB) return SIMSD_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)SIMSD_LAYOUT_PHYSICAL_POSITIONS) return SIMSD_ERR_INVALID_ARG;
   if (batch == 0) return SIMSD_OK;
   if (!tau || !prompt_len || !pos_ids || !labels || !dev_err) return SIMSD_ERR_INVALID_ARG;
   const int warps = 4;
   const int grid = (batch + warps - 1) / warps;
+  const int offset = (flags & SIMSD_LAYOUT_PHYSICAL_POSITIONS) ? B : 0;
   simsd::build_layout_kernel<<<grid, warps * 32, 0, (cudaStream_t)stream>>>(
-      tau, prompt_len, batch, B, pos_ids, labels, dev_err);
+      tau, prompt_len, batch, B, offset, pos_ids, labels, dev_err);
   return simsd::last_launch_status();
+}
+
+SIMSD_API simsd_status simsd_build_layout(const int32_t* tau, const int32_t* prompt_len,
+                                          int batch, int B, int32_t* pos_ids, uint8_t* labels,
+                                          uint32_t* dev_err, simsd_stream_t stream) {
+  return simsd_build_layout_ex(tau, prompt_len, batch, B, 0u, pos_ids, labels, dev_err, stream);
 }

@@ -124,6 +124,19 @@ simsd_status simsd_build_layout(const int32_t* tau, const int32_t* prompt_len, i
                                 int B, int32_t* pos_ids, uint8_t* labels, uint32_t* dev_err,
                                 simsd_stream_t stream);
 
+/* simsd_build_layout_ex -- simsd_build_layout with layout flags (0: exactly
+ * simsd_build_layout).
+ *   SIMSD_LAYOUT_PHYSICAL_POSITIONS  pos_ids[r][B + k] = P_r + B + k: the mask slots take
+ *     their own index in the sequence instead of D_k's id. This is the "Without Aligned
+ *     RoPE" ablation of the SimSD notes' table ([SimSD-3]), kept as a negative control:
+ *     the prediction rows then no longer equal the explicit denoising states.
+ * Unknown flag bits return SIMSD_ERR_INVALID_ARG. */
+#define SIMSD_LAYOUT_PHYSICAL_POSITIONS 1u
+
+simsd_status simsd_build_layout_ex(const int32_t* tau, const int32_t* prompt_len, int batch,
+                                   int B, uint32_t flags, int32_t* pos_ids, uint8_t* labels,
+                                   uint32_t* dev_err, simsd_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * simsd_verify_attention  [SimSD-2], [SimSD-3], [SimSD-P] sections 2-4.
  *

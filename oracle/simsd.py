@@ -57,11 +57,13 @@ KHAT_ENTROPY = 1     # alpha_i = exp(-beta * H~_i)
 
 
 # ----------------------------------------------------------------------------- layout
-def build_layout(tau, prompt_len):
+def build_layout(tau, prompt_len, aligned_rope=True):
     """Paired layout [prompt | D_1..D_B | D~_1..D~_B].
 
     Position ids: prompt token j -> j (implicit); D_k -> P + k; D~_k copies D_k's id
-    (0-based k). Labels: one byte per response slot, (segment << 7) | tau, segment 0
+    (0-based k). With aligned_rope=False, the ablation of the SimSD notes' table ("Without
+    Aligned RoPE", positions increasing physically), D~_k takes its own index in the
+    sequence, P + B + k. Labels: one byte per response slot, (segment << 7) | tau, segment 0
     for D and 1 for D~. tau = 0 marks a slot committed in an earlier round of the same
     block (its token is known, like the prompt's); the other slots' labels must be a
     permutation of 1..R, R = their count (R = B in a block's first round). A request
@@ -89,7 +91,7 @@ def build_layout(tau, prompt_len):
                 labels[r, k] = labels[r, B + k] = INVALID_LABEL
                 continue
             pos[r, k] = P + k            # data slot D_k: next response position
-            pos[r, B + k] = P + k         # mask slot D~_k reuses the id of D_k
+            pos[r, B + k] = P + k if aligned_rope else P + B + k   # D~_k: D_k's id, or its own
             labels[r, k] = (SEG_DATA << 7) | int(tau[r, k])
             labels[r, B + k] = (SEG_MASK << 7) | int(tau[r, k])
     return pos, labels, err

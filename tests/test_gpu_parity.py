@@ -61,6 +61,51 @@ def test_layout_bit_exact(name):
     assert int(err.item()) == re_ == 0
 
 
+@pytest.mark.parametrize("name", ["tiny_fp32", "ragged_bf16"])
+def test_layout_physical_positions_bit_exact(name):
+    """The ablation layout (mask slots at their own sequence index), later rounds and
+    invalid requests included."""
+    w = W[name]
+    lay = workloads.make_layout_inputs(w)
+    tau = _later_round_taus(np.random.default_rng(3), w.batch, w.B, invalid_every=7)
+    plen = lay["prompt_len"].numpy().copy()
+    plen[5 % w.batch] = -1
+    b, B = tau.shape
+    pos = torch.empty(b, 2 * B, dtype=torch.int32, device="cuda")
+    lab = torch.empty(b, 2 * B, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _pkg().simsd_build_layout(torch.from_numpy(tau).to(torch.int32).cuda(),
+                              torch.from_numpy(plen).cuda(), pos, lab, err, flags=1)
+    rp, rl, re_ = oracle.build_layout(tau, plen, aligned_rope=False)
+    assert np.array_equal(pos.cpu().numpy(), rp)
+    assert np.array_equal(lab.cpu().numpy(), rl)
+    assert int(err.item()) == re_ != 0
+
+
+@pytest.mark.parametrize("case", ["fp32", "bf16", "bf16_cluster"])
+def test_attention_physical_positions_negative_control(case):
+    """Attention on the ablation layout against the oracle on the same positions (within
+    the usual tolerance), and the negative control: the prediction rows move away from the
+    aligned layout's by far more than that tolerance."""
+    if case == "fp32":
+        w = W["tiny_fp32"].with_(batch=3, B=6, gamma=6)
+        plen = [32, 5, 70]
+    else:
+        w = MEDIUM.with_(B=32, gamma=32, Hq=6, Hkv=2) if case == "bf16_cluster" else MEDIUM
+        plen = [0, 61, 128, 1000 + 37]
+    inputs, meta = H.make_case(w, seed=13, prompt_len=plen)
+    aligned = _step(w, inputs, meta)
+    base = H.to_np(aligned.out).copy()
+    st = _step(w, inputs, meta, aligned_rope=False)
+    assert int(st.dev_err.item()) == 0
+    P = np.array(plen)[:, None]
+    assert np.array_equal(st.pos_ids.cpu().numpy(), P + np.arange(2 * w.B)[None])
+    _attention_parity(w, inputs, meta, st)
+    got = H.to_np(st.out)
+    d = got[:, w.B:] - base[:, w.B:]
+    assert np.linalg.norm(d) / np.linalg.norm(base[:, w.B:]) > 0.1   # 0.37-0.53 in the oracle
+
+
 def test_layout_invalid_requests_and_block_32():
     B = 32
     rng = np.random.default_rng(0)

@@ -60,6 +60,9 @@ def test_host_argument_errors_return_status(lib):
     assert lib.simsd_build_layout(None, None, 4, 33, None, None, None, None) == 1
     assert lib.simsd_build_layout(None, None, 4, 4, None, None, None, None) == 1
     assert lib.simsd_build_layout(None, None, 0, 4, None, None, None, None) == 0
+    assert lib.simsd_build_layout_ex(None, None, 0, 4, 1, None, None, None, None) == 0
+    assert lib.simsd_build_layout_ex(None, None, 0, 4, 2, None, None, None, None) == 1
+    assert lib.simsd_build_layout_ex(None, None, 4, 4, 1, None, None, None, None) == 1
     # temperature 0 (greedy) is accepted, a negative one is not; gamma > B is invalid
     args = [None] * 4 + [2, 4, 4, 100, 0.0, 0, 0] + [None] * 4 + [None, 0, None, None]
     assert lib.simsd_accept(*args) == 1          # null pointers

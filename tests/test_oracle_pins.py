@@ -358,12 +358,18 @@ def test_attention_invariant_to_a_common_position_shift():
 
 
 def test_unaligned_positions_change_prediction_rows():
+    """The ablation layout (SimSD notes' table, "Without Aligned RoPE"): the position ids are
+    the physical indices P .. P + 2B - 1 of the response slots, and the prediction rows no
+    longer match the explicit-state view that the aligned layout reproduces."""
     rng = np.random.default_rng(7)
     B, Hq, Hkv, D, P, theta = 4, 2, 1, 16, 6, 1e4
     case = _random_case(rng, 1, B, Hq, Hkv, D, [P])
     base, _ = _run(case, theta)
+    pos, labels, err = oracle.build_layout(case["tau"], [P], aligned_rope=False)
+    assert err == 0 and np.array_equal(labels, case["labels"])
+    assert pos.tolist() == [list(range(P, P + 2 * B))]
     c = dict(case)
-    c["pos_ids"] = (P + np.arange(2 * B))[None].astype(np.int32)  # physical positions
+    c["pos_ids"] = pos
     out, _ = _run(c, theta)
     assert np.abs(out[0, B:] - base[0, B:]).max() > 1e-3
 
