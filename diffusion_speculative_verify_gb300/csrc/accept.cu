@@ -91,13 +91,6 @@ AcceptPlan make_plan(int batch, int gamma, int V, int models = 2) {
   return p;
 }
 
-__device__ __forceinline__ float4 ld_stream4(const float* p) {
-  float4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
-  return v;
-}
 
 
 // Merge two (max, sum exp(x - max)) pairs.
@@ -295,42 +288,37 @@ __device__ __forceinline__ void race_range(const LT* __restrict__ trow, const LT
                                            float inv_sd, bool on_p, uint32_t r, uint32_t off_lo,
                                            uint32_t off_hi, uint32_t key0, uint32_t key1,
                                            unsigned long long& best) {
+  using IO = LogitIO<LT>;
   const int g0 = c0 / 4, g1 = c0 < c1 ? (c1 + 3) / 4 : g0;
   for (int gb = g0 + t; gb < g1; gb += 4 * nthreads) {
-    float tv[4][4], dv[4][4];
+    // entries as loaded (aligned rows: one load per row and group; unaligned rows: one per
+    // entry), widened only where they are used, after every load of the batch is issued
+    typename IO::Raw4 rt[4], rd[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int g = gb + u * nthreads;
       if (g < g1) {
-        if (vec_ok) {
-          const float4 t4 = LogitIO<LT>::ldg4(trow, g);
-          tv[u][0] = t4.x; tv[u][1] = t4.y; tv[u][2] = t4.z; tv[u][3] = t4.w;
-          if (!on_p) {
-            const float4 d4 = LogitIO<LT>::ldg4(drow, g);
-            dv[u][0] = d4.x; dv[u][1] = d4.y; dv[u][2] = d4.z; dv[u][3] = d4.w;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int v = 4 * g + j;
-            tv[u][j] = v < c1 ? LogitIO<LT>::ld1(trow + v) : 0.f;
-            dv[u][j] = (v < c1 && !on_p) ? LogitIO<LT>::ld1(drow + v) : 0.f;
-          }
-        }
+        rt[u] = vec_ok ? IO::ldraw4(trow, g) : IO::ldraw4_each(trow, g, c1);
+        if (!on_p) rd[u] = vec_ok ? IO::ldraw4(drow, g) : IO::ldraw4_each(drow, g, c1);
       }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int g = gb + u * nthreads;
-      if (g < g1)
-        race_group(g, c1, tv[u], dv[u], T, unit_T, mt, inv_st, md, inv_sd, on_p, r, off_lo,
-                   off_hi, key0, key1, best);
+      if (g < g1) {
+        const float4 a = IO::widen4(rt[u]);
+        const float4 b = on_p ? a : IO::widen4(rd[u]);
+        const float tv[4] = {a.x, a.y, a.z, a.w}, dv[4] = {b.x, b.y, b.z, b.w};
+        race_group(g, c1, tv, dv, T, unit_T, mt, inv_st, md, inv_sd, on_p, r, off_lo, off_hi,
+                   key0, key1, best);
+      }
     }
   }
 }
 
+// Two CTAs per SM (the grid is one wave of them).
 template <typename LT>
-__global__ void __launch_bounds__(kFinishThreads) accept_finish_kernel(
+__global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     const LT* __restrict__ target, const LT* __restrict__ draft,
     const int32_t* __restrict__ tokens, const uint8_t* __restrict__ labels, int batch, int B,
     int gamma, int V, float T, uint32_t key0, uint32_t key1, uint32_t off_lo, uint32_t off_hi,

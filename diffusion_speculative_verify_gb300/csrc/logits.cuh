@@ -45,6 +45,17 @@ struct LogitIO<float> {
   static __device__ __forceinline__ float4 ldg4(const float* row, int i) {
     return __ldg(reinterpret_cast<const float4*>(row) + i);
   }
+  // entries 4i .. 4i + 3 as loaded, widened only where they are used (so that a batch of
+  // loads is issued before any of them is consumed)
+  using Raw4 = float4;
+  static __device__ __forceinline__ Raw4 ldraw4(const float* row, int i) { return ldg4(row, i); }
+  static __device__ __forceinline__ float4 widen4(const Raw4& w) { return w; }
+  // the same four entries from an unaligned row, one load each (0 at and past `end`)
+  static __device__ __forceinline__ Raw4 ldraw4_each(const float* row, int i, int end) {
+    const int v = 4 * i;
+    return make_float4(v < end ? __ldg(row + v) : 0.f, v + 1 < end ? __ldg(row + v + 1) : 0.f,
+                       v + 2 < end ? __ldg(row + v + 2) : 0.f, v + 3 < end ? __ldg(row + v + 3) : 0.f);
+  }
   static __device__ __forceinline__ float ld1(const float* p) { return __ldg(p); }
 };
 template <>
@@ -72,8 +83,22 @@ struct LogitIO<__nv_bfloat16> {
   }
   static __device__ __forceinline__ float max_value(MaxAcc a) { return fmaxf(lo(a), hi(a)); }
   static __device__ __forceinline__ float4 ldg4(const __nv_bfloat16* row, int i) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(row) + i);
+    return widen4(ldraw4(row, i));
+  }
+  using Raw4 = uint2;
+  static __device__ __forceinline__ Raw4 ldraw4(const __nv_bfloat16* row, int i) {
+    return __ldg(reinterpret_cast<const uint2*>(row) + i);
+  }
+  static __device__ __forceinline__ float4 widen4(const Raw4& w) {
     return make_float4(lo(w.x), hi(w.x), lo(w.y), hi(w.y));
+  }
+  static __device__ __forceinline__ Raw4 ldraw4_each(const __nv_bfloat16* row, int i, int end) {
+    const unsigned short* p = reinterpret_cast<const unsigned short*>(row);
+    const int v = 4 * i;
+    uint32_t e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) e[j] = v + j < end ? (uint32_t)__ldg(p + v + j) : 0u;
+    return make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
   }
   static __device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
     return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p)) << 16);
