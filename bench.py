@@ -169,7 +169,7 @@ def run_reference(args):
         return 0
     w = _workload(args)
     cores = len(os.sched_getaffinity(0))
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = max(0.05, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
     vals = []
     t0 = time.perf_counter()
     with _oracle_pool(cores) as pool:
@@ -188,7 +188,7 @@ def run_reference(args):
             "config": _config(w, args, "fp64 oracle on host cores"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": vals[0]["sample"] +
-                             f"; median over {args.steps} steps of {per_step:.1f} s each"},
+                             f"; median over {args.steps} steps of {per_step:.2f} s each"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": elapsed}
