@@ -403,11 +403,11 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _make_sets(w, args, device, n_sets, rank):
+def _make_sets(w, args, device, n_sets, rank, first=0):
     import torch
     import workloads
     sets = []
-    for i in range(n_sets):
+    for i in range(first, first + n_sets):
         seed = w.seed + 1000 * rank + i
         lay = workloads.make_layout_inputs(w, seed=seed)
         att = workloads.make_attention_inputs(w, lay["prompt_len"], seed=seed, device=device,
@@ -464,12 +464,15 @@ def run_ours(args):
     n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / max(1, alg["total_bytes"]))))
     sets = _make_sets(w, args, device, n_sets, rank)
     khat_mode = {None: None, "margin": pkg.KHAT_MARGIN, "entropy": pkg.KHAT_ENTROPY}[args.khat]
-    steps = [pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
-                            temperature=w.temperature, cache_layout=args.cache_layout,
-                            philox_seed=s["_seed"], coupled=args.coupled, khat_mode=khat_mode,
-                            khat_temperature=w.temperature if w.temperature > 0 else 1.0,
-                            aligned_rope=not args.physical_positions)
-             for s in sets]
+
+    def make_step(s):
+        return pkg.VerifyStep(s, gamma=w.gamma, rope_theta=w.rope_theta,
+                              temperature=w.temperature, cache_layout=args.cache_layout,
+                              philox_seed=s["_seed"], coupled=args.coupled, khat_mode=khat_mode,
+                              khat_temperature=w.temperature if w.temperature > 0 else 1.0,
+                              aligned_rope=not args.physical_positions)
+
+    steps = [make_step(s) for s in sets]
     algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled,
                                         with_khat=khat_mode is not None) for s in sets]
     stream = torch.cuda.Stream(device=device)
@@ -577,7 +580,11 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(w, sets[0], steps[0], args, stream, world, device)
+        e_sets, e_steps = sets, steps
+        if len(sets) < 2:  # a second device set, so that the end-to-end steps can overlap
+            extra = _make_sets(w, args, device, 1, rank, first=len(sets))
+            e_sets, e_steps = sets + extra, steps + [make_step(extra[0])]
+        e2e = _e2e(w, e_sets, e_steps, args, stream, world, device)
     clk = clocks.stop()
 
     # ---- CPU baseline (rank 0, N = 1)
@@ -609,47 +616,67 @@ def run_ours(args):
     return 0
 
 
-def _e2e(w, s, st, args, stream, world, device):
-    """Same metric through VerifyStep with host buffers: every step copies all inputs
-    from pinned host memory and reads the accept results back."""
+def _e2e(w, sets, steps, args, stream, world, device):
+    """Same metric through VerifyStep with host buffers: every step copies all of its inputs
+    from pinned host memory and reads the accept results back, both inside the timed
+    region. With two device input sets the steps are pipelined as a server would run them:
+    step k + 1's inputs go up on a copy stream while step k computes (a set is refilled only
+    after the step that used it has finished); with one set they run back to back."""
     import torch
     import torch.distributed as dist
     keys = ["tau", "prompt_len", "q", "k_resp", "v_resp", "k_cache", "v_cache", "cache_start",
             "target_logits", "draft_logits", "draft_tokens"]
-    host = {k: s[k].cpu().pin_memory() for k in keys}
-    outs = [st.accepted_len, st.n_commit, st.out_tokens, st.out_pos]
-    host_out = [o.cpu().pin_memory() for o in outs]
-    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    nbuf = 2 if len(sets) >= 2 else 1
+    host = [{k: sets[b][k].cpu().pin_memory() for k in keys} for b in range(nbuf)]
+    outs = [[st.accepted_len, st.n_commit, st.out_tokens, st.out_pos] for st in steps[:nbuf]]
+    host_out = [[o.cpu().pin_memory() for o in ob] for ob in outs]
+    nbytes = [sum(hb[k].numel() * hb[k].element_size() for k in keys) for hb in host]
     n = max(3, min(args.steps, 50))
+    copy_stream = torch.cuda.Stream(device=device) if nbuf == 2 else stream
+    copied = [torch.cuda.Event() for _ in range(nbuf)]
+    freed = [None] * nbuf
 
-    def one():
-        for k in keys:
-            s[k].copy_(host[k], non_blocking=True)
-        st.run(stream)
-        for o, h in zip(outs, host_out):
-            h.copy_(o, non_blocking=True)
+    def one(k):
+        b = k % nbuf
+        with torch.cuda.stream(copy_stream):
+            if freed[b] is not None:
+                copy_stream.wait_event(freed[b])
+            for key in keys:
+                sets[b][key].copy_(host[b][key], non_blocking=True)
+            copied[b].record(copy_stream)
+        with torch.cuda.stream(stream):
+            stream.wait_event(copied[b])
+            steps[b].run(stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            freed[b] = ev
+            for o, h in zip(outs[b], host_out[b]):
+                h.copy_(o, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
-        stream.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            one()
-        e1.record(stream)
+    for k in range(2):
+        one(k)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    for k in range(n):
+        one(k)
+    e1.record(stream)
     e1.synchronize()
     el = e0.elapsed_time(e1) / 1e3
     if world > 1:
         t = torch.tensor([el], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         el = float(t.item())
+    h2d = sum(nbytes[k % nbuf] for k in range(n)) // n   # per step, over the timed steps
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
     return {"value": world * w.batch * w.gamma * n / el, "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "pipeline": ("2 input sets, copies on a second stream overlapping the previous step"
+                         if nbuf == 2 else "serial"),
             "api": "VerifyStep.run (simsd_build_layout, simsd_verify_attention, simsd_accept)"}
 
 
