@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--workload", default="gqa8b_bf16")
     ap.add_argument("--cache-layout", choices=["NHD", "HND"], default="NHD")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="reference arm: oracle sampling time spread over the K + W steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -169,7 +171,7 @@ def run_reference(args):
         return 0
     w = _workload(args)
     cores = len(os.sched_getaffinity(0))
-    per_step = max(0.05, min(10.0, 90.0 / max(1, args.steps + args.warmup)))
+    per_step = max(0.05, min(10.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     vals = []
     t0 = time.perf_counter()
     with _oracle_pool(cores) as pool:
