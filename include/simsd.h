@@ -90,7 +90,11 @@ typedef enum { SIMSD_CACHE_NHD = 0, SIMSD_CACHE_HND = 1 } simsd_cache_layout;
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* simsd_status_str(simsd_status s);
 
-/* Library interface version (major * 10000 + minor * 100 + patch). */
+/* Library interface version (major * 10000 + minor * 100 + patch).
+ *   0.1.0  layout, verify attention, acceptance (+ workspace queries, allocation-free entry)
+ *   0.2.0  adds simsd_accept_coupled, simsd_accept_ex / simsd_accept_coupled_ex (bf16
+ *          logits), simsd_expected_prefix (+ workspace), simsd_build_layout_ex (flags);
+ *          every 0.1.0 call is unchanged */
 int simsd_version(void);
 
 /* Text of the CUDA runtime/driver error behind the most recent SIMSD_ERR_CUDA returned

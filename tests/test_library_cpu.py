@@ -51,7 +51,7 @@ def test_status_strings_and_version(lib):
     assert pkg.simsd_status_str(0) == "SIMSD_OK"
     assert pkg.simsd_status_str(3) == "SIMSD_ERR_WORKSPACE"
     assert pkg.simsd_status_str(99) == "SIMSD_ERR_UNKNOWN"
-    assert pkg.simsd_version() >= 100
+    assert pkg.simsd_version() == 200
 
 
 def test_host_argument_errors_return_status(lib):
