@@ -158,20 +158,15 @@ __global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
     if (hit && len > 0) {
       const int k = __ffs(hit) - 1;
       const LT* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
-      if (vec_ok) {  // batches of kPer 16-byte loads per lane in flight (c0 is a multiple of 8)
+      if (vec_ok) {  // c0 is a multiple of 8: every 16-byte load is aligned
         const LT* src = rowp + c0;
         const int nv = len / E;
-        for (int base = 0; base < nv; base += 32 * kPer) {
-          uint4 x[kPer];
-#pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int i = base + lane + 32 * u;
-            x[u] = i < nv ? ld_stream16(src + (size_t)E * i) : neg_inf;
-          }
-          // x / T rounded is monotone in x (T > 0), so the batch maximum is scaled once
+        // one batch of loads: its maximum first (x / T rounded is monotone in x, so the
+        // batch maximum is scaled once), then one ex2 per entry against the running maximum
+        auto reduce = [&](const auto& x, int K) {
           typename LogitIO<LT>::MaxAcc acc = LogitIO<LT>::max_init();
 #pragma unroll
-          for (int u = 0; u < kPer; ++u) acc = LogitIO<LT>::max_acc(acc, x[u]);
+          for (int u = 0; u < K; ++u) acc = LogitIO<LT>::max_acc(acc, x[u]);
           const float mb = scale_logit(LogitIO<LT>::max_value(acc), T, unit_T);
           if (mb > m) {  // rescale what was summed so far to the new maximum
             sum = (m == -INFINITY) ? 0.f : sum * exp_shifted(m, mb);
@@ -180,13 +175,44 @@ __global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
           if (m != -INFINITY) {
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < kPer; ++u)
+            for (int u = 0; u < K; ++u)
 #pragma unroll
               for (int j = 0; j < E; j += 2) {
                 s0 += exp_shifted(scale_logit(LogitIO<LT>::entry(x[u], j), T, unit_T), m);
                 s1 += exp_shifted(scale_logit(LogitIO<LT>::entry(x[u], j + 1), T, unit_T), m);
               }
             sum += s0 + s1;
+          }
+        };
+        if constexpr (sizeof(LT) == 2) {
+          // bf16 (8 entries per load, twice the arithmetic per byte): two halves of kPer / 2
+          // loads, one in flight while the other is reduced
+          constexpr int H = kPer / 2, step = 32 * H;
+          uint4 xa[H], xb[H];
+          auto load = [&](uint4 (&x)[H], int base) {
+#pragma unroll
+            for (int u = 0; u < H; ++u) {
+              const int i = base + lane + 32 * u;
+              x[u] = i < nv ? ld_stream16(src + (size_t)E * i) : neg_inf;
+            }
+          };
+          load(xa, 0);
+          for (int base = 0; base < nv; base += 2 * step) {
+            if (base + step < nv) load(xb, base + step);
+            reduce(xa, H);
+            if (base + step >= nv) break;
+            if (base + 2 * step < nv) load(xa, base + 2 * step);
+            reduce(xb, H);
+          }
+        } else {  // fp32: batches of kPer loads per lane in flight
+          for (int base = 0; base < nv; base += 32 * kPer) {
+            uint4 x[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+              const int i = base + lane + 32 * u;
+              x[u] = i < nv ? ld_stream16(src + (size_t)E * i) : neg_inf;
+            }
+            reduce(x, kPer);
           }
         }
       } else {
