@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(32 * kFinishWarps) khat_finish_kernel(
   const int r = blockIdx.x;
   __shared__ float s_alpha[kMaxB];
   // open slots carry the labels 1..R (0: committed in an earlier round); every warp
-  // derives the same verdict
+  // reaches the same decision
   const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : 0;
   const int tau = lb & 0x7F;
   const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau <= B);
