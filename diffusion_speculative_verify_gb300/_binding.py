@@ -53,6 +53,7 @@ class AttnParams(ctypes.Structure):
         ("pos_ids", ctypes.c_void_p), ("labels", ctypes.c_void_p),
         ("rope_theta", ctypes.c_float), ("softmax_scale", ctypes.c_float),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dev_err", ctypes.c_void_p),
+        ("wait_limit_ns", ctypes.c_uint64),
     ]
 
 
@@ -170,7 +171,7 @@ def simsd_build_layout(tau, prompt_len, pos_ids, labels, dev_err, stream=None, f
 
 def make_attn_params(q, k_resp, v_resp, k_cache, v_cache, cache_start, prompt_len, pos_ids,
                      labels, out, dev_err, rope_theta, softmax_scale=0.0, lse=None,
-                     cache_layout="NHD") -> AttnParams:
+                     cache_layout="NHD", wait_limit_ns=0) -> AttnParams:
     dt = q.dtype
     if dt not in (torch.float32, torch.bfloat16):
         raise ValueError("q must be float32 or bfloat16")
@@ -200,6 +201,7 @@ def make_attn_params(q, k_resp, v_resp, k_cache, v_cache, cache_start, prompt_le
     p.out = out.data_ptr()
     p.lse = lse.data_ptr() if lse is not None else None
     p.dev_err = dev_err.data_ptr()
+    p.wait_limit_ns = int(wait_limit_ns)
     return p
 
 

@@ -16,6 +16,7 @@
 //                         winners meet in a 64-bit atomicMax; the last CTA of the request
 //                         (atomic ticket, no waiting) writes the outputs and re-zeroes the
 //                         request's scratch.
+#include <cudaTypedefs.h>
 #include <float.h>
 
 #include <algorithm>
@@ -1027,12 +1028,43 @@ constexpr size_t kNoAllocScratchBytes = (size_t)1 << 20;  // 1 MiB
 static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices];
 
-// Device address of g_accept_scratch on the current device. Resolved on the first call
-// per device (with that device current) and cached; the host-side symbol itself is not a
-// device address and is never passed to a kernel.
+// Identity of the calling thread's current CUDA context (driver entry points resolved once
+// through the runtime). A device reset destroys the context and the next one loads the
+// library's device code again, possibly at another address; the identity tells the two apart.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = (PFN_cuCtxGetCurrent_v4000)p;
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = (PFN_cuCtxGetId_v12000)p;
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchAddr {
+  unsigned long long ctx;  // context the address belongs to
+  void* ptr;
+  bool valid;
+};
+std::mutex g_scratch_mutex;
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+// Device address of g_accept_scratch on the current device. Resolved (with that device
+// current) on the first call per device and again whenever the device's context has been
+// replaced (after a device reset); the host-side symbol itself is not a device address and
+// is never passed to a kernel. Where the context identity cannot be read, the address is
+// looked up on every call (a runtime query; it allocates nothing).
 simsd_status noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1042,16 +1074,24 @@ simsd_status noalloc_scratch(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return SIMSD_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
-    if (e != cudaSuccess || !ptr) {
-      record_cuda_error("cudaGetSymbolAddress", e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-      return SIMSD_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = ptr;
+  ScratchAddr& c = g_scratch_addr[dev];
+  unsigned long long ctx = 0;
+  bool have_ctx = current_context_id(&ctx);
+  if (have_ctx && c.valid && c.ctx == ctx) {
+    *out = c.ptr;
+    return SIMSD_OK;
   }
-  *out = g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
+  if (e != cudaSuccess || !ptr) {
+    record_cuda_error("cudaGetSymbolAddress", e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    return SIMSD_ERR_CUDA;
+  }
+  if (!have_ctx) have_ctx = current_context_id(&ctx);  // the lookup made the context current
+  c.ctx = ctx;
+  c.ptr = ptr;
+  c.valid = have_ctx;
+  *out = ptr;
   return SIMSD_OK;
 }
 }  // namespace
@@ -1067,9 +1107,16 @@ SIMSD_API simsd_status simsd_accept_noalloc(const float* target_logits, const fl
                                             int32_t* n_commit, uint32_t* dev_err,
                                             simsd_stream_t stream) {
   using namespace simsd;
+  // the argument checks of simsd_accept come first, so both return the same status
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;
-  if (batch > 0 && make_plan(batch, gamma, V, temperature == 0.f ? 1 : 2).bytes > kNoAllocScratchBytes)
+  if (!(temperature >= 0.f)) return SIMSD_ERR_INVALID_ARG;
+  if (batch == 0) return SIMSD_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !labels || !accepted_len ||
+      !out_tokens || !out_pos || !n_commit || !dev_err)
+    return SIMSD_ERR_INVALID_ARG;
+  if ((size_t)batch * B * (size_t)V >= ((size_t)1 << 40)) return SIMSD_ERR_UNSUPPORTED;
+  if (make_plan(batch, gamma, V, temperature == 0.f ? 1 : 2).bytes > kNoAllocScratchBytes)
     return SIMSD_ERR_WORKSPACE;  // these sizes need more scratch than the fixed array holds
   void* scratch = nullptr;
   if (batch > 0) {

@@ -24,7 +24,7 @@ SIMSD_API const char* simsd_status_str(simsd_status s) {
   return "SIMSD_ERR_UNKNOWN";
 }
 
-SIMSD_API int simsd_version(void) { return 200; }
+SIMSD_API int simsd_version(void) { return 300; }
 
 namespace simsd {
 static thread_local char g_last_error[256];

@@ -12,30 +12,34 @@
 // (its prologue and epilogue cost in tile units), are concatenated and cut into equal
 // contiguous ranges, one per schedule unit (stream-K); a unit therefore sees at most two
 // partial pairs (its first and last), whose (O, max, sum) partials are merged by
-// attn_tc_merge_kernel, a programmatic dependent launch. A unit is one CTA for pairs of up to 128 rows and a cluster of two
-// CTAs (rows [0, 128) and [128, 256)) above that; the two load each prompt tile once,
-// half each, multicast into both.
+// attn_tc_merge_kernel, a programmatic dependent launch.
 //
-// Per CTA, warp roles:
+// A schedule unit is one CTA for pairs of up to 128 rows and two CTAs (rows [0, 128) and
+// [128, 256)) above that; the two walk the same tiles, each loading every prompt tile into
+// its own shared memory (the second read of a tile mostly hits L2). Per CTA, warp roles:
 //   producer warp  : TMA loads of prompt K and V tiles (128-byte swizzle) into a ring of
-//                    three 64 KB shared-memory stages.
+//                    three 64 KB shared-memory slots.
 //   MMA warp       : one thread issues S = Q K^T (M = 128 rows, N = 128 keys, K = 128; A =
 //                    the rotated Q in TMEM) into one of two TMEM S buffers, then O += P V
-//                    (M = 128, N = 128, K = 128 keys; A = bf16 P in TMEM) into the TMEM O
+//                    (M = 128, N = 128 = D, K = 128 keys; A = bf16 P in TMEM) into the TMEM O
 //                    accumulator; completion is signalled with tcgen05.commit to mbarriers.
 //   softmax warps  : one thread per query row (TMEM lane). Per segment: load + rotate Q
-//                    into TMEM and build the response K/V tail tile; per tile: read S from
-//                    TMEM, apply the mask, and write P = 2^(s - m) (bf16) in place over the
-//                    S columns just read, in one pass unless the running max grows by more
-//                    than 2^8 (then O and the P already written are rescaled); epilogue:
-//                    O / l to global memory (or the partial to the workspace).
-// Every wait is bounded in time; on expiry the kernel raises SIMSD_DEVERR_TIMEOUT in the
-// error word and unwinds (no trap).
+//                    into TMEM and build the response K/V tail tile; per tile:
+//                    read S from TMEM, apply the mask, and write P = 2^(s - m) (bf16) in
+//                    place over the S columns just read, in one pass unless the running max
+//                    grows by more than 2^8 (then O and the P already written are rescaled);
+//                    epilogue: O / l to global memory (or the partial to the workspace).
+// Every wait is bounded in time (TcArgs::wait_ns). A wait that gives up raises
+// SIMSD_DEVERR_TIMEOUT and sets the CTA's abort flag. The softmax warps decide to stop
+// together, at the start of a segment (so none waits at a named barrier for one that has
+// left); the rows the CTA has not finished are set to NaN; the producer waits for its copies
+// in flight and the MMA thread for its MMAs; then the CTA frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -44,11 +48,13 @@
 namespace simsd {
 namespace tc {
 
-constexpr int kTileKeys = 64;
 constexpr int kD = 128;
+constexpr int kKeys = 128;                          // prompt keys per tile
 constexpr int kBlockRows = 128;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
-constexpr int kMaxStages = 8;                         // stage barriers reserved in shared memory
+constexpr int kTileKeys = 64;                       // granularity of the host-side grid heuristic
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint64_t kDrainWaitNs = 100000000ull;     // unwinding: copies / MMAs already issued
+constexpr int kMaxSlots = 8;                        // ring barriers reserved in shared memory
 // Start-up and finish of one pair segment (prologue, epilogue, pipeline refill) in units of
 // one prompt tile's time; the schedule charges it to every pair. It grows with the response
 // span (the RoPE table, the tail rows and the visibility masks scale with 2B): measured on
@@ -56,13 +62,14 @@ constexpr int kMaxStages = 8;                         // stage barriers reserved
 static int seg_cost_tiles(int twoB) { return 4 + twoB / 16; }
 constexpr int kPrefetchAhead = 4;  // tiles before a segment's end at which the next one is prefetched
 
+struct MergeDesc;
 
 struct TcArgs {
   int batch, B, Hq, Hkv, G, R, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
-  int cl;                                  // CTAs per schedule unit (a cluster): 1, or 2 when R > 128
-  int tile_keys;                           // prompt keys per tile (64 or 128)
-  int seg_cost;                            // virtual units charged per pair for start-up
+  int cl;                             // CTAs per schedule unit: 1, or 2 when R > 128
+  int seg_cost;                       // virtual units charged per pair for start-up
   int layout;
+  uint64_t wait_ns;                   // bound of every device-side wait
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_resp;
   const __nv_bfloat16* v_resp;
@@ -74,31 +81,37 @@ struct TcArgs {
   __nv_bfloat16* out;
   float* lse;
   uint32_t* dev_err;
-  float* ws_o;     // [2 * CTAs][128][128] partial numerators
-  float2* ws_ml;   // [2 * CTAs][128] partial (max, sum), log2 domain
-  struct MergeDesc* ws_desc;  // [ctas] split pair starting in each CTA (or none)
+  float* ws_o;         // [2 * ctas * cl][128][128] partial numerators
+  float2* ws_ml;       // [2 * ctas * cl][128] partial (max, sum), log2 domain
+  MergeDesc* ws_desc;  // [ctas * cl] split pair starting in each CTA (or none)
   RopeTable rope;
 };
 
 // Written by every CTA for the pair its range ends in, when that pair started inside the
 // range and continues past it; the merge kernel combines that pair's pieces.
 struct MergeDesc {
-  int b, h, c_last, slot0;  // b < 0: no split pair starts here
+  int b, h, c_last, piece0;  // b < 0: no split pair starts here; c_last: last unit holding a
+                             // piece; piece0: the piece's slot in this CTA (0 first, 1 last)
   long long T;
 };
+
+// Workspace slot of a partial: CTA `cta`, piece 0 (its range's first segment) or 1 (its last).
+__host__ __device__ __forceinline__ size_t part_slot(int cta, int piece) {
+  return (size_t)2 * cta + piece;
+}
 
 // ----------------------------------------------------------------------- scheduling
 // Pair (b, h) has nt(b) = 1 + ceil(P_b / 128) tiles (1 for an invalid request). Besides its
 // tiles it is charged `seg_cost` virtual units for its start-up and finish (prologue,
 // epilogue, pipeline refill), so it spans nt(b) + seg_cost units of the virtual sequence
-// that is cut into equal contiguous ranges, one per schedule unit. A range that begins
-// inside a pair's start-up share starts at the pair's tile 0; one that ends inside it does
-// not take the pair.
+// that is cut into equal contiguous ranges, one per schedule unit. A range that begins inside
+// a pair's start-up share starts at the pair's tile 0; one that ends inside it does not take
+// the pair.
 __device__ __forceinline__ int tiles_per_pair(const TcArgs& a, int b) {
   const int P = a.prompt_len[b];
   const uint8_t l0 = a.labels[(size_t)b * 2 * a.B];  // both loads issued together
   if ((P < 0) | (l0 == kLabelInvalid)) return 1;
-  return 1 + (P + a.tile_keys - 1) / a.tile_keys;
+  return 1 + (P + kKeys - 1) / kKeys;
 }
 __device__ __forceinline__ bool request_invalid(const TcArgs& a, int b) {
   const int P = a.prompt_len[b];
@@ -225,7 +238,7 @@ struct SegIter {
   }
 };
 
-// Yields the prompt tiles (kv head, first cache row) of one CTA's range, in order.
+// Yields the prompt tiles (kv head, first cache row) of one unit's range, in order.
 struct PromptTiles {
   SegIter it;
   int i;
@@ -246,7 +259,7 @@ struct PromptTiles {
           const int ii = i++;
           if (ii == 0) continue;
           h = it.h;
-          tok = (int)(a.cache_start[it.b] + (int64_t)(ii - 1) * a.tile_keys);
+          tok = (int)(a.cache_start[it.b] + (int64_t)(ii - 1) * kKeys);
           return true;
         }
       }
@@ -257,8 +270,10 @@ struct PromptTiles {
 };
 
 // --------------------------------------------------------------------- small helpers
-enum BarIdx { kFull0 = 0, kEmpty0 = kMaxStages, kSFull0 = 2 * kMaxStages, kSFree0 = kSFull0 + 2,
-              kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kQFull = kPFree0 + 2, kDrain = kQFull + 1,
+// Barriers: ring slots (full / empty); per S buffer: S written, the P V that read it
+// completed, P written; Q and tail stored; MMA drain; the first prologue's loads landed.
+enum BarIdx { kFull0 = 0, kEmpty0 = kMaxSlots, kSFull0 = 2 * kMaxSlots, kSFree0 = kSFull0 + 2,
+              kPFull0 = kSFree0 + 2, kQFull = kPFull0 + 2, kDrain = kQFull + 1,
               kLoads = kDrain + 1, kNumBars = kLoads + 1 };
 
 struct Shared {
@@ -270,21 +285,44 @@ struct Shared {
   int64_t wsum[4];          // block scan of the schedule
 };
 
+// Sets the CTA's abort flag and, once, the timeout bit of the error word.
+__device__ __forceinline__ void raise_abort(Shared* sh, uint32_t* dev_err) {
+  if (!*(volatile int*)&sh->abort) {
+    *(volatile int*)&sh->abort = 1;
+    atomicOr(dev_err, SIMSD_DEVERR_TIMEOUT);
+  }
+}
 
+// One probe of phase `parity` of mbarrier `bar`. A plain try_wait may suspend the thread
+// until the phase completes; below kHintedWaitNs the wait limit is passed as the suspend-time
+// hint instead, so that so short a limit can run out.
+constexpr uint64_t kHintedWaitNs = 1000000ull;
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return limit_ns < kHintedWaitNs ? ptx::mbar_try_wait_hint(bar, parity, (uint32_t)limit_ns)
+                                  : ptx::mbar_try_wait(bar, parity);
+}
+
+// Waits for phase `parity` of mbarrier `bar`. False if the CTA is unwinding, or if the wait
+// gave up after limit_ns (it then starts the unwinding).
 __device__ __forceinline__ bool wait_bar(Shared* sh, uint32_t bar, uint32_t parity,
-                                         uint32_t* dev_err) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+                                         uint32_t* dev_err, uint64_t limit_ns) {
+  if (bar_try(bar, parity, limit_ns)) return true;
   const uint64_t t_start = ptx::globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*(volatile int*)&sh->abort) return false;
-      if (ptx::globaltimer_ns() - t_start > kWaitLimitNs) {
-        *(volatile int*)&sh->abort = 1;
-        atomicOr(dev_err, SIMSD_DEVERR_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (bar_try(bar, parity, limit_ns)) return true;
+    if (*(volatile int*)&sh->abort) return false;
+    if (ptx::globaltimer_ns() - t_start > limit_ns) {
+      raise_abort(sh, dev_err);
+      return false;
     }
+  }
+}
+
+// Waits, bounded by kDrainWaitNs and regardless of the abort flag, for a phase that work this
+// CTA has already issued completes: used for copies and MMAs in flight before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t_start = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t_start < kDrainWaitNs) {
   }
 }
 
@@ -387,35 +425,47 @@ __device__ __forceinline__ void store_row_sw(uint8_t* tile, uint32_t half_bytes,
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half_bytes + sw128(r, c & 7)) = v[c];
 }
 
+// Which tail row (response K, rotated here, or response V) softmax thread `tid` loads in a
+// segment's prologue. When the threads beyond this CTA's rows (tid >= rw) can take all
+// 2 * 2B tail rows ("early"), they load them together with the Q rows; otherwise threads
+// 0..63 take the K rows and 64..127 the V rows (zero rows beyond 2B) once Q is in TMEM.
+struct TailRole {
+  int key;
+  bool row, k, early;
+};
+__device__ __forceinline__ TailRole tail_role(int rw, int twoB, int tid, bool has_tail) {
+  TailRole t;
+  t.early = has_tail && 128 - rw >= 2 * twoB;
+  if (t.early) {
+    const int e = tid - rw;
+    t.row = e >= 0 && e < 2 * twoB;
+    t.k = e < twoB;
+    t.key = t.k ? e : e - twoB;
+  } else {
+    t.key = tid & 63;
+    t.row = has_tail && t.key < twoB;
+    t.k = tid < 64;
+  }
+  return t;
+}
+
 // L2 prefetch of what the prologue of the segment (request nb, kv head nh, with a tail tile
 // when ntail) loads: this thread's Q row, its tail K or V row (same thread mapping as the
 // prologue) and the labels and position ids.
-__device__ __forceinline__ void prefetch_prologue(const TcArgs& a, int nb, int nh, int ntail, int twoB,
-                                                  int s_slot, int g, bool real, int rw, int tid) {
+__device__ __forceinline__ void prefetch_prologue(const TcArgs& a, int nb, int nh, int ntail,
+                                                  int twoB, int s_slot, int g, bool real, int rw,
+                                                  int tid) {
   if (real) {
     const __nv_bfloat16* qrow = a.q + (((size_t)nb * twoB + s_slot) * a.Hq + (size_t)nh * a.G + g) * kD;
     asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
     asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + 64));
   }
-  if (ntail) {
-    int key;
-    bool tail_row, tail_k;
-    if (128 - rw >= 2 * twoB) {
-      const int e = tid - rw;
-      tail_row = e >= 0 && e < 2 * twoB;
-      tail_k = e < twoB;
-      key = tail_k ? e : e - twoB;
-    } else {
-      key = tid & 63;
-      tail_row = key < twoB;
-      tail_k = tid < 64;
-    }
-    if (tail_row) {
-      const __nv_bfloat16* trow =
-          (tail_k ? a.k_resp : a.v_resp) + (((size_t)nb * twoB + key) * a.Hkv + nh) * kD;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
-    }
+  const TailRole tr = tail_role(rw, twoB, tid, ntail != 0);
+  if (tr.row) {
+    const __nv_bfloat16* trow =
+        (tr.k ? a.k_resp : a.v_resp) + (((size_t)nb * twoB + tr.key) * a.Hkv + nh) * kD;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
   }
   if (tid == 0) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a.labels + (size_t)nb * twoB));
@@ -440,10 +490,35 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]
   }
 }
 
+// This thread's output row of a segment the CTA did not finish: a whole pair's row (and its
+// lse) becomes NaN; a piece of a split pair gets a NaN partial, which the merge carries into
+// the pair's output. Invalid requests get their zero rows as usual.
+__device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& it, bool real,
+                                                size_t orow, size_t slot, int row) {
+  if (!real) return;
+  if (it.invalid) {
+    uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
+    if (a.lse) a.lse[orow] = -INFINITY;
+    return;
+  }
+  const float qnan = __int_as_float(0x7FC00000);
+  if (it.full) {
+    const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
+    uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) o[c] = make_uint4(nan2, nan2, nan2, nan2);
+    if (a.lse) a.lse[orow] = qnan;
+  } else {
+    a.ws_ml[slot * kBlockRows + row] = make_float2(qnan, qnan);
+  }
+}
+
 // =========================================================================================
-// Pairs of up to 128 query rows (2B*G <= 128): 128-key prompt tiles, and every operand that
-// an MMA reads as A lives in TMEM, which lets each tcgen05.mma run at full rate (an A
-// operand from shared memory, or N < 128, caps an M = 128 instruction well below it):
+// Every operand an MMA reads as A lives in TMEM, which lets each tcgen05.mma run at full
+// rate (an A operand from shared memory, or N < 128, caps an M = 128 instruction well below
+// it):
 //   S_j = Q K_j^T   A = rotated Q (TMEM), B = K tile (smem, K-major), N = 128 keys
 //   O  += P_j V_j   A = P_j (TMEM, bf16),  B = V tile (smem, MN-major), N = 128 = D
 // TMEM columns: S buffers [0,128) and [128,256), O [256,384), Q [384,448). P_j (bf16 pairs,
@@ -453,7 +528,6 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]
 // Warps 0-3: softmax (thread = row = TMEM lane; warps whose 32 rows are all padding skip
 // their work), warp 4: TMA producer, warp 5: MMA issuer (non-blocking event loop).
 namespace r128 {
-constexpr int kKeys = 128;                       // prompt keys per tile
 constexpr uint32_t kHalf = kKeys * 128;          // 16 KB: one 64-element half of a K or V tile
 constexpr uint32_t kKV = 2 * kHalf;              // 32 KB
 constexpr uint32_t kStage = 2 * kKV;             // 64 KB: K + V
@@ -464,11 +538,11 @@ constexpr uint32_t kTailKV = 2 * kTailHalf;      // 16 KB
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffTail = kOffStages + kStages * kStage;  // tail K (16 KB) then V (16 KB)
 constexpr uint32_t kOffBar = kOffTail + 2 * kTailKV;
-constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;
+constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;        // barriers + alignment slack
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemQ = 384, kTmemCols = 512;
-static_assert(kStages <= kMaxStages, "stage barriers");
+static_assert(kStages <= kMaxSlots, "stage barriers");
 }  // namespace r128
 
 __global__ void __launch_bounds__(r128::kThreads, 1)
@@ -484,23 +558,23 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = ptx::smem_u32(smem);
   auto bar = [&](int i) { return ptx::smem_u32(&sh->bars[i]); };
+  // Pairs of more than 128 rows: two CTAs take each schedule unit, CTA `crank` the rows
+  // [128 crank, 128 crank + 128); they are independent (each loads the unit's prompt tiles
+  // itself) and differ only in their rows.
+  const int cl = a.cl;
+  const int vcta = blockIdx.x / cl, crank = blockIdx.x - vcta * cl;
+  const int row0 = crank * 128;  // first pair row of this CTA
+  const uint64_t wait_ns = a.wait_ns;
   // kPFull0 + b: P of the tile in S buffer b written. kSFree0 + b: the P V that read S
   // buffer b completed; its phase for tile j is j / 2, and the previous phase (tile j - 2) is
   // always complete by the time anyone waits for tile j, so a parity wait is unambiguous.
-  // Pairs of more than 128 rows: a cluster of two CTAs takes each schedule unit, CTA `crank`
-  // the rows [128 crank, 128 crank + 128); each prompt tile is loaded once, half by each
-  // CTA, multicast into both, and a stage is refilled once both CTAs have released it.
-  const int cl = a.cl;
-  const int vcta = blockIdx.x / cl, crank = blockIdx.x - vcta * cl;
-  const uint16_t cmask = (uint16_t)((1u << cl) - 1u);
-  const int row0 = crank * 128;  // first pair row of this CTA
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       // When every unit is one pair, this unit's pair is known before the schedule: its
       // first prompt tiles go into L2 now, so that the stream, which starts after the first
       // prologue, finds them there.
-      if (cl == 1 && (int64_t)a.batch * a.Hkv == (int64_t)a.ctas) {
+      if ((int64_t)a.batch * a.Hkv == (int64_t)a.ctas) {
         const int gb = vcta / a.Hkv, gh = vcta - (vcta / a.Hkv) * a.Hkv;
         const int P = a.prompt_len[gb];
         const int64_t cs = a.cache_start[gb];
@@ -522,7 +596,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       sh->abort = 0;
       for (int i = 0; i < kStages; ++i) {
         ptx::mbar_init(bar(kFull0 + i), 1);
-        ptx::mbar_init(bar(kEmpty0 + i), (uint32_t)cl);
+        ptx::mbar_init(bar(kEmpty0 + i), 1);
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(bar(kSFull0 + i), 1);
@@ -550,13 +624,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       const bool real = prow < a.R;
       const int rw = (min(128, a.R - row0) + 31) & ~31;
       if (gb < a.batch)
-        prefetch_prologue(a, gb, gh, 1, 2 * a.B, real ? prow / a.G : 0, real ? prow % a.G : 0, real, rw, tid);
+        prefetch_prologue(a, gb, gh, 1, 2 * a.B, real ? prow / a.G : 0, real ? prow % a.G : 0,
+                          real, rw, tid);
     }
     block_schedule(a, vcta, a.ctas, tid, sh->wsum, &sh->T, &sh->t0, &sh->t1, &sh->Tb, &sh->b);
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (cl > 1) ptx::cluster_sync_all();  // the peer's barriers are initialised before any use
   ptx::tc_fence_after();
 
   SchedStart st;
@@ -573,55 +647,40 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     if (lane == 0) {
       PromptTiles tiles;
       tiles.init(a, st);
-      uint32_t m = 0;
-      bool ok = true;
+      uint32_t p = 0;  // tiles loaded (ring position)
+      bool ok = true, first = true;
       int h, tok;
-      while (tiles.next(a, h, tok)) {
-        const int s = m % kStages;
+      while (ok && tiles.next(a, h, tok)) {
         // the first prologue's global loads are issued before the prompt stream, so that
         // they are not queued behind it (the first tile the MMA issuer needs is the tail
         // tile, which the prologue builds in shared memory)
-        if (m == 0) {
-          ok = wait_bar(sh, bar(kLoads), 0, a.dev_err);
+        if (first) {
+          first = false;
+          ok = wait_bar(sh, bar(kLoads), 0, a.dev_err, wait_ns);
           if (!ok) break;
         }
-        ok = wait_bar(sh, bar(kEmpty0 + s), ((m / kStages) & 1) ^ 1, a.dev_err);
+        const int s = p % kStages;
+        ok = wait_bar(sh, bar(kEmpty0 + s), ((p / kStages) & 1) ^ 1, a.dev_err, wait_ns);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
         const uint32_t kdst = sbase + kOffStages + s * kStage;
         const uint32_t vdst = kdst + kKV;
-        if (cl == 1) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (a.layout == SIMSD_CACHE_NHD) {
-              ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
-              ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
-            } else {
-              ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
-              ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
-            }
-          }
-        } else {  // this CTA's half of the tile (K for rank 0, V for rank 1), into both CTAs
-          const CUtensorMap* map = crank == 0 ? &tmk : &tmv;
-          const uint32_t dst = crank == 0 ? kdst : vdst;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (a.layout == SIMSD_CACHE_NHD)
-              ptx::tma_load_3d_mc(dst + half * kHalf, map, half * 64, h, tok, bar(kFull0 + s), cmask);
-            else
-              ptx::tma_load_3d_mc(dst + half * kHalf, map, half * 64, tok, h, bar(kFull0 + s), cmask);
+        for (int half = 0; half < 2; ++half) {
+          if (a.layout == SIMSD_CACHE_NHD) {
+            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
+          } else {
+            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
+            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
           }
         }
-        ++m;
+        ++p;
       }
-      if (!ok) {  // let the loads already issued land before shared memory goes away
-        for (uint32_t k = m > (uint32_t)kStages ? m - kStages : 0; k < m; ++k) {
-          const uint64_t t_start = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(bar(kFull0 + k % kStages), (k / kStages) & 1) &&
-                 ptx::globaltimer_ns() - t_start < 100000000ull) {
-          }
-        }
-      }
+      // Whether the stream ended or the CTA is unwinding, the copies issued last may still be
+      // in flight; they land before the CTA can exit (earlier ones have been consumed).
+      for (uint32_t k = p > (uint32_t)kStages ? p - kStages : 0; k < p; ++k)
+        drain_wait(bar(kFull0 + k % kStages), (k / kStages) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------- MMA issuer
@@ -633,7 +692,37 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       it.init(a, st);
       uint32_t j = 0, m = 0, nseg = 0;
       bool ok = true;
-      int stage_of[8];  // per tile (ring): stage to release after its P V, -1 = tail tile
+      // Polls (no suspend) until the segment's Q and tail are stored; false once the CTA
+      // unwinds or after wait_ns.
+      auto poll_qfull = [&]() -> bool {
+        const uint64_t t_start = ptx::globaltimer_ns();
+        uint32_t spin = 0;
+        while (!ptx::mbar_test(bar(kQFull), nseg & 1)) {
+          if ((++spin & 255) == 0) {
+            if (*(volatile int*)&sh->abort) return false;
+            if (ptx::globaltimer_ns() - t_start > wait_ns) {
+              raise_abort(sh, a.dev_err);
+              return false;
+            }
+          }
+        }
+        return true;
+      };
+      // Called when the issue loop made no progress: true once it has gone wait_ns without
+      // any (then the CTA unwinds) or the CTA is unwinding.
+      uint32_t spins = 0;
+      uint64_t t_idle = 0;
+      auto stalled = [&]() -> bool {
+        if ((++spins & 63) != 0) return false;
+        const uint64_t now = ptx::globaltimer_ns();
+        if (spins == 64) t_idle = now;
+        if (*(volatile int*)&sh->abort || now - t_idle > wait_ns) {
+          raise_abort(sh, a.dev_err);
+          return true;
+        }
+        return false;
+      };
+      int stage_of[8];  // per tile (ring): slot to release after its P V, -1 = tail tile
       static_assert(kAhead + 1 <= 8, "tile ring");
       auto try_issue_s = [&](uint32_t jj, int i) -> bool {
         const int buf = jj & 1;
@@ -676,12 +765,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
                           ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV,
                           (first_in_seg && kk == 0) ? 0u : 1u);
         ptx::mma_commit(bar(kSFree0 + buf));
-        if (s >= 0) {
-          if (cl == 1)
-            ptx::mma_commit(bar(kEmpty0 + s));
-          else
-            ptx::mma_commit_mc(bar(kEmpty0 + s), cmask);  // the stage is free in both CTAs' eyes
-        }
+        if (s >= 0) ptx::mma_commit(bar(kEmpty0 + s));
         return true;
       };
       while (ok && it.next(a)) {
@@ -689,26 +773,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           it.advance(a);
           continue;
         }
-        {  // poll (no suspend): the segment cannot start before Q is in TMEM
-          const uint64_t t_start = ptx::globaltimer_ns();
-          uint32_t spin = 0;
-          while (!ptx::mbar_test(bar(kQFull), nseg & 1)) {
-            if ((++spin & 255) == 0 &&
-                (*(volatile int*)&sh->abort || ptx::globaltimer_ns() - t_start > kWaitLimitNs)) {
-              if (!*(volatile int*)&sh->abort) {
-                *(volatile int*)&sh->abort = 1;
-                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
-              }
-              ok = false;
-              break;
-            }
-          }
+        if (!poll_qfull()) {  // the segment cannot start before Q is in TMEM
+          ok = false;
+          break;
         }
-        if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t jfirst = j, jend = j + (uint32_t)it.n;
-        uint32_t ns = jfirst, npv = jfirst, spins = 0;
-        uint64_t t_idle = 0;
+        uint32_t ns = jfirst, npv = jfirst;
+        spins = 0;
         while (npv < jend) {
           bool progressed = false;
           if (npv < ns && try_issue_pv(npv, npv == jfirst)) {
@@ -721,19 +793,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           }
           if (progressed) {
             spins = 0;
-            continue;
-          }
-          if ((++spins & 63) == 0) {  // bounded: give up after kWaitLimitNs without progress
-            const uint64_t now = ptx::globaltimer_ns();
-            if (spins == 64) t_idle = now;
-            if (*(volatile int*)&sh->abort || now - t_idle > kWaitLimitNs) {
-              if (!*(volatile int*)&sh->abort) {
-                *(volatile int*)&sh->abort = 1;
-                atomicOr(a.dev_err, SIMSD_DEVERR_TIMEOUT);
-              }
-              ok = false;
-              break;
-            }
+          } else if (stalled()) {
+            ok = false;
+            break;
           }
         }
         if (!ok) break;
@@ -741,10 +803,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ++nseg;
         it.advance(a);
       }
+      // every MMA issued has completed before TMEM is freed
       ptx::mma_commit(bar(kDrain));
-      const uint64_t t_start = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar(kDrain), 0) && ptx::globaltimer_ns() - t_start < 100000000ull) {
-      }
+      drain_wait(bar(kDrain), 0);
     }
   } else {
     // -------------------------------------------------------------- softmax warps
@@ -755,307 +816,311 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     const int s_slot = real ? prow / a.G : 0;
     const int g = real ? prow % a.G : 0;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tmem_o = tmem + lane_off + kTmemO;
     uint8_t* tailk = smem + kOffTail;
     uint8_t* tailv = tailk + kTailKV;
+    const int rw = (min(128, a.R - row0) + 31) & ~31;  // threads below rw own this block's rows
     SegIter it;
     it.init(a, st);
     uint32_t j = 0;
-    bool ok = true;
+    bool aborted = false;
     bool loads_signalled = false;  // each thread arrives on kLoads once
     MergeDesc desc;
     desc.b = -1;
     desc.T = st.T;
-    while (ok && it.next(a)) {
+    while (it.next(a)) {
+      // Every softmax thread reaches this point once per segment: the decision to unwind is
+      // taken here by all of them together.
+      ptx::named_bar_sync(1, 128);
+      if (*(volatile int*)&sh->abort) {
+        aborted = true;
+        break;
+      }
       const int b = it.b, h = it.h;
       if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
         desc.b = b;
         desc.h = h;
         desc.c_last = (int)((it.pend * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
-        desc.slot0 = 2 * blockIdx.x + (it.first ? 0 : 1);
+        desc.piece0 = it.first ? 0 : 1;
       }
       const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
+      const size_t slot = part_slot(blockIdx.x, it.first ? 0 : 1);
       if (it.invalid) {
-        if (real) {
-          uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
-          if (a.lse) a.lse[orow] = -INFINITY;
-        }
+        mark_unfinished(a, it, real, orow, slot, row);  // zero rows, lse = -inf
         if (tid == 0 && h == 0 && a.prompt_len[b] < 0) atomicOr(a.dev_err, SIMSD_DEVERR_PROMPT_LEN);
         it.advance(a);
         continue;
       }
-      const int P = a.prompt_len[b];
-      const bool has_tail = it.has_tail;
-      // ---- prologue: rotated + scaled Q rows into TMEM, rotated tail K and plain tail V
-      // tiles. Each thread holds at most one row. When the warps beyond the pair's rows can
-      // take the 2 * 2B tail rows ("early"), those load them together with the Q rows, so
-      // the prologue waits on memory once; otherwise the tail rows are prefetched into L2
-      // with the Q loads and loaded once Q is in TMEM.
-      const int rw = (min(128, a.R - row0) + 31) & ~31;  // threads below rw own this block's rows
-      const bool early = has_tail && 128 - rw >= 2 * twoB;
-      int key;
-      bool tail_row, tail_k;
-      if (early) {
-        const int e = tid - rw;
-        tail_row = e >= 0 && e < 2 * twoB;
-        tail_k = e < twoB;
-        key = tail_k ? e : e - twoB;
-      } else {
-        key = tid & 63;
-        tail_row = has_tail && key < twoB;
-        tail_k = tid < 64;
-      }
-      // labels and position ids of the 2B response slots: every warp holds slot `lane` and
-      // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip);
-      // issued before the row loads, whose many requests would otherwise delay them
-      const size_t lrow = (size_t)b * twoB;
-      const uint32_t lab_lo = lane < twoB ? a.labels[lrow + lane] : 0u;
-      const uint32_t lab_hi = lane + 32 < twoB ? a.labels[lrow + 32 + lane] : 0u;
-      const int pos_lo = lane < twoB ? a.pos_ids[lrow + lane] : 0;
-      const int pos_hi = lane + 32 < twoB ? a.pos_ids[lrow + 32 + lane] : 0;
-      uint4 v[16];
-      const __nv_bfloat16* trow =
-          (tail_k ? a.k_resp : a.v_resp) + (((size_t)b * twoB + (tail_row ? key : 0)) * a.Hkv + h) * kD;
-      if (warp_active) {
-        if (real) load_row(v, a.q + orow * kD);
-      } else if (early && tail_row) {
-        load_row(v, trow);
-      }
-      if (!early && tail_row) {  // into L2 now, into registers once Q is in TMEM
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
-      }
-      // (cos, sin) of the 2B response positions, over the tail K and V area (2B <= 64:
-      // at most 32 KB); the tail rows are stored once every read of the table is done. Rows
-      // are 66 float2 apart where that fits (16 bytes of padding: threads reading different
-      // positions' rows then hit different banks), else 64. Thread t fills pair t % 64 of
-      // the slots t / 64, t / 64 + 2, ... (the slot is warp-uniform).
-      float2* rtab = reinterpret_cast<float2*>(tailk);
-      const int tstride = twoB * 66 * 8 <= (int)(2 * kTailKV) ? 66 : 64;
-      {
-        const int d = tid & 63;
-        const float c_hi = a.rope.c_hi[d], c_lo = a.rope.c_lo[d];
-        for (int sidx = tid >> 6; sidx < twoB; sidx += 2) {
-          const int ps = __shfl_sync(0xffffffffu, sidx < 32 ? pos_lo : pos_hi, sidx & 31);
-          float sn, cs;
-          rope_sincos_fast(ps, c_hi, c_lo, &sn, &cs);
-          rtab[sidx * tstride + d] = make_float2(cs, sn);
-        }
-      }
-      // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
-      uint32_t vis0 = 0, vis1 = 0;
-      if (has_tail) {
-        const uint32_t own_lo = __shfl_sync(0xffffffffu, lab_lo, s_slot & 31);
-        const uint32_t own_hi = __shfl_sync(0xffffffffu, lab_hi, s_slot & 31);
-        const int th = row_threshold((uint8_t)(s_slot < 32 ? own_lo : own_hi));
-        for (int k = 0; k < twoB; ++k) {
-          const uint32_t lk = __shfl_sync(0xffffffffu, k < 32 ? lab_lo : lab_hi, k & 31);
-          if (response_key_visible((uint8_t)lk, th)) {
-            if (k < 32)
-              vis0 |= 1u << k;
-            else
-              vis1 |= 1u << (k - 32);
-          }
-        }
-        if (!real) {
-          vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
-          vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
-        }
-      }
-      ptx::named_bar_sync(1, 128);
-      if (warp_active) {
-        if (real) {
-          rope_row(v, rtab + s_slot * tstride, a.scale_log2);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
-        }
-        // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
-        tmem_st_row(tmem + lane_off + kTmemQ, v);
-        ptx::tmem_st_wait();
-      } else if (early && tail_row && tail_k) {
-        rope_row(v, rtab + key * tstride, 1.f);  // K rotated, V as is
-      }
-      if (!early && has_tail) {
-        if (tail_row) {
+      bool ok = true;
+      do {
+        const int P = a.prompt_len[b];
+        const bool has_tail = it.has_tail;
+        // ---- prologue: rotated + scaled Q rows into TMEM, rotated tail K and plain tail V
+        // tiles. Each thread holds at most one row.
+        const TailRole tr = tail_role(rw, twoB, tid, has_tail);
+        // labels and position ids of the 2B response slots: every warp holds slot `lane` and
+        // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip);
+        // issued before the row loads, whose many requests would otherwise delay them
+        const size_t lrow = (size_t)b * twoB;
+        const uint32_t lab_lo = lane < twoB ? a.labels[lrow + lane] : 0u;
+        const uint32_t lab_hi = lane + 32 < twoB ? a.labels[lrow + 32 + lane] : 0u;
+        const int pos_lo = lane < twoB ? a.pos_ids[lrow + lane] : 0;
+        const int pos_hi = lane + 32 < twoB ? a.pos_ids[lrow + 32 + lane] : 0;
+        uint4 v[16];
+        const __nv_bfloat16* trow =
+            (tr.k ? a.k_resp : a.v_resp) + (((size_t)b * twoB + (tr.row ? tr.key : 0)) * a.Hkv + h) * kD;
+        if (warp_active) {
+          if (real) load_row(v, a.q + orow * kD);
+        } else if (tr.early && tr.row) {
           load_row(v, trow);
-          if (tail_k) rope_row(v, rtab + key * tstride, 1.f);  // K rotated, V as is
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
         }
-      }
-      if (!loads_signalled) {  // this prologue's rows have landed: the prompt stream may start
-        ptx::mbar_arrive(bar(kLoads));
-        loads_signalled = true;
-      }
-      ptx::named_bar_sync(1, 128);  // table reads done
-      if (early) {
-        if (tail_row) store_row_sw(tail_k ? tailk : tailv, kTailHalf, key, v);
-        // keys 2B .. 63 of both tail tiles are zero (the tail MMAs read 64 keys)
-        const uint4 z[16] = {};
-        for (int e = tid; e < 2 * (64 - twoB); e += 128) {
-          const int zk = twoB + e % (64 - twoB);
-          store_row_sw(e < 64 - twoB ? tailk : tailv, kTailHalf, zk, z);
+        if (!tr.early && tr.row) {  // into L2 now, into registers once Q is in TMEM
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
         }
-      } else if (has_tail) {
-        store_row_sw(tail_k ? tailk : tailv, kTailHalf, key, v);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kQFull));
-      float m_used = -INFINITY, l = 0.f;
-      const uint32_t jfirst = j;
-      // The next segment's Q rows, tail rows and labels go into L2 a few tiles before this
-      // segment ends, so that its prologue does not wait behind the K/V stream in flight.
-      int pf_b = -1, pf_h = 0;  // next segment: request, kv head | has_tail << 16
-      {
-        SegIter nx = it;
-        nx.advance(a);
-        if (nx.next(a) && !nx.invalid) {
-          pf_b = nx.b;
-          pf_h = nx.h | (nx.has_tail ? 1 << 16 : 0);
-        }
-      }
-      const int pf_at = max(it.i0, it.i0 + it.n - kPrefetchAhead);
-      for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
-        const int buf = j & 1;
-        if (pf_b >= 0 && i == pf_at)
-          prefetch_prologue(a, pf_b, pf_h & 0xffff, pf_h >> 16, twoB, s_slot, g, real, rw, tid);
-        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err));
-        if (!ok) break;
-        if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
-          ptx::mbar_arrive(bar(kPFull0 + buf));
-          continue;
-        }
-        ptx::tc_fence_after();
-        const uint32_t ts = tmem + lane_off + kTmemS0 + buf * 128;
-        const int nchunks = (i == 0) ? 2 : kKeys / 32;  // warp-uniform
-        const int nvalid = (i == 0) ? 0 : P - (i - 1) * kKeys;
-        // valid-column bits of 32-column chunk k
-        auto chunk_mask = [&](int k) -> uint32_t {
-          if (i == 0) return k == 0 ? vis0 : vis1;
-          const int n = nvalid - 32 * k;
-          return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-        };
-        // One pass in the common case: chunk k's P = 2^(s - m) goes in place over S columns
-        // [16k, 16k + 16), which this thread has already read. If some row's max grows by
-        // more than 2^8 (always on the first tile of a segment), finish the tile's max over
-        // the remaining chunks, rescale O and the P chunks already written, and go on.
-        float lsum = 0.f;
-        int k = 0;
-        bool grew = false;
-#pragma unroll 1
-        for (; k < nchunks; ++k) {
-          uint32_t r[32];
-          ptx::tmem_ld32(ts + 32 * k, r);
-          ptx::tmem_ld_wait(r);
-          const uint32_t vm = chunk_mask(k);
-          if (__any_sync(0xffffffffu, chunk_max(r, vm) > m_used + 8.f)) {
-            grew = true;
-            break;
+        // (cos, sin) of the 2B response positions, over the tail K and V area (2B <= 64:
+        // at most 32 KB); the tail rows are stored once every read of the table is done.
+        // Rows are 66 float2 apart where that fits (16 bytes of padding: threads reading
+        // different positions' rows then hit different banks), else 64. Thread t fills pair
+        // t % 64 of the slots t / 64, t / 64 + 2, ... (the slot is warp-uniform).
+        float2* rtab = reinterpret_cast<float2*>(tailk);
+        const int tstride = twoB * 66 * 8 <= (int)(2 * kTailKV) ? 66 : 64;
+        {
+          const int d = tid & 63;
+          const float c_hi = a.rope.c_hi[d], c_lo = a.rope.c_lo[d];
+          for (int sidx = tid >> 6; sidx < twoB; sidx += 2) {
+            const int ps = __shfl_sync(0xffffffffu, sidx < 32 ? pos_lo : pos_hi, sidx & 31);
+            float sn, cs;
+            rope_sincos_fast(ps, c_hi, c_lo, &sn, &cs);
+            rtab[sidx * tstride + d] = make_float2(cs, sn);
           }
-          uint32_t pk[16];
-          lsum += chunk_exp(r, vm, m_used == -INFINITY ? 0.f : m_used, pk);
-          ptx::tmem_st16(ts + 16 * k, pk);
         }
-        if (grew) {
-          float mt = -INFINITY;
-#pragma unroll 1
-          for (int kk = k; kk < nchunks; ++kk) {
-            uint32_t r[32];
-            ptx::tmem_ld32(ts + 32 * kk, r);
-            ptx::tmem_ld_wait(r);
-            mt = fmaxf(mt, chunk_max(r, chunk_mask(kk)));
-          }
-          const float m_new = fmaxf(m_used, mt);
-          const float alpha = m_used == -INFINITY ? 0.f : ptx::ex2(m_used - m_new);
-          if (j != jfirst) {  // O holds P V of earlier tiles: rescale once the last P V landed
-            const uint32_t jp = j - 1;
-            ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jp & 1)), (jp >> 1) & 1, a.dev_err));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            l *= alpha;
-            const uint32_t to = tmem + lane_off + kTmemO;
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk) {
-              uint32_t o[32];
-              ptx::tmem_ld32(to + 32 * kk, o);
-              ptx::tmem_ld_wait(o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(to + 32 * kk, o);
+        // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
+        uint32_t vis0 = 0, vis1 = 0;
+        if (has_tail) {
+          const uint32_t own_lo = __shfl_sync(0xffffffffu, lab_lo, s_slot & 31);
+          const uint32_t own_hi = __shfl_sync(0xffffffffu, lab_hi, s_slot & 31);
+          const int th = row_threshold((uint8_t)(s_slot < 32 ? own_lo : own_hi));
+          for (int k = 0; k < twoB; ++k) {
+            const uint32_t lk = __shfl_sync(0xffffffffu, k < 32 ? lab_lo : lab_hi, k & 31);
+            if (response_key_visible((uint8_t)lk, th)) {
+              if (k < 32)
+                vis0 |= 1u << k;
+              else
+                vis1 |= 1u << (k - 32);
             }
           }
-          lsum *= alpha;
-#pragma unroll 1
-          for (int kk = 0; kk < k; ++kk) {  // P chunks already written with the old max
-            uint32_t pk[16];
-            ptx::tmem_ld16(ts + 16 * kk, pk);
-            ptx::tmem_ld16_wait(pk);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(bf16_lo(pk[e]) * alpha, bf16_hi(pk[e]) * alpha);
-            ptx::tmem_st16(ts + 16 * kk, pk);
+          if (!real) {
+            vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
+            vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
           }
-          m_used = m_new;
-          const float msafe = m_used == -INFINITY ? 0.f : m_used;
+        }
+        ptx::named_bar_sync(1, 128);
+        if (warp_active) {
+          if (real) {
+            rope_row(v, rtab + s_slot * tstride, a.scale_log2);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+          }
+          // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
+          tmem_st_row(tmem + lane_off + kTmemQ, v);
+          ptx::tmem_st_wait();
+        } else if (tr.early && tr.row && tr.k) {
+          rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
+        }
+        if (!tr.early && has_tail) {
+          if (tr.row) {
+            load_row(v, trow);
+            if (tr.k) rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (!loads_signalled) {  // this prologue's rows have landed: the prompt stream may start
+          ptx::mbar_arrive(bar(kLoads));
+          loads_signalled = true;
+        }
+        ptx::named_bar_sync(1, 128);  // table reads done
+        if (tr.early) {
+          if (tr.row) store_row_sw(tr.k ? tailk : tailv, kTailHalf, tr.key, v);
+          // keys 2B .. 63 of both tail tiles are zero (the tail MMAs read 64 keys)
+          const uint4 z[16] = {};
+          for (int e = tid; e < 2 * (64 - twoB); e += 128) {
+            const int zk = twoB + e % (64 - twoB);
+            store_row_sw(e < 64 - twoB ? tailk : tailv, kTailHalf, zk, z);
+          }
+        } else if (has_tail) {
+          store_row_sw(tr.k ? tailk : tailv, kTailHalf, tr.key, v);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kQFull));
+        float m_used = -INFINITY, l = 0.f;
+        const uint32_t jfirst = j;
+        // The next segment's Q rows, tail rows and labels go into L2 a few tiles before this
+        // segment ends, so that its prologue does not wait behind the K/V stream in flight.
+        int pf_b = -1, pf_h = 0;  // next segment: request, kv head | has_tail << 16
+        {
+          SegIter nx = it;
+          nx.advance(a);
+          if (nx.next(a) && !nx.invalid) {
+            pf_b = nx.b;
+            pf_h = nx.h | (nx.has_tail ? 1 << 16 : 0);
+          }
+        }
+        const int pf_at = max(it.i0, it.i0 + it.n - kPrefetchAhead);
+        for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
+          const int buf = j & 1;
+          if (pf_b >= 0 && i == pf_at)
+            prefetch_prologue(a, pf_b, pf_h & 0xffff, pf_h >> 16, twoB, s_slot, g, real, rw, tid);
+          ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err, wait_ns));
+          if (!ok) break;
+          if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
+            ptx::mbar_arrive(bar(kPFull0 + buf));
+            continue;
+          }
+          ptx::tc_fence_after();
+          const uint32_t ts = tmem + lane_off + kTmemS0 + buf * 128;
+          const int nchunks = (i == 0) ? 2 : kKeys / 32;  // warp-uniform
+          const int nvalid = (i == 0) ? 0 : P - (i - 1) * kKeys;
+          // valid-column bits of 32-column chunk k
+          auto chunk_mask = [&](int k) -> uint32_t {
+            if (i == 0) return k == 0 ? vis0 : vis1;
+            const int n = nvalid - 32 * k;
+            return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+          };
+          // One pass in the common case: chunk k's P = 2^(s - m) goes in place over S columns
+          // [16k, 16k + 16), which this thread has already read. If some row's max grows by
+          // more than 2^8 (always on the first tile of a segment), finish the tile's max over
+          // the remaining chunks, rescale O and the P chunks already written, and go on.
+          float lsum = 0.f;
+          int k = 0;
+          bool grew = false;
 #pragma unroll 1
           for (; k < nchunks; ++k) {
-            uint32_t r[32], pk[16];
+            uint32_t r[32];
             ptx::tmem_ld32(ts + 32 * k, r);
             ptx::tmem_ld_wait(r);
-            lsum += chunk_exp(r, chunk_mask(k), msafe, pk);
+            const uint32_t vm = chunk_mask(k);
+            if (__any_sync(0xffffffffu, chunk_max(r, vm) > m_used + 8.f)) {
+              grew = true;
+              break;
+            }
+            uint32_t pk[16];
+            lsum += chunk_exp(r, vm, m_used == -INFINITY ? 0.f : m_used, pk);
             ptx::tmem_st16(ts + 16 * k, pk);
           }
-        }
-        l += lsum;
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kPFull0 + buf));
-      }
-      if (!ok) break;
-      // ---- epilogue: wait for the last P V, then O / l (or the partial)
-      const uint32_t jl = j - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if (warp_active) {
-        const uint32_t to = tmem + lane_off + kTmemO;
-        const int slot = 2 * blockIdx.x + (it.first ? 0 : 1);
-        const float inv = it.full ? 1.f / l : 1.f;
+          if (grew) {
+            float mt = -INFINITY;
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
-          uint32_t o[32];
-          ptx::tmem_ld32(to + 32 * k, o);
-          ptx::tmem_ld_wait(o);
-          if (!real) continue;
-          if (it.full) {
-            uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + 32 * k);
+            for (int kk = k; kk < nchunks; ++kk) {
+              uint32_t r[32];
+              ptx::tmem_ld32(ts + 32 * kk, r);
+              ptx::tmem_ld_wait(r);
+              mt = fmaxf(mt, chunk_max(r, chunk_mask(kk)));
+            }
+            const float m_new = fmaxf(m_used, mt);
+            const float alpha = m_used == -INFINITY ? 0.f : ptx::ex2(m_used - m_new);
+            if (j != jfirst) {  // O holds P V of earlier tiles: rescale it once the last P V landed
+              const uint32_t jp = j - 1;
+              ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jp & 1)), (jp >> 1) & 1,
+                                                    a.dev_err, wait_ns));
+              if (!ok) break;
+              ptx::tc_fence_after();
+              l *= alpha;
+#pragma unroll 1
+              for (int kk = 0; kk < 4; ++kk) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tmem_o + 32 * kk, o);
+                ptx::tmem_ld_wait(o);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pack_bf16(__uint_as_float(o[8 * c]) * inv, __uint_as_float(o[8 * c + 1]) * inv),
-                                  pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
-                                  pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
-                                  pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(a.ws_o + ((size_t)slot * kBlockRows + row) * kD + 32 * k);
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                ptx::tmem_st32(tmem_o + 32 * kk, o);
+              }
+            }
+            lsum *= alpha;
+#pragma unroll 1
+            for (int kk = 0; kk < k; ++kk) {  // P chunks already written with the old max
+              uint32_t pk[16];
+              ptx::tmem_ld16(ts + 16 * kk, pk);
+              ptx::tmem_ld16_wait(pk);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                                   __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+              for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(bf16_lo(pk[e]) * alpha, bf16_hi(pk[e]) * alpha);
+              ptx::tmem_st16(ts + 16 * kk, pk);
+            }
+            m_used = m_new;
+            const float msafe = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll 1
+            for (; k < nchunks; ++k) {
+              uint32_t r[32], pk[16];
+              ptx::tmem_ld32(ts + 32 * k, r);
+              ptx::tmem_ld_wait(r);
+              lsum += chunk_exp(r, chunk_mask(k), msafe, pk);
+              ptx::tmem_st16(ts + 16 * k, pk);
+            }
+          }
+          l += lsum;
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kPFull0 + buf));
+        }
+        if (!ok) break;
+        // ---- epilogue: wait for the last P V, then O / l (or the partial)
+        const uint32_t jl = j - 1;
+        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err, wait_ns));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (warp_active) {
+          const float inv = it.full ? 1.f / l : 1.f;
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tmem_o + 32 * k, o);
+            ptx::tmem_ld_wait(o);
+            if (!real) continue;
+            if (it.full) {
+              uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + 32 * k);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dst[c] = make_uint4(pack_bf16(__uint_as_float(o[8 * c]) * inv, __uint_as_float(o[8 * c + 1]) * inv),
+                                    pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
+                                    pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
+                                    pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(a.ws_o + (slot * kBlockRows + row) * kD + 32 * k);
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                     __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+            }
+          }
+          if (real) {
+            if (it.full) {
+              if (a.lse) a.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994530942f;
+            } else {
+              a.ws_ml[slot * kBlockRows + row] = make_float2(m_used, l);
+            }
           }
         }
-        if (real) {
-          if (it.full) {
-            if (a.lse) a.lse[orow] = (m_used + __log2f(l)) * 0.69314718055994530942f;
-          } else {
-            a.ws_ml[(size_t)slot * kBlockRows + row] = make_float2(m_used, l);
-          }
-        }
-      }
-      ptx::tc_fence_before();
+        ptx::tc_fence_before();
+      } while (false);
+      if (!ok) mark_unfinished(a, it, real, orow, slot, row);  // this segment stopped part-way
       it.advance(a);
+    }
+    if (aborted) {  // the segment reached and every later one of the range are unfinished
+      do {
+        if (!it.full && it.i0 == 0 && !it.invalid) {
+          desc.b = it.b;
+          desc.h = it.h;
+          desc.c_last = (int)((it.pend * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
+          desc.piece0 = it.first ? 0 : 1;
+        }
+        const size_t orow = ((size_t)it.b * twoB + s_slot) * a.Hq + (size_t)it.h * a.G + g;
+        mark_unfinished(a, it, real, orow, part_slot(blockIdx.x, it.first ? 0 : 1), row);
+        it.advance(a);
+      } while (it.next(a));
     }
     if (tid == 0) a.ws_desc[blockIdx.x] = desc;
     if (!loads_signalled) ptx::mbar_arrive(bar(kLoads));  // no prologue ran: release the producer
@@ -1065,12 +1130,11 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (cl > 1) ptx::cluster_sync_all();  // no CTA leaves while its peer may still signal it
 }
 
-// Merges the pieces of every pair split between CTAs. Block (c, y) reads CTA c's merge
-// descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that pair:
-// one thread per (row, 4 output elements), so every load is independent.
+// Merges the pieces of every pair split between units. Block (c, y) reads CTA c's merge
+// descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that CTA's row
+// block of the pair: one thread per (row, 4 output elements), so every load is independent.
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the attention grid has completed
   const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
@@ -1084,24 +1148,23 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   if (row >= kBlockRows || prow >= a.R) return;
   const int64_t T = d.T;
   const int C = a.ctas;
-  const size_t stride = kBlockRows;
-  // pieces: unit vc (slot0) and every later non-empty unit up to c_last (its first slot),
-  // each in the CTA of the same row block
+  // pieces: unit vc (its piece0) and every later non-empty unit up to c_last (its first
+  // piece), each in the CTA of the same row block
   float mmax = -INFINITY;
 #pragma unroll 4
   for (int vcc = vc; vcc <= d.c_last; ++vcc) {
     if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
-    const int slot = (vcc == vc) ? d.slot0 : 2 * (vcc * cl + crank);
-    mmax = fmaxf(mmax, a.ws_ml[(size_t)slot * stride + row].x);
+    const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
+    mmax = fmaxf(mmax, a.ws_ml[slot * kBlockRows + row].x);
   }
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int vcc = vc; vcc <= d.c_last; ++vcc) {
     if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
-    const int slot = (vcc == vc) ? d.slot0 : 2 * (vcc * cl + crank);
-    const float2 ml = a.ws_ml[(size_t)slot * stride + row];
-    const float4 o = reinterpret_cast<const float4*>(a.ws_o + ((size_t)slot * stride + row) * kD)[quad];
+    const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
+    const float2 ml = a.ws_ml[slot * kBlockRows + row];
+    const float4 o = reinterpret_cast<const float4*>(a.ws_o + (slot * kBlockRows + row) * kD)[quad];
     const float w = exp2f(ml.x - mmax);
     L += w * ml.y;
     acc.x += w * o.x;
@@ -1168,12 +1231,26 @@ static bool encode_cache_map(CUtensorMap* map, const void* base, int layout, int
   return r == CUDA_SUCCESS;
 }
 
+// True when `ptr` is device memory of the current device `dev` (or managed memory): the
+// tensor maps read the cache through this GPU's own memory system only.
+static bool on_device(const void* ptr, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return false;
+  }
+  if (at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
 static int rows_per_pair(const simsd_attn_params* p) { return 2 * p->B * (p->Hq / p->Hkv); }
+// CTAs per schedule unit: two for pairs of more than 128 rows (one per 128-row block).
+static int ctas_per_unit(const simsd_attn_params* p) { return rows_per_pair(p) > 128 ? 2 : 1; }
 
 // Persistent grid: one CTA per SM; when every (request, kv head) pair fits on the SMs and
-// prompts are short, one CTA per pair instead (no pair is split, nothing to merge).
+// prompts are short, one unit per pair instead (no pair is split, nothing to merge).
 // (With `cl` CTAs per unit: at most SMs / cl units.)
-static int grid_ctas(const simsd_attn_params* p, int cl = 1) {
+static int grid_units(const simsd_attn_params* p, int cl) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 148;
   sms /= cl;
@@ -1182,8 +1259,6 @@ static int grid_ctas(const simsd_attn_params* p, int cl = 1) {
   if (pairs > 0 && pairs <= sms && avg_tiles <= 64) return (int)pairs;
   return sms;
 }
-// CTAs per schedule unit: a cluster of two for pairs of more than 128 rows.
-static int cluster_size(const simsd_attn_params* p) { return rows_per_pair(p) > 128 ? 2 : 1; }
 
 struct WsLayout {
   size_t o, ml, desc, bytes;
@@ -1197,7 +1272,32 @@ static WsLayout ws_layout(int ctas) {
   return w;
 }
 
+// The dynamic shared memory attribute is set once per device.
+static std::mutex g_attr_mutex;
+static bool g_attr_done[64];
+
+static simsd_status set_smem_attr(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (dev >= 0 && dev < 64 && g_attr_done[dev]) return SIMSD_OK;
+  const cudaError_t e = cudaFuncSetAttribute(attn_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)r128::kSmemBytes);
+  if (e != cudaSuccess) {
+    record_cuda_error("cudaFuncSetAttribute", e);
+    return SIMSD_ERR_CUDA;
+  }
+  if (dev >= 0 && dev < 64) g_attr_done[dev] = true;
+  return SIMSD_OK;
+}
+
 static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int dev = 0;
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) {
+    record_cuda_error("cudaGetDevice", de);
+    return SIMSD_ERR_CUDA;
+  }
+  if (p->cache_tokens > 0 && (!on_device(p->k_cache, dev) || !on_device(p->v_cache, dev)))
+    return SIMSD_ERR_INVALID_ARG;
   TcArgs a;
   a.batch = p->batch;
   a.B = p->B;
@@ -1205,11 +1305,11 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.Hkv = p->Hkv;
   a.G = p->Hq / p->Hkv;
   a.R = rows_per_pair(p);
-  a.tile_keys = r128::kKeys;
+  a.cl = ctas_per_unit(p);
   a.seg_cost = seg_cost_tiles(2 * p->B);
-  a.cl = cluster_size(p);
-  a.ctas = grid_ctas(p, a.cl);
+  a.ctas = grid_units(p, a.cl);
   a.layout = (int)p->cache_layout;
+  a.wait_ns = p->wait_limit_ns > 0 ? p->wait_limit_ns : kDefaultWaitNs;
   a.q = (const __nv_bfloat16*)p->q;
   a.k_resp = (const __nv_bfloat16*)p->k_resp;
   a.v_resp = (const __nv_bfloat16*)p->v_resp;
@@ -1232,38 +1332,20 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   CUtensorMap tmk, tmv;
   const void* kbase = p->cache_tokens > 0 ? p->k_cache : p->k_resp;  // any valid address
   const void* vbase = p->cache_tokens > 0 ? p->v_cache : p->v_resp;
-  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv, a.tile_keys) ||
-      !encode_cache_map(&tmv, vbase, a.layout, p->cache_tokens, p->Hkv, a.tile_keys)) {
+  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv, kKeys) ||
+      !encode_cache_map(&tmv, vbase, a.layout, p->cache_tokens, p->Hkv, kKeys)) {
     record_cuda_error("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     return SIMSD_ERR_CUDA;
   }
-
-  const int threads = r128::kThreads;
-  const uint32_t smem_bytes = r128::kSmemBytes;
-  static bool attr_done[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(attn_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem_bytes);
-    if (e != cudaSuccess) {
-      record_cuda_error("cudaFuncSetAttribute", e);
-      return SIMSD_ERR_CUDA;
-    }
-    attr_done[dev] = true;
-  }
+  const simsd_status ast = set_smem_attr(dev);
+  if (ast != SIMSD_OK) return ast;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;  // pairs of more than 128 rows: clusters of 2
-  at[0].val.clusterDim.x = (unsigned)a.cl;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
-  cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.blockDim = dim3((unsigned)r128::kThreads);
+  cfg.dynamicSmemBytes = r128::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = at;
-  cfg.numAttrs = a.cl > 1 ? 1 : 0;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc128_kernel, tmk, tmv, a);
   if (le == cudaSuccess) le = cudaGetLastError();
   if (le != cudaSuccess) {
@@ -1273,7 +1355,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
       snprintf(what, sizeof(what),
                "attention kernel launch (threads %d, regs %d, max threads %d, dyn smem %u, "
                "max dyn smem %d, static smem %zu, local %zu)",
-               threads, fa.numRegs, fa.maxThreadsPerBlock, smem_bytes,
+               r128::kThreads, fa.numRegs, fa.maxThreadsPerBlock, r128::kSmemBytes,
                fa.maxDynamicSharedSizeBytes, fa.sharedSizeBytes, fa.localSizeBytes);
     record_cuda_error(what, le);
     return SIMSD_ERR_CUDA;
@@ -1310,8 +1392,8 @@ bool attn_tc_supported(const simsd_attn_params* p) {
 }
 
 size_t attn_tc_workspace(const simsd_attn_params* p) {
-  const int cl = tc::cluster_size(p);
-  return tc::ws_layout(tc::grid_ctas(p, cl) * cl).bytes;
+  const int cl = tc::ctas_per_unit(p);
+  return tc::ws_layout(tc::grid_units(p, cl) * cl).bytes;
 }
 
 simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_bytes,
@@ -1322,7 +1404,7 @@ simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_byte
     return SIMSD_ERR_UNSUPPORTED;
   if (p->cache_tokens > 0 && ((((uintptr_t)p->k_cache) | ((uintptr_t)p->v_cache)) & mask))
     return SIMSD_ERR_UNSUPPORTED;
-  // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: a cluster of two
+  // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: two CTAs
   return tc::launch(p, ws, ws_bytes, stream);
 }
 

@@ -94,7 +94,9 @@ const char* simsd_status_str(simsd_status s);
  *   0.1.0  layout, verify attention, acceptance (+ workspace queries, allocation-free entry)
  *   0.2.0  adds simsd_accept_coupled, simsd_accept_ex / simsd_accept_coupled_ex (bf16
  *          logits), simsd_expected_prefix (+ workspace), simsd_build_layout_ex (flags);
- *          every 0.1.0 call is unchanged */
+ *          every 0.1.0 call is unchanged
+ *   0.3.0  simsd_attn_params gains wait_limit_ns (its last field; zero keeps the 0.2.0
+ *          behaviour, so callers that zero-initialise the struct need no other change) */
 int simsd_version(void);
 
 /* Text of the CUDA runtime/driver error behind the most recent SIMSD_ERR_CUDA returned
@@ -157,6 +159,8 @@ simsd_status simsd_build_layout_ex(const int32_t* tau, const int32_t* prompt_len
  *
  * BF16 path: tcgen05 tensor-core kernel (fp32 accumulation), split over the prompt keys
  * and merged; FP32 path: CUDA-core kernel in fp32 throughout.
+ * Zero-initialise the struct (e.g. `simsd_attn_params p = {0};`) and set every field
+ * below; fields added by later versions then keep their default.
  * --------------------------------------------------------------------------------- */
 typedef struct {
   simsd_dtype dtype;        /* element type of q, k_resp, v_resp, k_cache, v_cache, out */
@@ -177,10 +181,18 @@ typedef struct {
   void* out;                /* [batch, 2B, Hq, D] output, dtype as the inputs           */
   float* lse;               /* fp32 [batch, 2B, Hq] output, or NULL                     */
   uint32_t* dev_err;        /* device error word                                        */
+  uint64_t wait_limit_ns;   /* bound of every device-side wait of the BF16 kernel, in
+                               ns; 0 selects 2 s (see below)                            */
 } simsd_attn_params;
 /* Data errors: a request with labels 0xFF or P_r < 0 (bit SIMSD_DEVERR_PROMPT_LEN for
- * the latter) gets zero output rows and lse = -inf. Host errors: SIMSD_ERR_INVALID_ARG
- * (null pointer, Hq % Hkv != 0, B outside 1..32, negative sizes),
+ * the latter) gets zero output rows and lse = -inf.
+ * Bounded waits: the BF16 kernel's warps wait on one another (copies, MMAs, softmax). A
+ * wait that makes no progress for wait_limit_ns (0: 2 s, far beyond any legitimate wait)
+ * sets SIMSD_DEVERR_TIMEOUT; the kernel then stops early and returns (it never hangs and
+ * never traps): every output row it did not finish is NaN (lse NaN), the rows it finished
+ * are valid. The context stays usable and the next call runs normally.
+ * Host errors: SIMSD_ERR_INVALID_ARG (null pointer, Hq % Hkv != 0, B outside 1..32,
+ * negative sizes, a BF16 prompt cache that is not device memory of the current device),
  * SIMSD_ERR_UNSUPPORTED (D not 64/128; BF16 needs D = 128 and 2B*G <= 256 on this
  * build; cache rows or pointers not 16-byte aligned), SIMSD_ERR_WORKSPACE. */
 
@@ -336,10 +348,13 @@ simsd_status simsd_expected_prefix(const void* draft_logits, simsd_dtype logit_d
  * (no cudaMalloc, cudaFree or allocating library routine): its scratch is a fixed
  * 1 MiB device array inside the library, present on every device that loads the library
  * until the process exits.
- *   - Arguments, outputs, error bits and sentinels: exactly as simsd_accept.
+ *   - Arguments, outputs, error bits, sentinels and status codes: exactly as
+ *     simsd_accept (the same argument checks run first, in the same order).
  *   - The first call on each device looks up that array's device address (a runtime
  *     query, with that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture. A device reset replaces the device's context, and with it the
+ *     array's address: the next call notices the new context and looks the address up
+ *     again (make it, too, outside any stream capture).
  *   - Sizes whose scratch would exceed the array (see simsd_accept_noalloc_max_scratch;
  *     simsd_accept_workspace(batch, B, gamma, V) must not exceed it) return
  *     SIMSD_ERR_WORKSPACE and launch nothing.

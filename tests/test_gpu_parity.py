@@ -82,7 +82,7 @@ def test_layout_physical_positions_bit_exact(name):
     assert int(err.item()) == re_ != 0
 
 
-@pytest.mark.parametrize("case", ["fp32", "bf16", "bf16_cluster"])
+@pytest.mark.parametrize("case", ["fp32", "bf16", "bf16_two_ctas"])
 def test_attention_physical_positions_negative_control(case):
     """Attention on the ablation layout against the oracle on the same positions (within
     the usual tolerance), and the negative control: the prediction rows move away from the
@@ -91,7 +91,7 @@ def test_attention_physical_positions_negative_control(case):
         w = W["tiny_fp32"].with_(batch=3, B=6, gamma=6)
         plen = [32, 5, 70]
     else:
-        w = MEDIUM.with_(B=32, gamma=32, Hq=6, Hkv=2) if case == "bf16_cluster" else MEDIUM
+        w = MEDIUM.with_(B=32, gamma=32, Hq=6, Hkv=2) if case == "bf16_two_ctas" else MEDIUM
         plen = [0, 61, 128, 1000 + 37]
     inputs, meta = H.make_case(w, seed=13, prompt_len=plen)
     aligned = _step(w, inputs, meta)
@@ -219,9 +219,9 @@ def test_attention_bf16_ragged_tiles_full_compare(layout, B):
 
 
 @pytest.mark.parametrize("Hq,Hkv,B", [(6, 2, 32), (10, 2, 13), (8, 1, 9)])
-def test_attention_bf16_cluster_partial_second_block(Hq, Hkv, B):
-    # 2B*G rows per (request, kv-head) pair between 129 and 255: the pair runs on a
-    # cluster of two CTAs whose second CTA holds a partial row block (64, 2 and 16 rows)
+def test_attention_bf16_two_ctas_partial_second_block(Hq, Hkv, B):
+    # 2B*G rows per (request, kv-head) pair between 129 and 255: the pair runs on two CTAs
+    # whose second one holds a partial row block (64, 2 and 16 rows)
     w = MEDIUM.with_(Hq=Hq, Hkv=Hkv, B=B, gamma=B)
     assert 128 < 2 * B * (Hq // Hkv) < 256
     inputs, meta = H.make_case(w, seed=100 + B, prompt_len=[0, 61, 128, 1000 + 37])
@@ -297,6 +297,53 @@ def test_attention_invalid_request_rows_are_zero():
     assert torch.count_nonzero(st.out[1].float()) == 0
     assert torch.isneginf(st.lse[1]).all()
     _attention_parity(w, inputs, meta, st, requests=[0, 2, 3])
+
+
+@pytest.mark.parametrize("case", ["one_cta_per_pair", "split_pairs_two_ctas"])
+def test_attention_bounded_wait_gives_up_and_next_call_is_exact(case):
+    """The kernel's warps wait on one another (copies, MMAs, softmax), each wait bounded by
+    wait_limit_ns. A limit of 1 ns makes those waits run out (the pipeline takes microseconds),
+    which exercises the give-up path without hanging anything: the call returns, the error
+    word carries SIMSD_DEVERR_TIMEOUT, every output row is either the row a normal call
+    produces (bit for bit: same schedule, same arithmetic) or all NaN, and the next call with
+    the default limit, on the same context, reproduces the normal output."""
+    pkg = _pkg()
+    if case == "one_cta_per_pair":
+        w = MEDIUM.with_(B=8, gamma=8)
+        plen = [0, 61, 128, 1000 + 37]
+    else:  # 192 rows per pair (two CTAs each) and long prompts: pairs split across units
+        w = MEDIUM.with_(Hq=6, Hkv=2, B=32, gamma=32)
+        plen = [20000, 61, 128, 9000]
+    inputs, meta = H.make_case(w, seed=21, prompt_len=plen)
+    st = _step(w, inputs, meta)
+    assert int(st.dev_err.item()) == 0
+    _attention_parity(w, inputs, meta, st)
+    ref_out, ref_lse = st.out.clone(), st.lse.clone()
+
+    st.params.wait_limit_ns = 1
+    st.dev_err.zero_()
+    st.out.fill_(7.0)
+    st.lse.fill_(7.0)
+    st.attention()
+    torch.cuda.synchronize()
+    err = int(st.dev_err.item())
+    assert err & pkg.DEVERR_TIMEOUT, err
+    out = st.out.float().reshape(-1, w.D)
+    ref = ref_out.float().reshape(-1, w.D)
+    nan_rows = torch.isnan(out).all(dim=1)
+    same_rows = (out == ref).all(dim=1)
+    assert bool((nan_rows | same_rows).all())
+    assert int(nan_rows.sum()) > 0
+    lse, rlse = st.lse.reshape(-1), ref_lse.reshape(-1)
+    assert bool((torch.isnan(lse) | (lse == rlse)).all())
+    assert bool((torch.isnan(lse) == nan_rows).all())
+
+    st.params.wait_limit_ns = 0   # the default limit: a normal call on the same context
+    st.dev_err.zero_()
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.dev_err.item()) == 0
+    assert torch.equal(st.out, ref_out) and torch.equal(st.lse, ref_lse)
 
 
 def test_masked_slots_do_not_influence_prediction_rows():

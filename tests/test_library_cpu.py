@@ -51,7 +51,7 @@ def test_status_strings_and_version(lib):
     assert pkg.simsd_status_str(0) == "SIMSD_OK"
     assert pkg.simsd_status_str(3) == "SIMSD_ERR_WORKSPACE"
     assert pkg.simsd_status_str(99) == "SIMSD_ERR_UNKNOWN"
-    assert pkg.simsd_version() == 200
+    assert pkg.simsd_version() == 300
 
 
 def test_host_argument_errors_return_status(lib):
@@ -116,3 +116,20 @@ def test_attention_parameter_checks(lib):
     assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1
     p.B, p.rope_theta = 4, 0.0
     assert lib.simsd_verify_attention(ctypes.byref(p), None, 0, None) == 1
+
+
+def test_noalloc_accept_returns_the_status_of_accept(lib):
+    # the allocation-free entry runs simsd_accept's argument checks first and in the same
+    # order, so a bad argument gives the same status even for sizes beyond its fixed scratch
+    big = [1 << 16, 32, 32, 1000]   # batch, B, gamma, V: a plan larger than the fixed array
+    for temperature in (float("nan"), -1.0):
+        a = [None] * 4 + big + [temperature, 0, 0] + [None] * 4 + [None, 0, None, None]
+        n = [None] * 4 + big + [temperature, 0, 0] + [None] * 4 + [None, None]
+        assert lib.simsd_accept(*a) == 1
+        assert lib.simsd_accept_noalloc(*n) == 1
+    n = [None] * 4 + [0, 4, 4, 100, 1.0, 0, 0] + [None] * 4 + [None, None]
+    assert lib.simsd_accept_noalloc(*n) == 0      # batch 0: nothing to do
+    n[4] = 2
+    assert lib.simsd_accept_noalloc(*n) == 1      # null pointers
+    n[6] = 5
+    assert lib.simsd_accept_noalloc(*n) == 1      # gamma > B
