@@ -2,8 +2,9 @@
 """Benchmark of the SimSD verification step on GB300.
 
 One step = simsd_build_layout + simsd_verify_attention (one layer) + simsd_accept over one
-batch of synthetic input of a named workload (default: the 8B-class GQA layer, batch 16,
-32 q / 8 kv heads, D 128, prompt 512, block 4, vocab 151936). Prints ONE JSON line.
+batch of synthetic input of a named workload (default: ragged serving, batch 256, prompt
+lengths uniform in [128, 8192], 32 q / 8 kv heads, D 128, block 8, vocab 151936, the
+largest workload that fits one GPU). Prints ONE JSON line.
 
 Metric: verified candidate tokens/s = batch * gamma / step time.
   value      device-resident inputs; K steps replayed back to back (one CUDA graph per
@@ -14,7 +15,11 @@ Metric: verified candidate tokens/s = batch * gamma / step time.
   roofline   the call with the most algorithmic bytes, timed on its own (CUDA events on
              its launch stream, graph replays over the rotating sets).
   cpu_baseline  the fp64 oracle on the host cores (rank 0, N = 1), bounded sample.
+  clocks     SM clock, power and clock-event reasons sampled through NVML during the timed
+             steps and the per-call timing replays.
 --impl reference times the oracle itself (the CPU reference implementation of the step).
+Under torchrun (N ranks) every rank takes one shard of a global batch of N x batch requests,
+split longest-prompt-first so that the ranks' attention work is balanced.
 """
 from __future__ import annotations
 
@@ -43,7 +48,9 @@ def _args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa8b_bf16")
+    ap.add_argument("--workload", default="ragged_bf16")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiler captures)")
     ap.add_argument("--cache-layout", choices=["NHD", "HND"], default="NHD")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -68,6 +75,8 @@ def _args():
 def _overrides(args):
     """Workload fields and the verification mode the command line changes."""
     ov = {"coupled": bool(getattr(args, "coupled", False))}
+    if getattr(args, "batch", None) is not None:
+        ov["batch"] = args.batch
     if args.temperature is not None:
         ov["temperature"] = args.temperature
     if getattr(args, "logit_dtype", None) is not None:
@@ -204,7 +213,8 @@ def _config(w, args, launch):
            "D": w.D, "gamma": w.gamma, "V": w.V, "rope_theta": w.rope_theta,
            "temperature": w.temperature, "logit_dtype": w.logit_dtype,
            "cache_layout": args.cache_layout,
-           "parallelism": f"dp{args.gpus} (independent requests per rank)"}
+           "parallelism": (f"dp{args.gpus} (one global batch of {args.gpus} x {w.batch} requests, "
+                           f"split longest prompt first)" if args.gpus > 1 else "dp1")}
     if w.prompt_len is not None:
         cfg["P"] = w.prompt_len
     else:
@@ -266,7 +276,7 @@ class ClockSampler:
                     reasons.add(n)
         os.unlink(self.path)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_max": max(power) if power else None}
@@ -343,25 +353,25 @@ class NvmlSampler:
     def timed_begin(self):
         self._switch = sys.getswitchinterval()
         sys.setswitchinterval(1e-4)   # let the poller run while the launch loop holds the GIL
-        if self.lib is None:
-            self.smi.start()
+        if self.lib is None and self.smi.proc is None:
+            self.smi.start()          # nvidia-smi runs from the first timed window to stop()
         self.active.set()
 
     def timed_end(self):
         self.active.clear()
         sys.setswitchinterval(self._switch)
-        if self.lib is None:
-            self.smi_result = self.smi.stop()
 
     def stop(self):
         if self.lib is None:
-            return getattr(self, "smi_result", {"sm_mhz": None, "sm_max_mhz": None,
-                                                "reasons": ["no samples"]})
+            if self.smi.proc is None:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                        "samples": 0}
+            return self.smi.stop()
         self.done.set()
         self.thread.join(timeout=2)
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
-                    "source": "nvml"}
+                    "samples": 0, "source": "nvml"}
         reasons = sorted({n for _, _, r in self.samples for bit, n in self.REASONS.items()
                           if r & bit})
         power = [p for _, p, _ in self.samples if p is not None]
@@ -369,7 +379,7 @@ class NvmlSampler:
                 "sm_max_mhz": self.max_mhz, "reasons": reasons,
                 "samples": len(self.samples), "sm_mhz_min": min(m for m, _, _ in self.samples),
                 "power_w_max": max(power) if power else None,
-                "source": "nvml, timed region only"}
+                "source": "nvml, timed steps and per-call timing replays"}
 
 
 def _traffic(workload, call):
@@ -405,16 +415,28 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _make_sets(w, args, device, n_sets, rank, first=0):
+def _make_sets(w, args, device, n_sets, rank, first=0, world=1):
+    """Input sets of this rank. With world > 1 each set is one shard of a global batch of
+    world x batch requests (prompt lengths and step labels drawn once for the whole batch,
+    then split longest prompt first across the ranks); the rank's tensors are drawn from
+    its own seed. Each set carries its local workload (batch = the shard's size)."""
     import torch
     import workloads
+    from diffusion_speculative_verify_gb300.sharding import shard_requests
     sets = []
     for i in range(first, first + n_sets):
         seed = w.seed + 1000 * rank + i
-        lay = workloads.make_layout_inputs(w, seed=seed)
-        att = workloads.make_attention_inputs(w, lay["prompt_len"], seed=seed, device=device,
+        if world > 1:
+            glay = workloads.make_layout_inputs(w.with_(batch=w.batch * world), seed=w.seed + i)
+            mine = torch.tensor(shard_requests(glay["prompt_len"].tolist(), world)[rank])
+            lay = {"tau": glay["tau"][mine], "prompt_len": glay["prompt_len"][mine]}
+            wl = w.with_(batch=len(mine))
+        else:
+            lay = workloads.make_layout_inputs(w, seed=seed)
+            wl = w
+        att = workloads.make_attention_inputs(wl, lay["prompt_len"], seed=seed, device=device,
                                               cache_layout=args.cache_layout)
-        acc = workloads.make_accept_inputs(w, seed=seed, device=device)
+        acc = workloads.make_accept_inputs(wl, seed=seed, device=device)
         sets.append({
             "tau": lay["tau"].to(device), "prompt_len": lay["prompt_len"].to(device),
             "q": att["q"], "k_resp": att["k_resp"], "v_resp": att["v_resp"],
@@ -422,7 +444,7 @@ def _make_sets(w, args, device, n_sets, rank, first=0):
             "cache_start": att["cache_offsets"][:-1].contiguous().to(device),
             "target_logits": acc["target_logits"], "draft_logits": acc["draft_logits"],
             "draft_tokens": acc["draft_tokens"], "_seed": acc["philox_seed"],
-            "_prompt_len_cpu": lay["prompt_len"]})
+            "_prompt_len_cpu": lay["prompt_len"], "_w": wl})
     return sets
 
 
@@ -464,7 +486,7 @@ def run_ours(args):
     probe = workloads.make_layout_inputs(w)
     alg = workloads.algorithmic_bytes(w, probe["prompt_len"])
     n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / max(1, alg["total_bytes"]))))
-    sets = _make_sets(w, args, device, n_sets, rank)
+    sets = _make_sets(w, args, device, n_sets, rank, world=world)
     khat_mode = {None: None, "margin": pkg.KHAT_MARGIN, "entropy": pkg.KHAT_ENTROPY}[args.khat]
 
     def make_step(s):
@@ -475,7 +497,7 @@ def run_ours(args):
                               aligned_rope=not args.physical_positions)
 
     steps = [make_step(s) for s in sets]
-    algs = [workloads.algorithmic_bytes(w, s["_prompt_len_cpu"], target_only=args.coupled,
+    algs = [workloads.algorithmic_bytes(s["_w"], s["_prompt_len_cpu"], target_only=args.coupled,
                                         with_khat=khat_mode is not None) for s in sets]
     stream = torch.cuda.Stream(device=device)
     torch.cuda.synchronize()
@@ -546,9 +568,11 @@ def run_ours(args):
     per_call = {}
     if use_graph:
         reps = max(args.steps, 3 * n_sets)
+        clocks.timed_begin()
         with torch.cuda.stream(stream):
             for name, gl in g_calls.items():
                 per_call[name] = _time_graphs(gl, reps, stream) / reps
+        clocks.timed_end()
     mean_alg = {k: statistics.mean(a[k] for a in algs)
                 for k in ("attn_bytes", "accept_bytes", "khat_bytes", "total_bytes", "attn_flops")}
     peak, peak_kind = _peaks()
@@ -584,7 +608,7 @@ def run_ours(args):
     if not args.no_e2e:
         e_sets, e_steps = sets, steps
         if len(sets) < 2:  # a second device set, so that the end-to-end steps can overlap
-            extra = _make_sets(w, args, device, 1, rank, first=len(sets))
+            extra = _make_sets(w, args, device, 1, rank, first=len(sets), world=world)
             e_sets, e_steps = sets + extra, steps + [make_step(extra[0])]
         e2e = _e2e(w, e_sets, e_steps, args, stream, world, device)
     clk = clocks.stop()

@@ -31,3 +31,27 @@ def test_reference_arm_prints_one_contract_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_multi_rank_sets_are_shards_of_one_global_batch():
+    """Under torchrun each rank's input set is its longest-prompt-first shard of one global
+    batch of world x batch requests: together the shards hold every request's prompt length
+    and step labels once, and each set's workload has the shard's batch size."""
+    import argparse
+    import sys as _sys
+    _sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    w = workloads.WORKLOADS["ragged_bf16"].with_(batch=6, Hq=4, Hkv=1, V=64)
+    args = argparse.Namespace(cache_layout="NHD")
+    world = 2
+    glay = workloads.make_layout_inputs(w.with_(batch=w.batch * world), seed=w.seed)
+    plens, taus = [], []
+    for rank in range(world):
+        (s,) = bench._make_sets(w, args, "cpu", 1, rank, world=world)
+        assert s["_w"].batch == s["prompt_len"].numel() == s["q"].shape[0]
+        assert int(s["k_cache"].shape[0]) == int(s["prompt_len"].sum())
+        plens += s["prompt_len"].tolist()
+        taus += [tuple(t) for t in s["tau"].tolist()]
+    assert sorted(plens) == sorted(glay["prompt_len"].tolist())
+    assert sorted(taus) == sorted(tuple(t) for t in glay["tau"].tolist())
