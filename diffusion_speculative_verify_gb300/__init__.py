@@ -10,7 +10,7 @@ from __future__ import annotations
 import torch
 
 from ._binding import (CACHE_HND, CACHE_NHD, DEVERR_PROMPT_LEN, DEVERR_TAU,  # noqa: F401
-                       DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, KHAT_ENTROPY, KHAT_MARGIN,
+                       DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_TOKEN, EXPORTED, KHAT_ENTROPY, KHAT_MARGIN,
                        LAYOUT_PHYSICAL_POSITIONS, LIB_PATH, AttnParams,
                        SimsdError, load_library, make_attn_params, simsd_accept, simsd_accept_coupled,
                        simsd_accept_coupled_ex, simsd_accept_ex, simsd_accept_noalloc, simsd_accept_noalloc_max_scratch,

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libsimsd.so")
 SIMSD_OK = 0
 STATUS_NAMES = {0: "SIMSD_OK", 1: "SIMSD_ERR_INVALID_ARG", 2: "SIMSD_ERR_UNSUPPORTED",
                 3: "SIMSD_ERR_WORKSPACE", 4: "SIMSD_ERR_CUDA", 5: "SIMSD_ERR_TIMEOUT"}
-DEVERR_TAU, DEVERR_PROMPT_LEN, DEVERR_TOKEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_TAU, DEVERR_PROMPT_LEN, DEVERR_TOKEN, DEVERR_TIMEOUT, DEVERR_BOUNDS = 1, 2, 4, 8, 16
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 KHAT_MARGIN, KHAT_ENTROPY = 0, 1
 CACHE_NHD, CACHE_HND = 0, 1

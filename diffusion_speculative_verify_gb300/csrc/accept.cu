@@ -37,6 +37,8 @@ struct AcceptWs {
   float2* stats;                // [batch][gamma][2][nchunk]  (max, sum exp) per chunk
   unsigned long long* winners;  // [batch][2]  race winners: residual, target (0: no positive residual)
   unsigned* ticket;             // [batch]     CTAs of K3b finished
+  long long n_stats;            // entries of `stats` (checked build)
+  uint32_t* err;                // the call's error word
 };
 
 struct AcceptPlan {
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
   const long items = (long)batch * gamma * 2 * nchunk;
   if (blockIdx.x == 0) {  // scratch of K3b starts at zero on every call
     for (int i = threadIdx.x; i < batch; i += blockDim.x) {
+      if (!chk(2LL * i, 2, 2LL * batch, ws.err)) continue;
       ws.winners[2 * i] = 0ull;
       ws.winners[2 * i + 1] = 0ull;
       ws.ticket[i] = 0u;
@@ -151,12 +154,14 @@ __global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
     const int model = (int)(row & 1);
     const int step = (int)((row >> 1) % gamma);
     const int r = (int)((row >> 1) / gamma);
-    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
+    const bool lab_ok = chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, ws.err);
+    const uint8_t lb = lane < B && lab_ok ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
     const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
     float m = -INFINITY, sum = 0.f;
     const int c0 = chunk * plan.chunk_a;
     const int len = min(plan.chunk_a, V - c0);
-    if (hit && len > 0) {
+    if (hit && len > 0 &&
+        chk(((long long)r * B + (__ffs(hit) - 1)) * V + c0, len, (long long)batch * B * V, ws.err)) {
       const int k = __ffs(hit) - 1;
       const LT* rowp = (model ? draft : target) + ((size_t)r * B + k) * (size_t)V;
       if (vec_ok) {  // c0 is a multiple of 8: every 16-byte load is aligned
@@ -233,7 +238,8 @@ __global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(
       const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
       lse_merge(m, sum, m2, s2);
     }
-    if (lane == 0) ws.stats[item] = make_float2(m, sum);  // items enumerate [row][chunk]
+    if (lane == 0 && chk(item, 1, ws.n_stats, ws.err))
+      ws.stats[item] = make_float2(m, sum);  // items enumerate [row][chunk]
   }
 }
 
@@ -355,6 +361,12 @@ __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
   const int chunk = blockIdx.x % plan.nchunk_b;
   const int r = blockIdx.x / plan.nchunk_b;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // checked build: the request's labels, tokens, outputs, scratch and chunk statistics lie
+  // inside their arrays (block-uniform; else the block does nothing)
+  if (!chk(r, 1, batch, dev_err) || !chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, dev_err) ||
+      !chk((long long)r * B, B, (long long)batch * B, dev_err) ||
+      !chk((long long)r * gamma * 2 * plan.nchunk_a, (long long)gamma * 2 * plan.nchunk_a, ws.n_stats, dev_err))
+    return;
   const uint8_t* lab = labels + (size_t)r * 2 * B;
   const bool unit_T = (T == 1.f);
 
@@ -390,7 +402,7 @@ __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     }
     const bool tok_bad = perm && lane < gr_w && (x_w < 0 || x_w >= V);
     if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
-    if (!bad_w && lane < gr_w) {
+    if (!bad_w && lane < gr_w && chk(((long long)r * B + k_w) * V + x_w, 1, (long long)batch * B * V, dev_err)) {
       const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
       tx = scale_logit(LogitIO<LT>::ld1(target + rowoff), T, unit_T);
       dx = scale_logit(LogitIO<LT>::ld1(draft + rowoff), T, unit_T);
@@ -499,8 +511,9 @@ __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     const int c1 = min(V, c0 + plan.chunk_b);
     unsigned long long best_res = 0ull;
     const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
-    race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
-               1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
+    if (chk(((long long)r * B + k) * V + min(c0, V), c1 - min(c0, V), (long long)batch * B * V, dev_err))
+      race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
+                 1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
@@ -531,8 +544,9 @@ __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
     unsigned long long best = 0ull;
     const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
-    race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
-               1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
+    if (chk(((long long)r * B + k) * V, V, (long long)batch * B * V, dev_err))
+      race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
+                 1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -614,13 +628,15 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
     const long row = item / nchunk;
     const int step = (int)(row % gamma);
     const int r = (int)(row / gamma);
-    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
+    const bool lab_ok = chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, ws.err);
+    const uint8_t lb = lane < B && lab_ok ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
     const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
     float m = -INFINITY;
     int mi = kNoIndex;
     const int c0 = chunk * plan.chunk_a;
     const int len = min(plan.chunk_a, V - c0);
-    if (hit && len > 0) {
+    if (hit && len > 0 &&
+        chk(((long long)r * B + (__ffs(hit) - 1)) * V + c0, len, (long long)batch * B * V, ws.err)) {
       const int slot = __ffs(hit) - 1;
       const LT* rowp = target + ((size_t)r * B + slot) * (size_t)V + c0;
       const uint32_t apos = nk.on ? (uint32_t)pos_ids[(size_t)r * 2 * B + slot] : 0u;
@@ -706,7 +722,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(
       const int i2 = __shfl_xor_sync(0xffffffffu, mi, o);
       argmax_merge(m, mi, m2, i2);
     }
-    if (lane == 0) ws.stats[item] = make_float2(m, __int_as_float(mi));
+    if (lane == 0 && chk(item, 1, ws.n_stats, ws.err)) ws.stats[item] = make_float2(m, __int_as_float(mi));
   }
 }
 
@@ -722,7 +738,13 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
   // labels, order and draft tokens before the grid dependency wait (they are not the
   // argmax pass's results)
   int bad = 0, k = 0, x = 0, gr = gamma;  // gr: steps verified, min(gamma, R)
-  if (r < batch) {
+  // checked build: the request's labels, tokens, outputs and chunk results lie inside their
+  // arrays (warp-uniform; else the warp does nothing)
+  const bool rows_ok = r >= batch ||
+                       (chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, dev_err) &&
+                        chk((long long)r * B, B, (long long)batch * B, dev_err) &&
+                        chk((long long)r * gamma * plan.nchunk_a, (long long)gamma * plan.nchunk_a, ws.n_stats, dev_err));
+  if (r < batch && rows_ok) {
     // labels 1..R of the open slots (0: committed in an earlier round) -> order o_t
     const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : 0;
     const int tau = lb & 0x7F;
@@ -743,7 +765,7 @@ __global__ void __launch_bounds__(256) accept_greedy_finish_kernel(
     if (__any_sync(0xffffffffu, perm && lane < gr && (x < 0 || x >= V))) bad |= (int)SIMSD_DEVERR_TOKEN;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (r >= batch) return;  // warp-uniform
+  if (r >= batch || !rows_ok) return;  // warp-uniform
   if (bad) {
     if (lane == 0) {
       atomicOr(dev_err, (uint32_t)bad);
@@ -873,6 +895,8 @@ simsd_status accept_impl(const LT* target_logits, const LT* draft_logits, const 
   ws.stats = (float2*)(base + plan.off_stats);
   ws.winners = (unsigned long long*)(base + plan.off_winners);
   ws.ticket = (unsigned*)(base + plan.off_ticket);
+  ws.n_stats = (long long)batch * gamma * (greedy ? 1 : 2) * plan.nchunk_a;
+  ws.err = dev_err;
   const long grid_a = (long)batch * gamma * 2 * plan.nchunk_a;
   const long grid_b = (long)batch * plan.nchunk_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
@@ -928,6 +952,8 @@ simsd_status accept_coupled_impl(const LT* target_logits, const int32_t* draft_t
   ws.stats = (float2*)(base + plan.off_stats);
   ws.winners = (unsigned long long*)(base + plan.off_winners);
   ws.ticket = (unsigned*)(base + plan.off_ticket);
+  ws.n_stats = (long long)batch * gamma * plan.nchunk_a;
+  ws.err = dev_err;
   const NoiseKey nk = {temperature > 0.f, temperature > 0.f ? 1.f / temperature : 0.f,
                        (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), (uint32_t)(offset & 0xffffffffu)};
   return launch_argmax_verify<LT>(target_logits, draft_tokens, labels, pos_ids, batch, B, gamma, V, plan, ws,
@@ -944,6 +970,7 @@ SIMSD_API simsd_status simsd_accept_ex(const void* target_logits, const void* dr
                                        int32_t* accepted_len, int32_t* out_tokens, int32_t* out_pos,
                                        int32_t* n_commit, void* workspace, size_t workspace_bytes,
                                        uint32_t* dev_err, simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_accept_ex");
   using namespace simsd;
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;
@@ -985,6 +1012,7 @@ SIMSD_API simsd_status simsd_accept_coupled_ex(const void* target_logits, simsd_
                                                int32_t* out_pos, int32_t* n_commit, void* workspace,
                                                size_t workspace_bytes, uint32_t* dev_err,
                                                simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_accept_coupled_ex");
   using namespace simsd;
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;
@@ -1106,6 +1134,7 @@ SIMSD_API simsd_status simsd_accept_noalloc(const float* target_logits, const fl
                                             int32_t* out_tokens, int32_t* out_pos,
                                             int32_t* n_commit, uint32_t* dev_err,
                                             simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_accept_noalloc");
   using namespace simsd;
   // the argument checks of simsd_accept come first, so both return the same status
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)

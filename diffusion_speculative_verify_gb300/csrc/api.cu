@@ -44,6 +44,7 @@ SIMSD_API size_t simsd_verify_attention_workspace(const simsd_attn_params* p) {
 
 SIMSD_API simsd_status simsd_verify_attention(const simsd_attn_params* p, void* workspace,
                                               size_t workspace_bytes, simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_verify_attention");
   const simsd_status st = simsd::check_attn_params(p);
   if (st != SIMSD_OK) return st;
   if (p->batch == 0) return SIMSD_OK;

@@ -42,7 +42,14 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
   const int D = a.D;
   const int half = D / 2;
 
-  T* out = (T*)a.out + (((int64_t)r * twoB + s) * a.Hq + hq) * D;
+  // checked build: the row's output, labels, position ids and request scalars lie inside
+  // their arrays (else the row is skipped, SIMSD_DEVERR_BOUNDS raised)
+  const int64_t orow = ((int64_t)r * twoB + s) * a.Hq + hq;
+  const int64_t nrows = (int64_t)a.batch * twoB * a.Hq;
+  if (!chk(orow * D, D, nrows * D, a.dev_err) || !chk((int64_t)r * twoB, twoB, (int64_t)a.batch * twoB, a.dev_err) ||
+      !chk(r, 1, a.batch, a.dev_err))
+    return;
+  T* out = (T*)a.out + orow * D;
   const uint8_t* lab = a.labels + (int64_t)r * twoB;
   const uint8_t lab_s = lab[s];
   const int P = a.prompt_len[r];
@@ -50,7 +57,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
     if (P < 0 && lane == 0 && s == 0 && hq == 0) atomicOr(a.dev_err, SIMSD_DEVERR_PROMPT_LEN);
 #pragma unroll
     for (int j = 0; j < NPL; ++j) store_f(out + lane + 32 * j, 0.f);
-    if (a.lse && lane == 0) a.lse[((int64_t)r * twoB + s) * a.Hq + hq] = -INFINITY;
+    if (a.lse && lane == 0) a.lse[orow] = -INFINITY;
     return;
   }
   const int t = row_threshold(lab_s);
@@ -59,9 +66,9 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
   // rotated query, elements d = lane + 32 j
   float qv[NPL];
   {
-    const T* qp = (const T*)a.q + (((int64_t)r * twoB + s) * a.Hq + hq) * D;
+    const T* qp = (const T*)a.q + orow * D;
 #pragma unroll
-    for (int j = 0; j < NPL; ++j) qv[j] = load_f(qp + lane + 32 * j);
+    for (int j = 0; j < NPL; ++j) qv[j] = load_f(qp + lane + 32 * j);  // q has out's shape
 #pragma unroll
     for (int j = 0; j < NPL / 2; ++j) {
       const int d = lane + 32 * j;  // first element of the pair (d, d + half)
@@ -102,8 +109,11 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
   const int64_t start = a.cache_start[r];
   const T* kc = (const T*)a.k_cache;
   const T* vc = (const T*)a.v_cache;
+  const int64_t cache_elems = a.cache_tokens * a.Hkv * D;
   for (int jk = 0; jk < P; ++jk) {
     const int64_t base = cache_index(a.layout, a.cache_tokens, a.Hkv, D, start + jk, h);
+    if (!chk(start + jk, 1, a.cache_tokens, a.dev_err) || !chk(base, D, cache_elems, a.dev_err))
+      continue;
     float kk[NPL], vv[NPL];
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
@@ -117,6 +127,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
     if (!response_key_visible(lab[js], t)) continue;
     const int pos_j = a.pos_ids[(int64_t)r * twoB + js];
     const int64_t base = (((int64_t)r * twoB + js) * a.Hkv + h) * D;
+    if (!chk(base, D, (int64_t)a.batch * twoB * a.Hkv * D, a.dev_err)) continue;
     float kk[NPL], vv[NPL];
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
@@ -137,8 +148,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const __grid_constant__ 
   const float inv = 1.f / l;
 #pragma unroll
   for (int j = 0; j < NPL; ++j) store_f(out + lane + 32 * j, acc[j] * inv);
-  if (a.lse && lane == 0)
-    a.lse[((int64_t)r * twoB + s) * a.Hq + hq] = (m + log2f(l)) * 0.69314718055994530942f;
+  if (a.lse && lane == 0) a.lse[orow] = (m + log2f(l)) * 0.69314718055994530942f;
 }
 
 simsd_status launch_attn_simt(const simsd_attn_params* p, cudaStream_t stream) {

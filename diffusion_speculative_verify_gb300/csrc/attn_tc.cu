@@ -69,6 +69,7 @@ struct TcArgs {
   int cl;                             // CTAs per schedule unit: 1, or 2 when R > 128
   int seg_cost;                       // virtual units charged per pair for start-up
   int layout;
+  int64_t cache_tokens;               // rows of the packed prompt cache
   uint64_t wait_ns;                   // bound of every device-side wait
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_resp;
@@ -107,13 +108,16 @@ __host__ __device__ __forceinline__ size_t part_slot(int cta, int piece) {
 // that is cut into equal contiguous ranges, one per schedule unit. A range that begins inside
 // a pair's start-up share starts at the pair's tile 0; one that ends inside it does not take
 // the pair.
+// (Checked build: a request index outside the batch reads as an invalid request.)
 __device__ __forceinline__ int tiles_per_pair(const TcArgs& a, int b) {
+  if (!chk(b, 1, a.batch, a.dev_err)) return 1;
   const int P = a.prompt_len[b];
   const uint8_t l0 = a.labels[(size_t)b * 2 * a.B];  // both loads issued together
   if ((P < 0) | (l0 == kLabelInvalid)) return 1;
   return 1 + (P + kKeys - 1) / kKeys;
 }
 __device__ __forceinline__ bool request_invalid(const TcArgs& a, int b) {
+  if (!chk(b, 1, a.batch, a.dev_err)) return true;
   const int P = a.prompt_len[b];
   const uint8_t l0 = a.labels[(size_t)b * 2 * a.B];
   return (P < 0) | (l0 == kLabelInvalid);
@@ -259,7 +263,7 @@ struct PromptTiles {
           const int ii = i++;
           if (ii == 0) continue;
           h = it.h;
-          tok = (int)(a.cache_start[it.b] + (int64_t)(ii - 1) * kKeys);
+          tok = (int)(a.cache_start[it.b] + (int64_t)(ii - 1) * kKeys);  // it.b checked by it.next
           return true;
         }
       }
@@ -496,6 +500,10 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]
 __device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& it, bool real,
                                                 size_t orow, size_t slot, int row) {
   if (!real) return;
+  const int64_t nrows = (int64_t)a.batch * 2 * a.B * a.Hq;
+  if (!chk((int64_t)orow, 1, nrows, a.dev_err) ||
+      !chk((int64_t)slot * kBlockRows + row, 1, (int64_t)2 * a.ctas * a.cl * kBlockRows, a.dev_err))
+    return;
   if (it.invalid) {
     uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
 #pragma unroll
@@ -574,13 +582,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       // When every unit is one pair, this unit's pair is known before the schedule: its
       // first prompt tiles go into L2 now, so that the stream, which starts after the first
       // prologue, finds them there.
-      if ((int64_t)a.batch * a.Hkv == (int64_t)a.ctas) {
+      if ((int64_t)a.batch * a.Hkv == (int64_t)a.ctas && chk(vcta / a.Hkv, 1, a.batch, a.dev_err)) {
         const int gb = vcta / a.Hkv, gh = vcta - (vcta / a.Hkv) * a.Hkv;
         const int P = a.prompt_len[gb];
         const int64_t cs = a.cache_start[gb];
         const int n = min(kStages, (max(P, 0) + kKeys - 1) / kKeys);
         for (int i = 0; i < n; ++i) {
           const int tok = (int)(cs + (int64_t)i * kKeys);
+          if (!chk(tok, 1, a.cache_tokens, a.dev_err)) break;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             if (a.layout == SIMSD_CACHE_NHD) {
@@ -662,6 +671,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         const int s = p % kStages;
         ok = wait_bar(sh, bar(kEmpty0 + s), ((p / kStages) & 1) ^ 1, a.dev_err, wait_ns);
         if (!ok) break;
+        // checked build: a tile row outside the cache or a head outside Hkv is not copied
+        // (the stage completes without data, the error word records it)
+        if (!chk(tok, 1, a.cache_tokens, a.dev_err) || !chk(h, 1, a.Hkv, a.dev_err)) {
+          ptx::mbar_arrive(bar(kFull0 + s));
+          ++p;
+          continue;
+        }
         ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
         const uint32_t kdst = sbase + kOffStages + s * kStage;
         const uint32_t vdst = kdst + kKV;
@@ -862,16 +878,21 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip);
         // issued before the row loads, whose many requests would otherwise delay them
         const size_t lrow = (size_t)b * twoB;
-        const uint32_t lab_lo = lane < twoB ? a.labels[lrow + lane] : 0u;
-        const uint32_t lab_hi = lane + 32 < twoB ? a.labels[lrow + 32 + lane] : 0u;
-        const int pos_lo = lane < twoB ? a.pos_ids[lrow + lane] : 0;
-        const int pos_hi = lane + 32 < twoB ? a.pos_ids[lrow + 32 + lane] : 0;
+        // checked build: the request's labels / positions, this thread's Q row and tail row
+        // lie inside their arrays (a row outside is not loaded)
+        const bool lab_ok = chk((int64_t)lrow, twoB, (int64_t)a.batch * twoB, a.dev_err);
+        const uint32_t lab_lo = lab_ok && lane < twoB ? a.labels[lrow + lane] : 0u;
+        const uint32_t lab_hi = lab_ok && lane + 32 < twoB ? a.labels[lrow + 32 + lane] : 0u;
+        const int pos_lo = lab_ok && lane < twoB ? a.pos_ids[lrow + lane] : 0;
+        const int pos_hi = lab_ok && lane + 32 < twoB ? a.pos_ids[lrow + 32 + lane] : 0;
         uint4 v[16];
-        const __nv_bfloat16* trow =
-            (tr.k ? a.k_resp : a.v_resp) + (((size_t)b * twoB + (tr.row ? tr.key : 0)) * a.Hkv + h) * kD;
+        const size_t tidx = (((size_t)b * twoB + (tr.row ? tr.key : 0)) * a.Hkv + h) * kD;
+        const __nv_bfloat16* trow = (tr.k ? a.k_resp : a.v_resp) + tidx;
+        const bool q_ok = chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err);
+        const bool t_ok = !tr.row || chk((int64_t)tidx, kD, (int64_t)a.batch * twoB * a.Hkv * kD, a.dev_err);
         if (warp_active) {
-          if (real) load_row(v, a.q + orow * kD);
-        } else if (tr.early && tr.row) {
+          if (real && q_ok) load_row(v, a.q + orow * kD);
+        } else if (tr.early && tr.row && t_ok) {
           load_row(v, trow);
         }
         if (!tr.early && tr.row) {  // into L2 now, into registers once Q is in TMEM
@@ -930,7 +951,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
         }
         if (!tr.early && has_tail) {
-          if (tr.row) {
+          if (tr.row && t_ok) {
             load_row(v, trow);
             if (tr.k) rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
           } else {
@@ -1072,7 +1093,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err, wait_ns));
         if (!ok) break;
         ptx::tc_fence_after();
-        if (warp_active) {
+        if (warp_active && chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err) &&
+            chk((int64_t)slot * kBlockRows + row, 1, (int64_t)2 * a.ctas * a.cl * kBlockRows, a.dev_err)) {
           const float inv = it.full ? 1.f / l : 1.f;
 #pragma unroll 1
           for (int k = 0; k < 4; ++k) {
@@ -1122,7 +1144,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         it.advance(a);
       } while (it.next(a));
     }
-    if (tid == 0) a.ws_desc[blockIdx.x] = desc;
+    if (tid == 0 && chk(blockIdx.x, 1, (int64_t)a.ctas * a.cl, a.dev_err)) a.ws_desc[blockIdx.x] = desc;
     if (!loads_signalled) ptx::mbar_arrive(bar(kLoads));  // no prologue ran: release the producer
   }
 
@@ -1138,6 +1160,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the attention grid has completed
   const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
+  if (!chk(c, 1, (int64_t)a.ctas * a.cl, a.dev_err)) return;
   const MergeDesc d = a.ws_desc[c];
   if (d.b < 0) return;
   const int cl = a.cl;
@@ -1151,10 +1174,12 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   // pieces: unit vc (its piece0) and every later non-empty unit up to c_last (its first
   // piece), each in the CTA of the same row block
   float mmax = -INFINITY;
+  const int64_t nslots = (int64_t)2 * a.ctas * cl;
 #pragma unroll 4
   for (int vcc = vc; vcc <= d.c_last; ++vcc) {
     if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
     const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
+    if (!chk((int64_t)slot, 1, nslots, a.dev_err)) continue;
     mmax = fmaxf(mmax, a.ws_ml[slot * kBlockRows + row].x);
   }
   float L = 0.f;
@@ -1163,6 +1188,7 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   for (int vcc = vc; vcc <= d.c_last; ++vcc) {
     if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
     const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
+    if (!chk((int64_t)slot, 1, nslots, a.dev_err)) continue;
     const float2 ml = a.ws_ml[slot * kBlockRows + row];
     const float4 o = reinterpret_cast<const float4*>(a.ws_o + (slot * kBlockRows + row) * kD)[quad];
     const float w = exp2f(ml.x - mmax);
@@ -1175,6 +1201,7 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   const float inv = 1.f / L;
   const int s_slot = prow / a.G, g = prow % a.G;
   const size_t orow = ((size_t)d.b * 2 * a.B + s_slot) * a.Hq + (size_t)d.h * a.G + g;
+  if (!chk((int64_t)orow, 1, (int64_t)a.batch * 2 * a.B * a.Hq, a.dev_err)) return;
   uint2 pk;
   pk.x = pack_bf16(acc.x * inv, acc.y * inv);
   pk.y = pack_bf16(acc.z * inv, acc.w * inv);
@@ -1309,6 +1336,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   a.seg_cost = seg_cost_tiles(2 * p->B);
   a.ctas = grid_units(p, a.cl);
   a.layout = (int)p->cache_layout;
+  a.cache_tokens = p->cache_tokens;
   a.wait_ns = p->wait_limit_ns > 0 ? p->wait_limit_ns : kDefaultWaitNs;
   a.q = (const __nv_bfloat16*)p->q;
   a.k_resp = (const __nv_bfloat16*)p->k_resp;

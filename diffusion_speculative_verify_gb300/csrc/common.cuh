@@ -9,6 +9,8 @@
 
 #define SIMSD_API extern "C" __attribute__((visibility("default")))
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace simsd {
 
 constexpr int kMaxB = 32;          // block size limit (labels hold tau in 7 bits; warp scans)
@@ -36,6 +38,42 @@ static inline int device_sm_count() {
 }
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// NVTX range around one call of the C interface, named after it, so that a timeline
+// profiler shows each call with its kernels (an NVTX call costs a few ns when no tool is
+// attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define SIMSD_NVTX_RANGE(name) ::simsd::NvtxRange simsd_nvtx_range_(name)
+
+// --------------------------------------------------------------------- checked build
+// Built with -DSIMSD_CHECKED, every kernel checks the index of each global access against
+// the extent of the array it addresses (extents follow from the call's sizes; for a row
+// read in one piece the row's range is checked); an index outside sets SIMSD_DEVERR_BOUNDS
+// in the call's error word and the access is skipped (a skipped load yields a neutral
+// value). It stands in for a memory checker where none can run. In the default build every
+// check is the constant true and compiles away.
+#ifdef SIMSD_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// True when [i, i + len) lies inside [0, n); otherwise (checked build only) raises
+// SIMSD_DEVERR_BOUNDS in *err.
+__device__ __forceinline__ bool chk(long long i, long long len, long long n, uint32_t* err) {
+  if constexpr (!kChecked) {
+    return true;
+  } else {
+    if (i >= 0 && len >= 0 && i + len <= n) return true;
+    atomicOr(err, SIMSD_DEVERR_BOUNDS);
+    return false;
+  }
+}
 
 // ------------------------------------------------------------------------------ Philox
 // Philox4x32-10 as defined by Salmon, Moraes, Dror, Shaw (SC'11): each round forms the

@@ -22,8 +22,9 @@ __global__ void __launch_bounds__(128) build_layout_kernel(
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= batch) return;
   const bool active = lane < B;
-  const int t = active ? tau[(size_t)r * B + lane] : 0;
-  const int P = prompt_len[r];
+  const long long ti = (long long)r * B + lane;
+  const int t = active && chk(ti, 1, (long long)batch * B, dev_err) ? tau[ti] : 0;
+  const int P = chk(r, 1, batch, dev_err) ? prompt_len[r] : 0;
   // tau = 0 marks a slot committed in an earlier round of the block; the R other labels
   // must be a permutation of 1..R  <=>  every value lies in 0..B and the R nonzero values
   // set R distinct bits, the bits of 1..R.
@@ -38,6 +39,9 @@ __global__ void __launch_bounds__(128) build_layout_kernel(
   if (P < 0) bad |= SIMSD_DEVERR_PROMPT_LEN;
   if (!active) return;
   const size_t row = (size_t)r * 2 * B;
+  if (!chk((long long)row + lane, 1, (long long)batch * 2 * B, dev_err) ||
+      !chk((long long)row + B + lane, 1, (long long)batch * 2 * B, dev_err))
+    return;
   if (bad) {
     pos_ids[row + lane] = -1;
     pos_ids[row + B + lane] = -1;
@@ -58,6 +62,7 @@ SIMSD_API simsd_status simsd_build_layout_ex(const int32_t* tau, const int32_t* 
                                              int batch, int B, uint32_t flags, int32_t* pos_ids,
                                              uint8_t* labels, uint32_t* dev_err,
                                              simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_build_layout_ex");
   if (batch < 0 || B < 1 || B > simsd::kMaxB) return SIMSD_ERR_INVALID_ARG;
   if (flags & ~(uint32_t)SIMSD_LAYOUT_PHYSICAL_POSITIONS) return SIMSD_ERR_INVALID_ARG;
   if (batch == 0) return SIMSD_OK;

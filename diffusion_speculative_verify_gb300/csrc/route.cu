@@ -163,7 +163,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 template <typename LT>
 __global__ void __launch_bounds__(kKhatThreads, 2) khat_stats_kernel(
     const LT* __restrict__ draft, const uint8_t* __restrict__ labels, int batch, int B,
-    int gamma, int V, float T, KhatPlan plan, float4* __restrict__ stats) {
+    int gamma, int V, float T, KhatPlan plan, float4* __restrict__ stats, uint32_t* __restrict__ err) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long warp_global = (long)blockIdx.x * (kKhatThreads / 32) + (threadIdx.x >> 5);
@@ -181,12 +181,14 @@ __global__ void __launch_bounds__(kKhatThreads, 2) khat_stats_kernel(
     const int step = (int)(row % gamma);
     const int r = (int)(row / gamma);
     // the data slot labelled step + 1 (none for an invalid request or a step past R)
-    const uint8_t lb = lane < B ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
+    const bool lab_ok = chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, err);
+    const uint8_t lb = lane < B && lab_ok ? labels[(size_t)r * 2 * B + lane] : (uint8_t)0;
     const unsigned hit = __ballot_sync(0xffffffffu, lane < B && !(lb & kSegMask) && (lb & 0x7F) == step + 1);
     float4 st = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
     const int c0 = chunk * plan.chunk;
     const int len = min(plan.chunk, V - c0);
-    if (hit && len > 0) {
+    if (hit && len > 0 &&
+        chk(((long long)r * B + (__ffs(hit) - 1)) * V + c0, len, (long long)batch * B * V, err)) {
       const LT* rowp = draft + ((size_t)r * B + (__ffs(hit) - 1)) * (size_t)V + c0;
       float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;  // relative to st.x
       if (vec_ok) {  // c0 is a multiple of 8: every load is 16-byte aligned
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kKhatThreads, 2) khat_stats_kernel(
       other.w = __shfl_xor_sync(0xffffffffu, st.w, o);
       stat_merge(st, other);
     }
-    if (lane == 0) stats[item] = st;
+    if (lane == 0 && chk(item, 1, items, err)) stats[item] = st;
   }
 }
 
@@ -274,6 +276,12 @@ __global__ void __launch_bounds__(32 * kFinishWarps) khat_finish_kernel(
     float* __restrict__ khat, float* __restrict__ alpha_out, uint32_t* __restrict__ dev_err) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x;
+  // checked build: the request's labels, chunk statistics and outputs lie inside their
+  // arrays (block-uniform; else the block does nothing)
+  if (!chk(r, 1, batch, dev_err) || !chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, dev_err) ||
+      !chk((long long)r * gamma * plan.nchunk, (long long)gamma * plan.nchunk,
+           (long long)batch * gamma * plan.nchunk, dev_err))
+    return;
   __shared__ float s_alpha[kMaxB];
   // open slots carry the labels 1..R (0: committed in an earlier round); every warp
   // reaches the same decision
@@ -360,7 +368,8 @@ simsd_status expected_prefix_impl(const LT* draft, const uint8_t* labels, int ba
   float4* stats = (float4*)workspace;
   const long max_ctas = std::max(1, resident_khat_warps() / (kKhatThreads / 32));
   const long grid = std::max<long>(1, std::min<long>((items + kKhatThreads / 32 - 1) / (kKhatThreads / 32), max_ctas));
-  khat_stats_kernel<LT><<<(unsigned)grid, kKhatThreads, 0, s>>>(draft, labels, batch, B, gamma, V, T, plan, stats);
+  khat_stats_kernel<LT><<<(unsigned)grid, kKhatThreads, 0, s>>>(draft, labels, batch, B, gamma, V, T, plan, stats,
+                                                                dev_err);
   simsd_status st = last_launch_status();
   if (st != SIMSD_OK) return st;
   cudaLaunchConfig_t cfg = {};
@@ -396,6 +405,7 @@ SIMSD_API simsd_status simsd_expected_prefix(const void* draft_logits, simsd_dty
                                              float beta, float* khat, float* alpha, void* workspace,
                                              size_t workspace_bytes, uint32_t* dev_err,
                                              simsd_stream_t stream) {
+  SIMSD_NVTX_RANGE("simsd_expected_prefix");
   using namespace simsd;
   if (batch < 0 || B < 1 || B > kMaxB || gamma < 1 || gamma > B || V < 1)
     return SIMSD_ERR_INVALID_ARG;

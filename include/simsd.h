@@ -72,6 +72,9 @@ typedef enum {
 #define SIMSD_DEVERR_PROMPT_LEN 2u /* prompt length < 0                                 */
 #define SIMSD_DEVERR_TOKEN 4u      /* a verified draft token id is outside [0, V)       */
 #define SIMSD_DEVERR_TIMEOUT 8u    /* a bounded wait inside a kernel gave up            */
+#define SIMSD_DEVERR_BOUNDS 16u    /* checked builds only (compiled with SIMSD_CHECKED):
+                                      a kernel computed a global index outside the array
+                                      it addresses; that access was skipped             */
 
 /* Label byte of a response slot: (segment << 7) | tau, segment 0 = D, 1 = D~.
  * 0xFF marks every slot of a request the layout call rejected. */
