@@ -846,9 +846,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     desc.T = st.T;
     while (it.next(a)) {
       // Every softmax thread reaches this point once per segment: the decision to unwind is
-      // taken here by all of them together.
-      ptx::named_bar_sync(1, 128);
-      if (*(volatile int*)&sh->abort) {
+      // taken here by all of them together (the flag may be raised while they read it, so
+      // the barrier reduces what each saw to one answer).
+      if (ptx::bar_or(1, 128, *(volatile int*)&sh->abort != 0)) {
         aborted = true;
         break;
       }
