@@ -284,16 +284,21 @@ struct Shared {
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort;
+  uint32_t peer_abort;  // CTA pairs: cluster address of the other CTA's abort flag (else 0)
   int64_t T, t0, t1, Tb;
   int b;
   int64_t wsum[4];          // block scan of the schedule
+  uint32_t vis[64][2];      // per response slot: visibility bits of response keys 0-31, 32-63
 };
 
 // Sets the CTA's abort flag and, once, the timeout bit of the error word.
+// In a CTA pair the other CTA's flag is raised too, so that it unwinds without waiting out
+// its own limit.
 __device__ __forceinline__ void raise_abort(Shared* sh, uint32_t* dev_err) {
   if (!*(volatile int*)&sh->abort) {
     *(volatile int*)&sh->abort = 1;
     atomicOr(dev_err, SIMSD_DEVERR_TIMEOUT);
+    if (sh->peer_abort) ptx::st_cluster_u32(sh->peer_abort, 1u);
   }
 }
 
@@ -546,18 +551,41 @@ constexpr uint32_t kTailKV = 2 * kTailHalf;      // 16 KB
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffTail = kOffStages + kStages * kStage;  // tail K (16 KB) then V (16 KB)
 constexpr uint32_t kOffBar = kOffTail + 2 * kTailKV;
-constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;        // barriers + alignment slack
+constexpr uint32_t kSmemBytes = kOffBar + 2048 + 1024;        // barriers + alignment slack
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemQ = 384, kTmemCols = 512;
 static_assert(kStages <= kMaxSlots, "stage barriers");
+// CTA pairs (pairs of 129..256 rows): per CTA and prompt tile, K of 64 of the tile's 128 keys
+// (CTA r: keys [64 r, 64 r + 64), all dims as two 64-dim halves) then V of all 128 keys for
+// 64 of the dims (CTA r: dims [64 r, 64 r + 64)); the tail tile likewise: tail K keys
+// [32 r, 32 r + 32), tail V dims [64 r, 64 r + 64) of all 64 tail keys.
+constexpr uint32_t kPKHalf = 64 * 128;                    // 8 KB
+constexpr uint32_t kPStage = 2 * kPKHalf + kKeys * 128;   // 32 KB
+constexpr int kPStages = 6;
+constexpr uint32_t kPTailKHalf = 32 * 128;                // 4 KB
+static_assert(kPStages * kPStage == kStages * kStage, "one ring size for both modes");
+static_assert(kPStages <= kMaxSlots, "stage barriers");
 }  // namespace r128
 
+// kPair: the two CTAs of a schedule unit form a cluster and one tcgen05.mma (cta_group::2,
+// M = 256) covers both 128-row blocks; each CTA loads only its half of every K and V tile
+// (above), so a tile crosses from memory once per pair, and the ring holds six tiles.
+// The even CTA issues every MMA; the odd CTA's MMA warp forwards the completion of its own
+// copies to the even CTA's ring barriers.
+template <bool kPair>
 __global__ void __launch_bounds__(r128::kThreads, 1)
     attn_tc128_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ TcArgs a) {
   using namespace r128;
-  static_assert(sizeof(Shared) <= 1024, "barrier area");
+  static_assert(sizeof(Shared) <= 2048, "barrier area");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  constexpr uint32_t STG = kPair ? kPStage : kStage;    // bytes of one ring stage
+  constexpr int NSTG = kPair ? kPStages : kStages;      // ring stages
+  constexpr uint32_t KHALF = kPair ? kPKHalf : kHalf;   // one 64-dim half of a stage's K
+  constexpr uint32_t VOFF = 2 * KHALF;                  // V within a stage
+  constexpr uint32_t TKHALF = kPair ? kPTailKHalf : kTailHalf;
+  constexpr int MROWS = kPair ? 256 : 128;              // rows of one MMA
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // let the merge grid be placed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -567,8 +595,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   const uint32_t sbase = ptx::smem_u32(smem);
   auto bar = [&](int i) { return ptx::smem_u32(&sh->bars[i]); };
   // Pairs of more than 128 rows: two CTAs take each schedule unit, CTA `crank` the rows
-  // [128 crank, 128 crank + 128); they are independent (each loads the unit's prompt tiles
-  // itself) and differ only in their rows.
+  // [128 crank, 128 crank + 128). Without kPair they are independent (each loads the unit's
+  // whole prompt tiles) and differ only in their rows; with kPair they are the two halves of
+  // one MMA unit (cluster rank = crank).
   const int cl = a.cl;
   const int vcta = blockIdx.x / cl, crank = blockIdx.x - vcta * cl;
   const int row0 = crank * 128;  // first pair row of this CTA
@@ -576,6 +605,32 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   // kPFull0 + b: P of the tile in S buffer b written. kSFree0 + b: the P V that read S
   // buffer b completed; its phase for tile j is j / 2, and the previous phase (tile j - 2) is
   // always complete by the time anyone waits for tile j, so a parity wait is unambiguous.
+  // With kPair, the ring barriers count this CTA's own copies; the even CTA's full barriers
+  // also wait for the odd CTA's forwarded arrival, and its P and Q barriers count one arrival
+  // per softmax warp of both CTAs. Every other barrier is arrived at by MMA commits, in both
+  // CTAs at once.
+
+  // This CTA's boxes of prompt tile (kv head h, first key tok): K as two 64-dim halves, then
+  // V, into the stage at `dst` (counted on `fbar`); !load: into L2 only.
+  auto tile_boxes = [&](int h, int tok, bool load, uint32_t dst, uint32_t fbar) {
+    auto box = [&](const CUtensorMap* map, int d0, int key0, uint32_t to) {
+      const int c1 = a.layout == SIMSD_CACHE_NHD ? h : key0;
+      const int c2 = a.layout == SIMSD_CACHE_NHD ? key0 : h;
+      if (load)
+        ptx::tma_load_3d(to, map, d0, c1, c2, fbar);
+      else
+        ptx::tma_prefetch_3d(map, d0, c1, c2);
+    };
+    const int ktok = kPair ? tok + 64 * crank : tok;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) box(&tmk, half * 64, ktok, dst + half * KHALF);
+    if constexpr (kPair) {
+      box(&tmv, 64 * crank, tok, dst + VOFF);
+    } else {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) box(&tmv, half * 64, tok, dst + VOFF + half * kHalf);
+    }
+  };
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -590,29 +645,22 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         for (int i = 0; i < n; ++i) {
           const int tok = (int)(cs + (int64_t)i * kKeys);
           if (!chk(tok, 1, a.cache_tokens, a.dev_err)) break;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (a.layout == SIMSD_CACHE_NHD) {
-              ptx::tma_prefetch_3d(&tmk, half * 64, gh, tok);
-              ptx::tma_prefetch_3d(&tmv, half * 64, gh, tok);
-            } else {
-              ptx::tma_prefetch_3d(&tmk, half * 64, tok, gh);
-              ptx::tma_prefetch_3d(&tmv, half * 64, tok, gh);
-            }
-          }
+          tile_boxes(gh, tok, false, 0u, 0u);
         }
       }
       sh->abort = 0;
-      for (int i = 0; i < kStages; ++i) {
-        ptx::mbar_init(bar(kFull0 + i), 1);
+      sh->peer_abort = kPair ? ptx::mapa(ptx::smem_u32(&sh->abort), (uint32_t)(crank ^ 1)) : 0u;
+      const bool lead = kPair && crank == 0;
+      for (int i = 0; i < NSTG; ++i) {
+        ptx::mbar_init(bar(kFull0 + i), lead ? 2 : 1);
         ptx::mbar_init(bar(kEmpty0 + i), 1);
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(bar(kSFull0 + i), 1);
         ptx::mbar_init(bar(kSFree0 + i), 1);
-        ptx::mbar_init(bar(kPFull0 + i), 128);
+        ptx::mbar_init(bar(kPFull0 + i), kPair ? 8 : 128);
       }
-      ptx::mbar_init(bar(kQFull), 128);
+      ptx::mbar_init(bar(kQFull), kPair ? 8 : 128);
       ptx::mbar_init(bar(kDrain), 1);
       ptx::mbar_init(bar(kLoads), 128);
       ptx::fence_mbar_init();
@@ -620,8 +668,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       ptx::prefetch_tensormap(&tmv);
     }
   } else if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(&sh->tmem_base), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(&sh->tmem_base), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   } else {
     {  // Before the schedule is known: this unit's likely first pair (exact when every unit
        // is one whole pair) has its prologue rows prefetched into L2, so that the first
@@ -639,7 +692,11 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     block_schedule(a, vcta, a.ctas, tid, sh->wsum, &sh->T, &sh->t0, &sh->t1, &sh->Tb, &sh->b);
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    ptx::cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
+  } else {
+    __syncthreads();
+  }
   ptx::tc_fence_after();
 
   SchedStart st;
@@ -668,8 +725,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           ok = wait_bar(sh, bar(kLoads), 0, a.dev_err, wait_ns);
           if (!ok) break;
         }
-        const int s = p % kStages;
-        ok = wait_bar(sh, bar(kEmpty0 + s), ((p / kStages) & 1) ^ 1, a.dev_err, wait_ns);
+        const int s = p % NSTG;
+        ok = wait_bar(sh, bar(kEmpty0 + s), ((p / NSTG) & 1) ^ 1, a.dev_err, wait_ns);
         if (!ok) break;
         // checked build: a tile row outside the cache or a head outside Hkv is not copied
         // (the stage completes without data, the error word records it)
@@ -678,32 +735,50 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           ++p;
           continue;
         }
-        ptx::mbar_arrive_expect_tx(bar(kFull0 + s), kStage);
-        const uint32_t kdst = sbase + kOffStages + s * kStage;
-        const uint32_t vdst = kdst + kKV;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (a.layout == SIMSD_CACHE_NHD) {
-            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, h, tok, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, h, tok, bar(kFull0 + s));
-          } else {
-            ptx::tma_load_3d(kdst + half * kHalf, &tmk, half * 64, tok, h, bar(kFull0 + s));
-            ptx::tma_load_3d(vdst + half * kHalf, &tmv, half * 64, tok, h, bar(kFull0 + s));
-          }
-        }
+        ptx::mbar_arrive_expect_tx(bar(kFull0 + s), STG);
+        tile_boxes(h, tok, true, sbase + kOffStages + s * STG, bar(kFull0 + s));
         ++p;
       }
       // Whether the stream ended or the CTA is unwinding, the copies issued last may still be
-      // in flight; they land before the CTA can exit (earlier ones have been consumed).
-      for (uint32_t k = p > (uint32_t)kStages ? p - kStages : 0; k < p; ++k)
-        drain_wait(bar(kFull0 + k % kStages), (k / kStages) & 1);
+      // in flight; they land before the CTA can exit (earlier ones have been consumed). (The
+      // even CTA of a pair counts the odd CTA's forwarded arrival on the same barriers: if
+      // that one never comes, the bounded drain gives up.)
+      for (uint32_t k = p > (uint32_t)NSTG ? p - NSTG : 0; k < p; ++k)
+        drain_wait(bar(kFull0 + k % NSTG), (k / NSTG) & 1);
     }
   } else if (warp == kMmaWarp) {
+    if (kPair && crank != 0 && lane == 0) {
+      // ------------------------------------------------- copy completion forwarder (odd CTA)
+      // The even CTA issues the MMAs that read this CTA's half of every stage: each stage's
+      // completion here becomes one arrival on the even CTA's full barrier of that stage, in
+      // ring order (the producer fills stages in that order; a stage is refilled only after
+      // the MMAs, which wait for this arrival, have released it).
+      PromptTiles tiles;
+      tiles.init(a, st);
+      int h, tok;
+      for (uint32_t p = 0; tiles.next(a, h, tok); ++p) {
+        const int s = p % NSTG;
+        if (!wait_bar(sh, bar(kFull0 + s), (p / NSTG) & 1, a.dev_err, wait_ns)) break;
+        ptx::mbar_arrive_remote(ptx::mapa(bar(kFull0 + s), 0u));
+      }
+    }
     // ------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = ptx::idesc_bf16(128, kKeys, 0, 0);
-      constexpr uint32_t idS_tail = ptx::idesc_bf16(128, 64, 0, 0);
-      constexpr uint32_t idPV = ptx::idesc_bf16(128, kD, 0, 1);
+    if (lane == 0 && (!kPair || crank == 0)) {
+      constexpr uint32_t idS = ptx::idesc_bf16(MROWS, kKeys, 0, 0);
+      constexpr uint32_t idS_tail = ptx::idesc_bf16(MROWS, 64, 0, 0);
+      constexpr uint32_t idPV = ptx::idesc_bf16(MROWS, kD, 0, 1);
+      auto mma = [&](uint32_t d, uint32_t at, uint64_t bd, uint32_t id, uint32_t acc) {
+        if constexpr (kPair)
+          ptx::mma_f16_ts_pair(d, at, bd, id, acc);
+        else
+          ptx::mma_f16_ts(d, at, bd, id, acc);
+      };
+      auto commit = [&](uint32_t b) {  // with kPair: the barrier of both CTAs
+        if constexpr (kPair)
+          ptx::mma_commit_pair_both(b);
+        else
+          ptx::mma_commit(b);
+      };
       SegIter it;
       it.init(a, st);
       uint32_t j = 0, m = 0, nseg = 0;
@@ -742,8 +817,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       static_assert(kAhead + 1 <= 8, "tile ring");
       auto try_issue_s = [&](uint32_t jj, int i) -> bool {
         const int buf = jj & 1;
-        const int s = m % kStages;
-        if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / kStages) & 1)) return false;
+        const int s = m % NSTG;
+        if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / NSTG) & 1)) return false;
         if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj >> 1) & 1) ^ 1)) return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem + kTmemS0 + buf * 128;
@@ -751,37 +826,38 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           const uint32_t kaddr = sbase + kOffTail;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            ptx::mma_f16_ts(d, tmem + kTmemQ + kk * 8,
-                            ptx::sdesc_sw128(kaddr + (kk >> 2) * kTailHalf + (kk & 3) * 32, 16, 1024),
-                            idS_tail, kk > 0 ? 1u : 0u);
+            mma(d, tmem + kTmemQ + kk * 8,
+                ptx::sdesc_sw128(kaddr + (kk >> 2) * TKHALF + (kk & 3) * 32, 16, 1024), idS_tail,
+                kk > 0 ? 1u : 0u);
           stage_of[jj & 7] = -1;
         } else {
-          const uint32_t kaddr = sbase + kOffStages + s * kStage;
+          const uint32_t kaddr = sbase + kOffStages + s * STG;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            ptx::mma_f16_ts(d, tmem + kTmemQ + kk * 8,
-                            ptx::sdesc_sw128(kaddr + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                            idS, kk > 0 ? 1u : 0u);
+            mma(d, tmem + kTmemQ + kk * 8,
+                ptx::sdesc_sw128(kaddr + (kk >> 2) * KHALF + (kk & 3) * 32, 16, 1024), idS,
+                kk > 0 ? 1u : 0u);
           stage_of[jj & 7] = s;
           ++m;
         }
-        ptx::mma_commit(bar(kSFull0 + buf));
+        commit(bar(kSFull0 + buf));
         return true;
       };
+      // V as B is N-major: 16 keys (rows of 128 bytes) per K step; with kPair each CTA holds
+      // a single 64-dim column of atoms, so the leading (N) offset is never used.
       auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
         const int buf = jj & 1;
         if (!ptx::mbar_test(bar(kPFull0 + buf), (jj >> 1) & 1)) return false;
         ptx::tc_fence_after();
         const int s = stage_of[jj & 7];
-        const uint32_t vaddr = s < 0 ? sbase + kOffTail + kTailKV : sbase + kOffStages + s * kStage + kKV;
+        const uint32_t vaddr = s < 0 ? sbase + kOffTail + kTailKV : sbase + kOffStages + s * STG + VOFF;
         const uint32_t lbo = s < 0 ? kTailHalf : kHalf;
         const int nk = s < 0 ? 4 : kKeys / 16;
         for (int kk = 0; kk < nk; ++kk)
-          ptx::mma_f16_ts(tmem + kTmemO, tmem + kTmemS0 + buf * 128 + kk * 8,
-                          ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV,
-                          (first_in_seg && kk == 0) ? 0u : 1u);
-        ptx::mma_commit(bar(kSFree0 + buf));
-        if (s >= 0) ptx::mma_commit(bar(kEmpty0 + s));
+          mma(tmem + kTmemO, tmem + kTmemS0 + buf * 128 + kk * 8,
+              ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV, (first_in_seg && kk == 0) ? 0u : 1u);
+        commit(bar(kSFree0 + buf));
+        if (s >= 0) commit(bar(kEmpty0 + s));
         return true;
       };
       while (ok && it.next(a)) {
@@ -820,7 +896,10 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         it.advance(a);
       }
       // every MMA issued has completed before TMEM is freed
-      ptx::mma_commit(bar(kDrain));
+      if constexpr (kPair)
+        ptx::mma_commit_pair_own(bar(kDrain));
+      else
+        ptx::mma_commit(bar(kDrain));
       drain_wait(bar(kDrain), 0);
     }
   } else {
@@ -836,6 +915,16 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     uint8_t* tailk = smem + kOffTail;
     uint8_t* tailv = tailk + kTailKV;
     const int rw = (min(128, a.R - row0) + 31) & ~31;  // threads below rw own this block's rows
+    // Arrival on the Q / P barriers: each thread, or with kPair one per warp on the even
+    // CTA's barrier (after every lane's TMEM stores and fences).
+    auto arrive_x = [&](int i) {
+      if constexpr (kPair) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa(bar(i), 0u));
+      } else {
+        ptx::mbar_arrive(bar(i));
+      }
+    };
     SegIter it;
     it.init(a, st);
     uint32_t j = 0;
@@ -873,10 +962,11 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         const bool has_tail = it.has_tail;
         // ---- prologue: rotated + scaled Q rows into TMEM, rotated tail K and plain tail V
         // tiles. Each thread holds at most one row.
-        const TailRole tr = tail_role(rw, twoB, tid, has_tail);
+        const TailRole tr = tail_role(kPair ? 128 : rw, twoB, tid, has_tail);  // kPair: never early
         // labels and position ids of the 2B response slots: every warp holds slot `lane` and
-        // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip);
-        // issued before the row loads, whose many requests would otherwise delay them
+        // slot 32 + lane, and hands them out by shuffles (no shared-memory round trip). The
+        // row loads come after the table and the masks: issued first, their many requests
+        // held up every shuffle behind them (measured: 4x slower loops).
         const size_t lrow = (size_t)b * twoB;
         // checked build: the request's labels / positions, this thread's Q row and tail row
         // lie inside their arrays (a row outside is not loaded)
@@ -890,11 +980,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         const __nv_bfloat16* trow = (tr.k ? a.k_resp : a.v_resp) + tidx;
         const bool q_ok = chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err);
         const bool t_ok = !tr.row || chk((int64_t)tidx, kD, (int64_t)a.batch * twoB * a.Hkv * kD, a.dev_err);
-        if (warp_active) {
-          if (real && q_ok) load_row(v, a.q + orow * kD);
-        } else if (tr.early && tr.row && t_ok) {
-          load_row(v, trow);
-        }
         if (!tr.early && tr.row) {  // into L2 now, into registers once Q is in TMEM
           asm volatile("prefetch.global.L2 [%0];" ::"l"(trow));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(trow + 64));
@@ -916,27 +1001,39 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
             rtab[sidx * tstride + d] = make_float2(cs, sn);
           }
         }
-        // visibility of the 2B response keys for this row (bit k of vis0 / vis1 = key k / 32 + k)
-        uint32_t vis0 = 0, vis1 = 0;
+        // visibility of the 2B response keys from each response slot: one ballot per slot and
+        // key half (lane l evaluates keys l and 32 + l); warp w takes slots w, w + 4, ...
         if (has_tail) {
-          const uint32_t own_lo = __shfl_sync(0xffffffffu, lab_lo, s_slot & 31);
-          const uint32_t own_hi = __shfl_sync(0xffffffffu, lab_hi, s_slot & 31);
-          const int th = row_threshold((uint8_t)(s_slot < 32 ? own_lo : own_hi));
-          for (int k = 0; k < twoB; ++k) {
-            const uint32_t lk = __shfl_sync(0xffffffffu, k < 32 ? lab_lo : lab_hi, k & 31);
-            if (response_key_visible((uint8_t)lk, th)) {
-              if (k < 32)
-                vis0 |= 1u << k;
-              else
-                vis1 |= 1u << (k - 32);
+          const int th_lo = row_threshold((uint8_t)lab_lo), th_hi = row_threshold((uint8_t)lab_hi);
+          for (int sl = warp; sl < twoB; sl += 4) {
+            const int th = __shfl_sync(0xffffffffu, sl < 32 ? th_lo : th_hi, sl & 31);
+            const uint32_t b0 = __ballot_sync(0xffffffffu, lane < twoB && response_key_visible((uint8_t)lab_lo, th));
+            const uint32_t b1 =
+                __ballot_sync(0xffffffffu, lane + 32 < twoB && response_key_visible((uint8_t)lab_hi, th));
+            if (lane == 0) {
+              sh->vis[sl][0] = b0;
+              sh->vis[sl][1] = b1;
             }
           }
-          if (!real) {
+        }
+        if (warp_active) {
+          if (real && q_ok) load_row(v, a.q + orow * kD);
+        } else if (tr.early && tr.row && t_ok) {
+          load_row(v, trow);
+        }
+        ptx::named_bar_sync(1, 128);
+        // this row's visibility bits (bit k of vis0 / vis1 = key k / 32 + k); padding rows see
+        // every response key (their scores stay finite)
+        uint32_t vis0 = 0, vis1 = 0;
+        if (has_tail) {
+          if (real) {
+            vis0 = sh->vis[s_slot][0];
+            vis1 = sh->vis[s_slot][1];
+          } else {
             vis0 = twoB >= 32 ? 0xffffffffu : ((1u << twoB) - 1u);
             vis1 = twoB >= 64 ? 0xffffffffu : (twoB > 32 ? ((1u << (twoB - 32)) - 1u) : 0u);
           }
         }
-        ptx::named_bar_sync(1, 128);
         if (warp_active) {
           if (real) {
             rope_row(v, rtab + s_slot * tstride, a.scale_log2);
@@ -950,7 +1047,29 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         } else if (tr.early && tr.row && tr.k) {
           rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
         }
-        if (!tr.early && has_tail) {
+        if constexpr (kPair) {
+          // this CTA's part of the tail tile: threads 0..31 tail K rows 32 crank + t (all dims,
+          // rotated), threads 64..127 dims [64 crank, 64 crank + 64) of tail V row t - 64;
+          // rows at or beyond 2B are zero
+          if (has_tail && (tid < 32 || tid >= 64)) {
+            const bool isk = tid < 32;
+            const int key = isk ? 32 * crank + tid : tid - 64;
+            const bool ld = key < twoB;
+            const size_t pidx = (((size_t)b * twoB + (ld ? key : 0)) * a.Hkv + h) * kD;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
+            if (ld && chk((int64_t)pidx, kD, (int64_t)a.batch * twoB * a.Hkv * kD, a.dev_err)) {
+              if (isk) {
+                load_row(v, a.k_resp + pidx);
+                rope_row(v, rtab + key * tstride, 1.f);
+              } else {
+                const uint4* src = reinterpret_cast<const uint4*>(a.v_resp + pidx + 64 * crank);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = __ldg(src + c);
+              }
+            }
+          }
+        } else if (!tr.early && has_tail) {
           if (tr.row && t_ok) {
             load_row(v, trow);
             if (tr.k) rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
@@ -964,7 +1083,16 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           loads_signalled = true;
         }
         ptx::named_bar_sync(1, 128);  // table reads done
-        if (tr.early) {
+        if constexpr (kPair) {
+          if (has_tail) {
+            if (tid < 32) {
+              store_row_sw(tailk, kPTailKHalf, tid, v);
+            } else if (tid >= 64) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(tailv + sw128(tid - 64, c)) = v[c];
+            }
+          }
+        } else if (tr.early) {
           if (tr.row) store_row_sw(tr.k ? tailk : tailv, kTailHalf, tr.key, v);
           // keys 2B .. 63 of both tail tiles are zero (the tail MMAs read 64 keys)
           const uint4 z[16] = {};
@@ -977,7 +1105,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kQFull));
+        arrive_x(kQFull);
         float m_used = -INFINITY, l = 0.f;
         const uint32_t jfirst = j;
         // The next segment's Q rows, tail rows and labels go into L2 a few tiles before this
@@ -999,7 +1127,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err, wait_ns));
           if (!ok) break;
           if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
-            ptx::mbar_arrive(bar(kPFull0 + buf));
+            arrive_x(kPFull0 + buf);
             continue;
           }
           ptx::tc_fence_after();
@@ -1085,7 +1213,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           l += lsum;
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(kPFull0 + buf));
+          arrive_x(kPFull0 + buf);
         }
         if (!ok) break;
         // ---- epilogue: wait for the last P V, then O / l (or the partial)
@@ -1149,9 +1277,17 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+  if constexpr (kPair) {
+    // the even CTA's MMAs read this CTA's shared memory and TMEM until its drain: neither CTA
+    // frees TMEM or exits before both are here
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  } else {
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // Merges the pieces of every pair split between units. Block (c, y) reads CTA c's merge
@@ -1274,13 +1410,68 @@ static int rows_per_pair(const simsd_attn_params* p) { return 2 * p->B * (p->Hq 
 // CTAs per schedule unit: two for pairs of more than 128 rows (one per 128-row block).
 static int ctas_per_unit(const simsd_attn_params* p) { return rows_per_pair(p) > 128 ? 2 : 1; }
 
+// The dynamic shared memory attribute of both kernels is set once per device; for the CTA-pair
+// kernel the number of its 2-CTA clusters that fit on the device at once is queried then too.
+static std::mutex g_attr_mutex;
+static bool g_attr_done[64];
+static int g_pair_clusters[64];
+
+static simsd_status set_smem_attr(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (dev >= 0 && dev < 64 && g_attr_done[dev]) return SIMSD_OK;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc128_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)r128::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)r128::kSmemBytes);
+  if (e != cudaSuccess) {
+    record_cuda_error("cudaFuncSetAttribute", e);
+    return SIMSD_ERR_CUDA;
+  }
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(sms & ~1));
+  cfg.blockDim = dim3((unsigned)r128::kThreads);
+  cfg.dynamicSmemBytes = r128::kSmemBytes;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_tc128_kernel<true>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  if (dev >= 0 && dev < 64) {
+    g_pair_clusters[dev] = n;
+    g_attr_done[dev] = true;
+  }
+  return SIMSD_OK;
+}
+
+static int pair_clusters_resident() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (set_smem_attr(dev) != SIMSD_OK) return 0;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  return g_pair_clusters[dev];
+}
+
 // Persistent grid: one CTA per SM; when every (request, kv head) pair fits on the SMs and
 // prompts are short, one unit per pair instead (no pair is split, nothing to merge).
-// (With `cl` CTAs per unit: at most SMs / cl units.)
+// (With `cl` = 2 CTAs per unit: at most as many units as 2-CTA clusters fit at once.)
 static int grid_units(const simsd_attn_params* p, int cl) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 148;
   sms /= cl;
+  if (cl == 2) {
+    const int nc = pair_clusters_resident();
+    if (nc > 0 && nc < sms) sms = nc;
+  }
   const int64_t pairs = (int64_t)p->batch * p->Hkv;
   const int64_t avg_tiles = 1 + (p->batch > 0 ? (p->cache_tokens / p->batch + kTileKeys - 1) / kTileKeys : 0);
   if (pairs > 0 && pairs <= sms && avg_tiles <= 64) return (int)pairs;
@@ -1299,22 +1490,6 @@ static WsLayout ws_layout(int ctas) {
   return w;
 }
 
-// The dynamic shared memory attribute is set once per device.
-static std::mutex g_attr_mutex;
-static bool g_attr_done[64];
-
-static simsd_status set_smem_attr(int dev) {
-  std::lock_guard<std::mutex> lock(g_attr_mutex);
-  if (dev >= 0 && dev < 64 && g_attr_done[dev]) return SIMSD_OK;
-  const cudaError_t e = cudaFuncSetAttribute(attn_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)r128::kSmemBytes);
-  if (e != cudaSuccess) {
-    record_cuda_error("cudaFuncSetAttribute", e);
-    return SIMSD_ERR_CUDA;
-  }
-  if (dev >= 0 && dev < 64) g_attr_done[dev] = true;
-  return SIMSD_OK;
-}
 
 static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
   int dev = 0;
@@ -1360,7 +1535,8 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   CUtensorMap tmk, tmv;
   const void* kbase = p->cache_tokens > 0 ? p->k_cache : p->k_resp;  // any valid address
   const void* vbase = p->cache_tokens > 0 ? p->v_cache : p->v_resp;
-  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv, kKeys) ||
+  // CTA pairs: each CTA's K box is 64 of a tile's keys (V: all 128 keys, 64 dims)
+  if (!encode_cache_map(&tmk, kbase, a.layout, p->cache_tokens, p->Hkv, a.cl == 2 ? 64 : kKeys) ||
       !encode_cache_map(&tmv, vbase, a.layout, p->cache_tokens, p->Hkv, kKeys)) {
     record_cuda_error("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     return SIMSD_ERR_CUDA;
@@ -1368,18 +1544,25 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   const simsd_status ast = set_smem_attr(dev);
   if (ast != SIMSD_OK) return ast;
   cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute cat[1];
+  cat[0].id = cudaLaunchAttributeClusterDimension;
+  cat[0].val.clusterDim.x = 2;
+  cat[0].val.clusterDim.y = 1;
+  cat[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
   cfg.blockDim = dim3((unsigned)r128::kThreads);
   cfg.dynamicSmemBytes = r128::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, attn_tc128_kernel, tmk, tmv, a);
+  cfg.attrs = a.cl == 2 ? cat : nullptr;
+  cfg.numAttrs = a.cl == 2 ? 1 : 0;
+  const void* kfn = a.cl == 2 ? (const void*)attn_tc128_kernel<true> : (const void*)attn_tc128_kernel<false>;
+  cudaError_t le = a.cl == 2 ? cudaLaunchKernelEx(&cfg, attn_tc128_kernel<true>, tmk, tmv, a)
+                             : cudaLaunchKernelEx(&cfg, attn_tc128_kernel<false>, tmk, tmv, a);
   if (le == cudaSuccess) le = cudaGetLastError();
   if (le != cudaSuccess) {
     cudaFuncAttributes fa;
     char what[200] = "attention kernel launch";
-    if (cudaFuncGetAttributes(&fa, attn_tc128_kernel) == cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, kfn) == cudaSuccess)
       snprintf(what, sizeof(what),
                "attention kernel launch (threads %d, regs %d, max threads %d, dyn smem %u, "
                "max dyn smem %d, static smem %zu, local %zu)",
