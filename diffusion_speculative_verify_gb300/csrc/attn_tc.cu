@@ -26,8 +26,9 @@
 //   softmax warps  : one thread per query row (TMEM lane). Per segment: load + rotate Q
 //                    into TMEM and build the response K/V tail tile; per tile:
 //                    read S from TMEM, apply the mask, and write P = 2^(s - m) (bf16) in
-//                    place over the S columns just read, in one pass unless the running max
-//                    grows by more than 2^8 (then O and the P already written are rescaled);
+//                    place over the S columns just read, in one pass against the running
+//                    max m unless some P would reach 2^16 (then m is raised to the tile's max
+//                    and O and the P already written are rescaled);
 //                    epilogue: O / l to global memory (or the partial to the workspace).
 // Every wait is bounded in time (TcArgs::wait_ns). A wait that gives up raises
 // SIMSD_DEVERR_TIMEOUT and sets the CTA's abort flag. The softmax warps decide to stop
@@ -1140,26 +1141,30 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
             const int n = nvalid - 32 * k;
             return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
           };
-          // One pass in the common case: chunk k's P = 2^(s - m) goes in place over S columns
-          // [16k, 16k + 16), which this thread has already read. If some row's max grows by
-          // more than 2^8 (always on the first tile of a segment), finish the tile's max over
-          // the remaining chunks, rescale O and the P chunks already written, and go on.
+          // One pass in the common case: chunk k's P = 2^(s - m), m the running max, goes in
+          // place over S columns [16k, 16k + 16), which this thread has already read, once the
+          // warp has checked that no row's chunk sum reached 2^16 (so every P of the chunk is
+          // below 2^16; no max pass is needed for that). Otherwise, and for a row that has no
+          // max yet (a segment's first scores), the tile's max is taken over the remaining
+          // chunks, O and the P chunks already written are rescaled, and it goes on.
           float lsum = 0.f;
           int k = 0;
-          bool grew = false;
+          bool grew = __any_sync(0xffffffffu, m_used == -INFINITY);
+          if (!grew) {
 #pragma unroll 1
-          for (; k < nchunks; ++k) {
-            uint32_t r[32];
-            ptx::tmem_ld32(ts + 32 * k, r);
-            ptx::tmem_ld_wait(r);
-            const uint32_t vm = chunk_mask(k);
-            if (__any_sync(0xffffffffu, chunk_max(r, vm) > m_used + 8.f)) {
-              grew = true;
-              break;
+            for (; k < nchunks; ++k) {
+              uint32_t r[32];
+              ptx::tmem_ld32(ts + 32 * k, r);
+              ptx::tmem_ld_wait(r);
+              uint32_t pk[16];
+              const float cs = chunk_exp(r, chunk_mask(k), m_used, pk);
+              if (__any_sync(0xffffffffu, !(cs < 65536.f))) {  // (a NaN sum takes the slow path)
+                grew = true;
+                break;
+              }
+              lsum += cs;
+              ptx::tmem_st16(ts + 16 * k, pk);
             }
-            uint32_t pk[16];
-            lsum += chunk_exp(r, vm, m_used == -INFINITY ? 0.f : m_used, pk);
-            ptx::tmem_st16(ts + 16 * k, pk);
           }
           if (grew) {
             float mt = -INFINITY;
