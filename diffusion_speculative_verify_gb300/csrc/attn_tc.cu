@@ -530,9 +530,9 @@ __device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& 
 }
 
 // =========================================================================================
-// Every operand an MMA reads as A lives in TMEM, which lets each tcgen05.mma run at full
-// rate (an A operand from shared memory, or N < 128, caps an M = 128 instruction well below
-// it):
+// Both MMAs take A from TMEM and run at N = 128 (measured on GB300: 64 cycles per
+// 128 x 128 x 16 instruction, A from TMEM or shared memory alike, and per 256 x 128 x 16
+// over a CTA pair; N = 64 runs about 1.4x slower per flop):
 //   S_j = Q K_j^T   A = rotated Q (TMEM), B = K tile (smem, K-major), N = 128 keys
 //   O  += P_j V_j   A = P_j (TMEM, bf16),  B = V tile (smem, MN-major), N = 128 = D
 // TMEM columns: S buffers [0,128) and [128,256), O [256,384), Q [384,448). P_j (bf16 pairs,
