@@ -1022,6 +1022,15 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         } else if (tr.early && tr.row && t_ok) {
           load_row(v, trow);
         }
+        // The prompt stream may start once every row this prologue loads is in flight (issued
+        // first, they are not queued behind it): here, unless the tail rows come after Q.
+        auto signal_loads = [&]() {
+          if (!loads_signalled) {
+            ptx::mbar_arrive(bar(kLoads));
+            loads_signalled = true;
+          }
+        };
+        if (tr.early || !has_tail) signal_loads();
         ptx::named_bar_sync(1, 128);
         // this row's visibility bits (bit k of vis0 / vis1 = key k / 32 + k); padding rows see
         // every response key (their scores stay finite)
@@ -1062,6 +1071,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
             if (ld && chk((int64_t)pidx, kD, (int64_t)a.batch * twoB * a.Hkv * kD, a.dev_err)) {
               if (isk) {
                 load_row(v, a.k_resp + pidx);
+                signal_loads();
                 rope_row(v, rtab + key * tstride, 1.f);
               } else {
                 const uint4* src = reinterpret_cast<const uint4*>(a.v_resp + pidx + 64 * crank);
@@ -1073,16 +1083,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         } else if (!tr.early && has_tail) {
           if (tr.row && t_ok) {
             load_row(v, trow);
+            signal_loads();
             if (tr.k) rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
           } else {
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
           }
         }
-        if (!loads_signalled) {  // this prologue's rows have landed: the prompt stream may start
-          ptx::mbar_arrive(bar(kLoads));
-          loads_signalled = true;
-        }
+        signal_loads();  // (threads without a tail row)
         ptx::named_bar_sync(1, 128);  // table reads done
         if constexpr (kPair) {
           if (has_tail) {
