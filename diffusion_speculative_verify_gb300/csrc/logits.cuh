@@ -130,15 +130,18 @@ template <typename K>
 int resident_blocks(K kernel, int threads, int* cache) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cache[dev] == 0) {
+  // (host threads may race here: each computes the same value; the accesses are atomic)
+  int v = __atomic_load_n(&cache[dev], __ATOMIC_ACQUIRE);
+  if (v == 0) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     const int sms = device_sm_count();
-    cache[dev] = per_sm * (sms > 0 ? sms : 148);
+    v = per_sm * (sms > 0 ? sms : 148);
+    __atomic_store_n(&cache[dev], v, __ATOMIC_RELEASE);
   }
-  return cache[dev];
+  return v;
 }
 
 }  // namespace simsd
