@@ -14,15 +14,18 @@
 // partial pairs (its first and last), whose (O, max, sum) partials are merged by
 // attn_tc_merge_kernel, a programmatic dependent launch.
 //
-// A schedule unit is one CTA for pairs of up to 128 rows and two CTAs (rows [0, 128) and
-// [128, 256)) above that; the two walk the same tiles, each loading every prompt tile into
-// its own shared memory (the second read of a tile mostly hits L2). Per CTA, warp roles:
+// A schedule unit is one CTA for pairs of up to 128 rows and, above that, a CTA pair (a
+// 2-CTA cluster, rows [0, 128) and [128, 256)) whose MMAs span both CTAs (tcgen05
+// cta_group::2, M = 256); each CTA of a pair loads only its half of every prompt tile, so a
+// tile crosses from memory once per pair. Per CTA, warp roles:
 //   producer warp  : TMA loads of prompt K and V tiles (128-byte swizzle) into a ring of
-//                    three 64 KB shared-memory slots.
+//                    three 64 KB shared-memory slots (CTA pairs: six 32 KB slots).
 //   MMA warp       : one thread issues S = Q K^T (M = 128 rows, N = 128 keys, K = 128; A =
 //                    the rotated Q in TMEM) into one of two TMEM S buffers, then O += P V
 //                    (M = 128, N = 128 = D, K = 128 keys; A = bf16 P in TMEM) into the TMEM O
 //                    accumulator; completion is signalled with tcgen05.commit to mbarriers.
+//                    (CTA pairs: the even CTA's thread issues for both; the odd CTA's MMA warp
+//                    forwards the completion of its own copies.)
 //   softmax warps  : one thread per query row (TMEM lane). Per segment: load + rotate Q
 //                    into TMEM and build the response K/V tail tile; per tile:
 //                    read S from TMEM, apply the mask, and write P = 2^(s - m) (bf16) in
@@ -1628,7 +1631,7 @@ simsd_status launch_attn_tc(const simsd_attn_params* p, void* ws, size_t ws_byte
     return SIMSD_ERR_UNSUPPORTED;
   if (p->cache_tokens > 0 && ((((uintptr_t)p->k_cache) | ((uintptr_t)p->v_cache)) & mask))
     return SIMSD_ERR_UNSUPPORTED;
-  // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: two CTAs
+  // up to 128 rows per pair: one CTA per schedule unit; 129..256 rows: a CTA pair
   return tc::launch(p, ws, ws_bytes, stream);
 }
 

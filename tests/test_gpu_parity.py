@@ -220,8 +220,8 @@ def test_attention_bf16_ragged_tiles_full_compare(layout, B):
 
 @pytest.mark.parametrize("Hq,Hkv,B", [(6, 2, 32), (10, 2, 13), (8, 1, 9)])
 def test_attention_bf16_two_ctas_partial_second_block(Hq, Hkv, B):
-    # 2B*G rows per (request, kv-head) pair between 129 and 255: the pair runs on two CTAs
-    # whose second one holds a partial row block (64, 2 and 16 rows)
+    # 2B*G rows per (request, kv-head) pair between 129 and 255: the pair runs on a CTA pair
+    # (2-CTA cluster) whose second CTA holds a partial row block (64, 2 and 16 rows)
     w = MEDIUM.with_(Hq=Hq, Hkv=Hkv, B=B, gamma=B)
     assert 128 < 2 * B * (Hq // Hkv) < 256
     inputs, meta = H.make_case(w, seed=100 + B, prompt_len=[0, 61, 128, 1000 + 37])
