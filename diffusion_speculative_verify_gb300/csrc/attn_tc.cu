@@ -638,6 +638,9 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
+      // (launched as a programmatic dependent of the layout kernel: no input is read before
+      // that grid has completed)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       // When every unit is one pair, this unit's pair is known before the schedule: its
       // first prompt tiles go into L2 now, so that the stream, which starts after the first
       // prologue, finds them there.
@@ -693,8 +696,10 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         prefetch_prologue(a, gb, gh, 1, 2 * a.B, real ? prow / a.G : 0, real ? prow % a.G : 0,
                           real, rw, tid);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // (the schedule reads the labels)
     block_schedule(a, vcta, a.ctas, tid, sh->wsum, &sh->T, &sh->t0, &sh->t1, &sh->Tb, &sh->b);
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // every thread, before its first input read
   ptx::tc_fence_before();
   if constexpr (kPair) {
     ptx::cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
@@ -1560,17 +1565,21 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   const simsd_status ast = set_smem_attr(dev);
   if (ast != SIMSD_OK) return ast;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute cat[1];
-  cat[0].id = cudaLaunchAttributeClusterDimension;
-  cat[0].val.clusterDim.x = 2;
-  cat[0].val.clusterDim.y = 1;
-  cat[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute cat[2];
+  // a programmatic dependent of the stream's previous kernel (the layout kernel), and with
+  // CTA pairs a 2-CTA cluster
+  cat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cat[0].val.programmaticStreamSerializationAllowed = 1;
+  cat[1].id = cudaLaunchAttributeClusterDimension;
+  cat[1].val.clusterDim.x = 2;
+  cat[1].val.clusterDim.y = 1;
+  cat[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(a.ctas * a.cl));
   cfg.blockDim = dim3((unsigned)r128::kThreads);
   cfg.dynamicSmemBytes = r128::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = a.cl == 2 ? cat : nullptr;
-  cfg.numAttrs = a.cl == 2 ? 1 : 0;
+  cfg.attrs = cat;
+  cfg.numAttrs = a.cl == 2 ? 2 : 1;
   const void* kfn = a.cl == 2 ? (const void*)attn_tc128_kernel<true> : (const void*)attn_tc128_kernel<false>;
   cudaError_t le = a.cl == 2 ? cudaLaunchKernelEx(&cfg, attn_tc128_kernel<true>, tmk, tmv, a)
                              : cudaLaunchKernelEx(&cfg, attn_tc128_kernel<false>, tmk, tmv, a);

@@ -18,6 +18,10 @@ __global__ void __launch_bounds__(128) build_layout_kernel(
     const int32_t* __restrict__ tau, const int32_t* __restrict__ prompt_len, int batch, int B,
     int mask_pos_offset, int32_t* __restrict__ pos_ids, uint8_t* __restrict__ labels,
     uint32_t* __restrict__ dev_err) {
+  // launched as a programmatic dependent of the stream's previous kernel: let the attention
+  // grid be placed at once, and read nothing before the previous grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= batch) return;
@@ -70,8 +74,21 @@ SIMSD_API simsd_status simsd_build_layout_ex(const int32_t* tau, const int32_t* 
   const int warps = 4;
   const int grid = (batch + warps - 1) / warps;
   const int offset = (flags & SIMSD_LAYOUT_PHYSICAL_POSITIONS) ? B : 0;
-  simsd::build_layout_kernel<<<grid, warps * 32, 0, (cudaStream_t)stream>>>(
-      tau, prompt_len, batch, B, offset, pos_ids, labels, dev_err);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)(warps * 32));
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, simsd::build_layout_kernel, tau, prompt_len, batch, B,
+                                           offset, pos_ids, labels, dev_err);
+  if (e != cudaSuccess) {
+    simsd::record_cuda_error("cudaLaunchKernelEx(build_layout_kernel)", e);
+    return SIMSD_ERR_CUDA;
+  }
   return simsd::last_launch_status();
 }
 
