@@ -19,13 +19,14 @@
 // cta_group::2, M = 256); each CTA of a pair loads only its half of every prompt tile, so a
 // tile crosses from memory once per pair. Per CTA, warp roles:
 //   producer warp  : TMA loads of prompt K and V tiles (128-byte swizzle) into a ring of
-//                    three 64 KB shared-memory slots (CTA pairs: six 32 KB slots).
+//                    three 64 KB shared-memory slots (CTA pairs: five 32 KB slots).
 //   MMA warp       : one thread issues S = Q K^T (M = 128 rows, N = 128 keys, K = 128; A =
 //                    the rotated Q in TMEM) into one of two TMEM S buffers, then O += P V
 //                    (M = 128, N = 128 = D, K = 128 keys; A = bf16 P in TMEM) into the TMEM O
 //                    accumulator; completion is signalled with tcgen05.commit to mbarriers.
 //                    (CTA pairs: the even CTA's thread issues for both; the odd CTA's MMA warp
-//                    forwards the completion of its own copies.)
+//                    forwards the completion of its own copies; Q is read from shared memory
+//                    and three S buffers rotate in TMEM.)
 //   softmax warps  : one thread per query row (TMEM lane). Per segment: load + rotate Q
 //                    into TMEM and build the response K/V tail tile; per tile:
 //                    read S from TMEM, apply the mask, and write P = 2^(s - m) (bf16) in
@@ -278,10 +279,11 @@ struct PromptTiles {
 };
 
 // --------------------------------------------------------------------- small helpers
-// Barriers: ring slots (full / empty); per S buffer: S written, the P V that read it
-// completed, P written; Q and tail stored; MMA drain; the first prologue's loads landed.
-enum BarIdx { kFull0 = 0, kEmpty0 = kMaxSlots, kSFull0 = 2 * kMaxSlots, kSFree0 = kSFull0 + 2,
-              kPFull0 = kSFree0 + 2, kQFull = kPFull0 + 2, kDrain = kQFull + 1,
+// Barriers: ring slots (full / empty); per S buffer (two, or three with CTA pairs): S
+// written, the P V that read it completed, P written; Q and tail stored; MMA drain; the first
+// prologue's loads landed.
+enum BarIdx { kFull0 = 0, kEmpty0 = kMaxSlots, kSFull0 = 2 * kMaxSlots, kSFree0 = kSFull0 + 3,
+              kPFull0 = kSFree0 + 3, kQFull = kPFull0 + 3, kDrain = kQFull + 1,
               kLoads = kDrain + 1, kNumBars = kLoads + 1 };
 
 struct Shared {
@@ -542,6 +544,11 @@ __device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& 
 // 64 columns) is written in place over the first columns of S_j, which the softmax has
 // already read, so P double-buffers with S; an S buffer is released by the commit of the
 // P V that read its P.
+// CTA pairs take A of S = Q K^T from shared memory instead (this CTA's 128 rotated Q rows,
+// 128-byte swizzle, behind a five-slot ring), which frees TMEM for a third S buffer:
+// S [0,128), [128,256), [256,384), O [384,512). S_{j+3} then waits for P_j V_j instead of
+// S_{j+2}, so the chain last P_j -> P_j V_j -> next S into that buffer has a tile of slack
+// against the softmax.
 // Warps 0-3: softmax (thread = row = TMEM lane; warps whose 32 rows are all padding skip
 // their work), warp 4: TMA producer, warp 5: MMA issuer (non-blocking event loop).
 namespace r128 {
@@ -549,7 +556,6 @@ constexpr uint32_t kHalf = kKeys * 128;          // 16 KB: one 64-element half o
 constexpr uint32_t kKV = 2 * kHalf;              // 32 KB
 constexpr uint32_t kStage = 2 * kKV;             // 64 KB: K + V
 constexpr int kStages = 3;
-constexpr int kAhead = kStages - 1;              // S runs up to 2 tiles ahead of P V
 constexpr uint32_t kTailHalf = 64 * 128;         // tail tile: 2B <= 64 keys, 64-key layout
 constexpr uint32_t kTailKV = 2 * kTailHalf;      // 16 KB
 constexpr uint32_t kOffStages = 0;
@@ -566,15 +572,18 @@ static_assert(kStages <= kMaxSlots, "stage barriers");
 // [32 r, 32 r + 32), tail V dims [64 r, 64 r + 64) of all 64 tail keys.
 constexpr uint32_t kPKHalf = 64 * 128;                    // 8 KB
 constexpr uint32_t kPStage = 2 * kPKHalf + kKeys * 128;   // 32 KB
-constexpr int kPStages = 6;
+constexpr int kPStages = 5;
 constexpr uint32_t kPTailKHalf = 32 * 128;                // 4 KB
-static_assert(kPStages * kPStage == kStages * kStage, "one ring size for both modes");
+constexpr uint32_t kPOffQ = kOffStages + kPStages * kPStage;  // 32 KB: Q as two 64-dim halves
+constexpr uint32_t kPTmemO = 384;
+static_assert(kPOffQ + 2 * kHalf == kOffTail, "ring + Q of a CTA pair fill the single-CTA ring");
 static_assert(kPStages <= kMaxSlots, "stage barriers");
 }  // namespace r128
 
 // kPair: the two CTAs of a schedule unit form a cluster and one tcgen05.mma (cta_group::2,
 // M = 256) covers both 128-row blocks; each CTA loads only its half of every K and V tile
-// (above), so a tile crosses from memory once per pair, and the ring holds six tiles.
+// (above), so a tile crosses from memory once per pair; the ring holds five tiles, Q sits
+// in shared memory and three S buffers rotate in TMEM.
 // The even CTA issues every MMA; the odd CTA's MMA warp forwards the completion of its own
 // copies to the even CTA's ring barriers.
 template <bool kPair>
@@ -590,6 +599,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   constexpr uint32_t VOFF = 2 * KHALF;                  // V within a stage
   constexpr uint32_t TKHALF = kPair ? kPTailKHalf : kTailHalf;
   constexpr int MROWS = kPair ? 256 : 128;              // rows of one MMA
+  constexpr int NSB = kPair ? 3 : 2;                    // S buffers in TMEM
+  constexpr uint32_t TMO = kPair ? kPTmemO : kTmemO;    // O accumulator column
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // let the merge grid be placed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -606,9 +617,10 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   const int vcta = blockIdx.x / cl, crank = blockIdx.x - vcta * cl;
   const int row0 = crank * 128;  // first pair row of this CTA
   const uint64_t wait_ns = a.wait_ns;
-  // kPFull0 + b: P of the tile in S buffer b written. kSFree0 + b: the P V that read S
-  // buffer b completed; its phase for tile j is j / 2, and the previous phase (tile j - 2) is
-  // always complete by the time anyone waits for tile j, so a parity wait is unambiguous.
+  // Tile j uses S buffer j % NSB. kPFull0 + b: P of the tile in S buffer b written.
+  // kSFree0 + b: the P V that read S buffer b completed; its phase for tile j is j / NSB, and
+  // the previous phase (tile j - NSB) is always complete by the time anyone waits for tile j,
+  // so a parity wait is unambiguous.
   // With kPair, the ring barriers count this CTA's own copies; the even CTA's full barriers
   // also wait for the odd CTA's forwarded arrival, and its P and Q barriers count one arrival
   // per softmax warp of both CTAs. Every other barrier is arrived at by MMA commits, in both
@@ -662,7 +674,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ptx::mbar_init(bar(kFull0 + i), lead ? 2 : 1);
         ptx::mbar_init(bar(kEmpty0 + i), 1);
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < NSB; ++i) {
         ptx::mbar_init(bar(kSFull0 + i), 1);
         ptx::mbar_init(bar(kSFree0 + i), 1);
         ptx::mbar_init(bar(kPFull0 + i), kPair ? 8 : 128);
@@ -782,6 +794,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         else
           ptx::mma_f16_ts(d, at, bd, id, acc);
       };
+      // S = Q K^T, K step kk: A = Q from TMEM, or with kPair from shared memory
+      auto mma_s = [&](uint32_t d, int kk, uint64_t bd, uint32_t id, uint32_t acc) {
+        if constexpr (kPair)
+          ptx::mma_f16_ss_pair(d, ptx::sdesc_sw128(sbase + kPOffQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+                               bd, id, acc);
+        else
+          ptx::mma_f16_ts(d, tmem + kTmemQ + kk * 8, bd, id, acc);
+      };
       auto commit = [&](uint32_t b) {  // with kPair: the barrier of both CTAs
         if constexpr (kPair)
           ptx::mma_commit_pair_both(b);
@@ -823,29 +843,27 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         return false;
       };
       int stage_of[8];  // per tile (ring): slot to release after its P V, -1 = tail tile
-      static_assert(kAhead + 1 <= 8, "tile ring");
+      static_assert(NSB + 1 <= 8, "tile ring");
       auto try_issue_s = [&](uint32_t jj, int i) -> bool {
-        const int buf = jj & 1;
+        const int buf = jj % NSB;
         const int s = m % NSTG;
         if (i != 0 && !ptx::mbar_test(bar(kFull0 + s), (m / NSTG) & 1)) return false;
-        if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj >> 1) & 1) ^ 1)) return false;
+        if (!ptx::mbar_test(bar(kSFree0 + buf), ((jj / NSB) & 1) ^ 1)) return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem + kTmemS0 + buf * 128;
         if (i == 0) {
           const uint32_t kaddr = sbase + kOffTail;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            mma(d, tmem + kTmemQ + kk * 8,
-                ptx::sdesc_sw128(kaddr + (kk >> 2) * TKHALF + (kk & 3) * 32, 16, 1024), idS_tail,
-                kk > 0 ? 1u : 0u);
+            mma_s(d, kk, ptx::sdesc_sw128(kaddr + (kk >> 2) * TKHALF + (kk & 3) * 32, 16, 1024), idS_tail,
+                  kk > 0 ? 1u : 0u);
           stage_of[jj & 7] = -1;
         } else {
           const uint32_t kaddr = sbase + kOffStages + s * STG;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            mma(d, tmem + kTmemQ + kk * 8,
-                ptx::sdesc_sw128(kaddr + (kk >> 2) * KHALF + (kk & 3) * 32, 16, 1024), idS,
-                kk > 0 ? 1u : 0u);
+            mma_s(d, kk, ptx::sdesc_sw128(kaddr + (kk >> 2) * KHALF + (kk & 3) * 32, 16, 1024), idS,
+                  kk > 0 ? 1u : 0u);
           stage_of[jj & 7] = s;
           ++m;
         }
@@ -855,15 +873,15 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       // V as B is N-major: 16 keys (rows of 128 bytes) per K step; with kPair each CTA holds
       // a single 64-dim column of atoms, so the leading (N) offset is never used.
       auto try_issue_pv = [&](uint32_t jj, bool first_in_seg) -> bool {
-        const int buf = jj & 1;
-        if (!ptx::mbar_test(bar(kPFull0 + buf), (jj >> 1) & 1)) return false;
+        const int buf = jj % NSB;
+        if (!ptx::mbar_test(bar(kPFull0 + buf), (jj / NSB) & 1)) return false;
         ptx::tc_fence_after();
         const int s = stage_of[jj & 7];
         const uint32_t vaddr = s < 0 ? sbase + kOffTail + kTailKV : sbase + kOffStages + s * STG + VOFF;
         const uint32_t lbo = s < 0 ? kTailHalf : kHalf;
         const int nk = s < 0 ? 4 : kKeys / 16;
         for (int kk = 0; kk < nk; ++kk)
-          mma(tmem + kTmemO, tmem + kTmemS0 + buf * 128 + kk * 8,
+          mma(tmem + TMO, tmem + kTmemS0 + buf * 128 + kk * 8,
               ptx::sdesc_sw128(vaddr + kk * 16 * 128, lbo, 1024), idPV, (first_in_seg && kk == 0) ? 0u : 1u);
         commit(bar(kSFree0 + buf));
         if (s >= 0) commit(bar(kEmpty0 + s));
@@ -888,7 +906,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
             ++npv;
             progressed = true;
           }
-          if (ns < jend && ns <= npv + kAhead && try_issue_s(ns, it.i0 + (int)(ns - jfirst))) {
+          if (ns < jend && ns <= npv + NSB && try_issue_s(ns, it.i0 + (int)(ns - jfirst))) {
             ++ns;
             progressed = true;
           }
@@ -920,7 +938,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     const int s_slot = real ? prow / a.G : 0;
     const int g = real ? prow % a.G : 0;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tmem_o = tmem + lane_off + kTmemO;
+    const uint32_t tmem_o = tmem + lane_off + TMO;
     uint8_t* tailk = smem + kOffTail;
     uint8_t* tailv = tailk + kTailKV;
     const int rw = (min(128, a.R - row0) + 31) & ~31;  // threads below rw own this block's rows
@@ -1059,9 +1077,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = make_uint4(0, 0, 0, 0);
           }
-          // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
-          tmem_st_row(tmem + lane_off + kTmemQ, v);
-          ptx::tmem_st_wait();
+          if constexpr (kPair) {
+            store_row_sw(smem + kPOffQ, kHalf, row, v);  // A of S, K-major, 128-byte swizzle
+          } else {
+            // row -> TMEM lane, dims (2c, 2c+1) -> column c (bf16 pair, low half first)
+            tmem_st_row(tmem + lane_off + kTmemQ, v);
+            ptx::tmem_st_wait();
+          }
         } else if (tr.early && tr.row && tr.k) {
           rope_row(v, rtab + tr.key * tstride, 1.f);  // K rotated, V as is
         }
@@ -1138,10 +1160,10 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         }
         const int pf_at = max(it.i0, it.i0 + it.n - kPrefetchAhead);
         for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
-          const int buf = j & 1;
+          const int buf = j % NSB;
           if (pf_b >= 0 && i == pf_at)
             prefetch_prologue(a, pf_b, pf_h & 0xffff, pf_h >> 16, twoB, s_slot, g, real, rw, tid);
-          ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j >> 1) & 1, a.dev_err, wait_ns));
+          ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j / NSB) & 1, a.dev_err, wait_ns));
           if (!ok) break;
           if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
             arrive_x(kPFull0 + buf);
@@ -1162,11 +1184,14 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           // warp has checked that no row's chunk sum reached 2^16 (so every P of the chunk is
           // below 2^16; no max pass is needed for that). Otherwise, and for a row that has no
           // max yet (a segment's first scores), the tile's max is taken over the remaining
-          // chunks, O and the P chunks already written are rescaled, and it goes on.
+          // chunks, O and the P chunks already written are rescaled, and it goes on. With CTA
+          // pairs (softmax-bound) chunks go two at a time (nchunks is even): one load wait and
+          // one vote per 64 columns; the single-CTA kernel (stream-bound) measured faster with
+          // one chunk at a time.
           float lsum = 0.f;
           int k = 0;
           bool grew = __any_sync(0xffffffffu, m_used == -INFINITY);
-          if (!grew) {
+          if (!grew && !kPair) {
 #pragma unroll 1
             for (; k < nchunks; ++k) {
               uint32_t r[32];
@@ -1180,6 +1205,25 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
               }
               lsum += cs;
               ptx::tmem_st16(ts + 16 * k, pk);
+            }
+          } else if (!grew) {
+#pragma unroll 1
+            for (; k < nchunks; k += 2) {
+              uint32_t r[32], r2[32];
+              ptx::tmem_ld32(ts + 32 * k, r);
+              ptx::tmem_ld32(ts + 32 * k + 32, r2);
+              ptx::tmem_ld_wait(r);
+              ptx::tmem_ld_wait(r2);
+              uint32_t pk[16], pk2[16];
+              const float cs = chunk_exp(r, chunk_mask(k), m_used, pk);
+              const float cs2 = chunk_exp(r2, chunk_mask(k + 1), m_used, pk2);
+              if (__any_sync(0xffffffffu, !(cs < 65536.f) || !(cs2 < 65536.f))) {  // (NaN: slow path)
+                grew = true;
+                break;
+              }
+              lsum += cs + cs2;
+              ptx::tmem_st16(ts + 16 * k, pk);
+              ptx::tmem_st16(ts + 16 * k + 16, pk2);
             }
           }
           if (grew) {
@@ -1195,7 +1239,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
             const float alpha = m_used == -INFINITY ? 0.f : ptx::ex2(m_used - m_new);
             if (j != jfirst) {  // O holds P V of earlier tiles: rescale it once the last P V landed
               const uint32_t jp = j - 1;
-              ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jp & 1)), (jp >> 1) & 1,
+              ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + jp % NSB), (jp / NSB) & 1,
                                                     a.dev_err, wait_ns));
               if (!ok) break;
               ptx::tc_fence_after();
@@ -1239,7 +1283,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         if (!ok) break;
         // ---- epilogue: wait for the last P V, then O / l (or the partial)
         const uint32_t jl = j - 1;
-        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + (jl & 1)), (jl >> 1) & 1, a.dev_err, wait_ns));
+        ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + jl % NSB), (jl / NSB) & 1, a.dev_err, wait_ns));
         if (!ok) break;
         ptx::tc_fence_after();
         if (warp_active && chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err) &&

@@ -229,6 +229,16 @@ __device__ __forceinline__ void mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (+)= A[smem desc] * B[smem desc] over both CTAs of the pair (issued by the even CTA): A
+// split by rows (each CTA's 128 rows at the same shared-memory offset), B by columns.
+__device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive (count 1) on the mbarrier at offset `bar` of both CTAs of the pair once every
 // tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
