@@ -618,10 +618,9 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_throughput(args.workload, args.cpu_seconds, ov=_overrides(args))
 
-    # layout; attention (the tensor-core kernel and its split merge, or the fp32 / D 64
-    # kernel alone); accept_stats and accept_finish
-    tc_path = w.dtype == "bf16" and w.D == 128 and 2 * w.B * (w.Hq // w.Hkv) <= 256
-    launches_per_step = 1 + (2 if tc_path else 1) + 2 + (2 if khat_mode is not None else 0)
+    # layout; attention (one kernel: the tensor-core kernel merges split pairs itself, and
+    # the fp32 / D 64 path is one kernel too); accept_stats and accept_finish
+    launches_per_step = 1 + 1 + 2 + (2 if khat_mode is not None else 0)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -11,8 +11,11 @@
 // stream the prompt keys, 128 at a time. All pairs' tiles, each pair with a start-up share
 // (its prologue and epilogue cost in tile units), are concatenated and cut into equal
 // contiguous ranges, one per schedule unit (stream-K); a unit therefore sees at most two
-// partial pairs (its first and last), whose (O, max, sum) partials are merged by
-// attn_tc_merge_kernel, a programmatic dependent launch.
+// partial pairs (its first and last). A pair split between units is merged inside the
+// kernel: every piece but the first writes its (O, max, sum) partial to the workspace and
+// publishes it with a flag; the unit holding the first piece (the last segment of its
+// range, so the last piece to finish) waits for those flags and combines the partials with
+// its own O, still in TMEM.
 //
 // A schedule unit is one CTA for pairs of up to 128 rows and, above that, a CTA pair (a
 // 2-CTA cluster, rows [0, 128) and [128, 256)) whose MMAs span both CTAs (tcgen05
@@ -66,8 +69,10 @@ constexpr int kMaxSlots = 8;                        // ring barriers reserved in
 // GB300, 2B = 16 costs about 5 tiles and 2B = 64 about 8 to 10.
 static int seg_cost_tiles(int twoB) { return 4 + twoB / 16; }
 constexpr int kPrefetchAhead = 4;  // tiles before a segment's end at which the next one is prefetched
-
-struct MergeDesc;
+// Merge of a split pair: partials staged in shared memory two at a time.
+constexpr int kMergeBatch = 2;
+constexpr uint32_t kMergeO = kBlockRows * kD * 4;   // 64 KB: one piece's O rows (fp32)
+constexpr uint32_t kMergeML = kBlockRows * 8;       // 1 KB: its (max, sum) per row
 
 struct TcArgs {
   int batch, B, Hq, Hkv, G, R, ctas;  // R = 2B*G real rows per pair; ctas: schedule units
@@ -89,16 +94,8 @@ struct TcArgs {
   uint32_t* dev_err;
   float* ws_o;         // [2 * ctas * cl][128][128] partial numerators
   float2* ws_ml;       // [2 * ctas * cl][128] partial (max, sum), log2 domain
-  MergeDesc* ws_desc;  // [ctas * cl] split pair starting in each CTA (or none)
+  uint64_t* ws_flag;   // [2 * ctas * cl] partial published (the launch's token) or not
   RopeTable rope;
-};
-
-// Written by every CTA for the pair its range ends in, when that pair started inside the
-// range and continues past it; the merge kernel combines that pair's pieces.
-struct MergeDesc {
-  int b, h, c_last, piece0;  // b < 0: no split pair starts here; c_last: last unit holding a
-                             // piece; piece0: the piece's slot in this CTA (0 first, 1 last)
-  long long T;
 };
 
 // Workspace slot of a partial: CTA `cta`, piece 0 (its range's first segment) or 1 (its last).
@@ -281,10 +278,10 @@ struct PromptTiles {
 // --------------------------------------------------------------------- small helpers
 // Barriers: ring slots (full / empty); per S buffer (two, or three with CTA pairs): S
 // written, the P V that read it completed, P written; Q and tail stored; MMA drain; the first
-// prologue's loads landed.
+// prologue's loads landed; the partials of a split pair copied in for its merge.
 enum BarIdx { kFull0 = 0, kEmpty0 = kMaxSlots, kSFull0 = 2 * kMaxSlots, kSFree0 = kSFull0 + 3,
               kPFull0 = kSFree0 + 3, kQFull = kPFull0 + 3, kDrain = kQFull + 1,
-              kLoads = kDrain + 1, kNumBars = kLoads + 1 };
+              kLoads = kDrain + 1, kMerge = kLoads + 1, kNumBars = kMerge + 1 };
 
 struct Shared {
   uint64_t bars[kNumBars];
@@ -505,9 +502,28 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint4 (&v)[16]
   }
 }
 
+// Flags of published partials: written with release and read with acquire at GPU scope.
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// The value a partial's flag takes in this launch: the grid's launch number, top bit set (so
+// never 0, the value every CTA gives its own flags at entry; replays of a CUDA graph reuse
+// the number, which is why flags are also cleared once merged).
+__device__ __forceinline__ uint64_t launch_token() {
+  uint64_t g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return g | (1ull << 63);
+}
+
 // This thread's output row of a segment the CTA did not finish: a whole pair's row (and its
-// lse) becomes NaN; a piece of a split pair gets a NaN partial, which the merge carries into
-// the pair's output. Invalid requests get their zero rows as usual.
+// lse) becomes NaN, and so does a split pair's when this is its first piece (the CTA that
+// merges the pair); a later piece gets a NaN partial (published like any partial), which the
+// merge carries into the pair's output. Invalid requests get their zero rows as usual.
 __device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& it, bool real,
                                                 size_t orow, size_t slot, int row) {
   if (!real) return;
@@ -523,7 +539,7 @@ __device__ __forceinline__ void mark_unfinished(const TcArgs& a, const SegIter& 
     return;
   }
   const float qnan = __int_as_float(0x7FC00000);
-  if (it.full) {
+  if (it.full || it.i0 == 0) {
     const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
     uint4* o = reinterpret_cast<uint4*>(a.out + orow * kD);
 #pragma unroll
@@ -601,7 +617,8 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
   constexpr int MROWS = kPair ? 256 : 128;              // rows of one MMA
   constexpr int NSB = kPair ? 3 : 2;                    // S buffers in TMEM
   constexpr uint32_t TMO = kPair ? kPTmemO : kTmemO;    // O accumulator column
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // let the merge grid be placed
+  // (No early launch_dependents: a following call on the same workspace must not start
+  // while this grid's CTAs still merge split pairs.)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
@@ -682,6 +699,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
       ptx::mbar_init(bar(kQFull), kPair ? 8 : 128);
       ptx::mbar_init(bar(kDrain), 1);
       ptx::mbar_init(bar(kLoads), 128);
+      ptx::mbar_init(bar(kMerge), 1);
       ptx::fence_mbar_init();
       ptx::prefetch_tensormap(&tmk);
       ptx::prefetch_tensormap(&tmv);
@@ -952,14 +970,27 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ptx::mbar_arrive(bar(i));
       }
     };
+    // Split pairs. This CTA's two partial slots (its range's first and last segment) are
+    // published by setting their flags to the launch token once every row is written; the
+    // flags are cleared here first (and by the merging CTA once consumed), so a flag left
+    // over from an earlier launch is gone long before any CTA of this one looks at it.
+    const uint64_t token = launch_token();
+    const int64_t nslots = (int64_t)2 * a.ctas * a.cl;
+    if (tid == 0 && chk((int64_t)2 * blockIdx.x + 1, 1, nslots, a.dev_err)) {
+      a.ws_flag[2 * blockIdx.x] = 0;
+      a.ws_flag[2 * blockIdx.x + 1] = 0;
+    }
+    // every softmax thread, once its row of the partial in `pslot` is written
+    auto publish = [&](size_t pslot) {
+      __threadfence();
+      ptx::named_bar_sync(1, 128);
+      if (tid == 0 && chk((int64_t)pslot, 1, nslots, a.dev_err)) st_release_u64(a.ws_flag + pslot, token);
+    };
     SegIter it;
     it.init(a, st);
     uint32_t j = 0;
     bool aborted = false;
     bool loads_signalled = false;  // each thread arrives on kLoads once
-    MergeDesc desc;
-    desc.b = -1;
-    desc.T = st.T;
     while (it.next(a)) {
       // Every softmax thread reaches this point once per segment: the decision to unwind is
       // taken here by all of them together (the flag may be raised while they read it, so
@@ -969,12 +1000,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         break;
       }
       const int b = it.b, h = it.h;
-      if (!it.full && it.i0 == 0 && !it.invalid) {  // a split pair starts here
-        desc.b = b;
-        desc.h = h;
-        desc.c_last = (int)((it.pend * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
-        desc.piece0 = it.first ? 0 : 1;
-      }
       const size_t orow = ((size_t)b * twoB + s_slot) * a.Hq + (size_t)h * a.G + g;
       const size_t slot = part_slot(blockIdx.x, it.first ? 0 : 1);
       if (it.invalid) {
@@ -984,6 +1009,7 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         continue;
       }
       bool ok = true;
+      float m_used = -INFINITY, l = 0.f;  // running max (log2 domain) and sum of this segment
       do {
         const int P = a.prompt_len[b];
         const bool has_tail = it.has_tail;
@@ -1145,7 +1171,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         arrive_x(kQFull);
-        float m_used = -INFINITY, l = 0.f;
         const uint32_t jfirst = j;
         // The next segment's Q rows, tail rows and labels go into L2 a few tiles before this
         // segment ends, so that its prologue does not wait behind the K/V stream in flight.
@@ -1281,13 +1306,15 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           arrive_x(kPFull0 + buf);
         }
         if (!ok) break;
-        // ---- epilogue: wait for the last P V, then O / l (or the partial)
+        // ---- epilogue: wait for the last P V, then O / l, or, for a later piece of a split
+        // pair, the partial (the pair's first piece keeps O in TMEM for the merge below)
         const uint32_t jl = j - 1;
         ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFree0 + jl % NSB), (jl / NSB) & 1, a.dev_err, wait_ns));
         if (!ok) break;
         ptx::tc_fence_after();
-        if (warp_active && chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err) &&
-            chk((int64_t)slot * kBlockRows + row, 1, (int64_t)2 * a.ctas * a.cl * kBlockRows, a.dev_err)) {
+        if ((it.full || it.i0 > 0) && warp_active &&
+            chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err) &&
+            chk((int64_t)slot * kBlockRows + row, 1, nslots * kBlockRows, a.dev_err)) {
           const float inv = it.full ? 1.f / l : 1.f;
 #pragma unroll 1
           for (int k = 0; k < 4; ++k) {
@@ -1304,11 +1331,13 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
                                     pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
                                     pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
             } else {
+              // 16-byte chunk c of this 32-column group goes to position c ^ (row & 7), so that
+              // the merging CTA reads its copy of the rows without bank conflicts
               float4* dst = reinterpret_cast<float4*>(a.ws_o + (slot * kBlockRows + row) * kD + 32 * k);
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                                     __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                dst[c ^ (row & 7)] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                                 __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
             }
           }
           if (real) {
@@ -1321,23 +1350,142 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
         }
         ptx::tc_fence_before();
       } while (false);
-      if (!ok) mark_unfinished(a, it, real, orow, slot, row);  // this segment stopped part-way
+      // One answer for the segment: a warp that gave up left the tile loop or the epilogue
+      // early and meets the others here.
+      ok = !ptx::bar_or(1, 128, !ok);
+      if (!ok) {
+        mark_unfinished(a, it, real, orow, slot, row);  // this segment stopped part-way
+        if (!it.full && it.i0 > 0) publish(slot);
+      } else if (!it.full && it.i0 > 0) {
+        publish(slot);
+      } else if (!it.full) {
+        // ---- merge of a split pair, by its first piece (the last segment of this range): the
+        // later pieces are the first segment of every non-empty unit up to the one holding
+        // the pair's end, in the CTA of this row block (partial slot 0)
+        const int64_t T = st.T;
+        const int C = a.ctas;
+        const int c_last = (int)((it.pend * (int64_t)C + T - 1) / T) - 1;
+        bool got = true;
+        if (tid == 0) {
+          const uint64_t t_start = ptx::globaltimer_ns();
+          for (int vc = vcta + 1; vc <= c_last && got; ++vc) {
+            if (cta_begin(T, C, vc) == cta_begin(T, C, vc + 1)) continue;
+            const int64_t ps = (int64_t)part_slot(vc * a.cl + crank, 0);
+            if (!chk(ps, 1, nslots, a.dev_err)) continue;
+            while (ld_acquire_u64(a.ws_flag + ps) != token) {
+              if (*(volatile int*)&sh->abort) {
+                got = false;
+                break;
+              }
+              if (ptx::globaltimer_ns() - t_start > wait_ns) {
+                raise_abort(sh, a.dev_err);
+                got = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+          if (got) {  // each slot is published once per launch: consumed, cleared
+            for (int vc = vcta + 1; vc <= c_last; ++vc) {
+              if (cta_begin(T, C, vc) == cta_begin(T, C, vc + 1)) continue;
+              const int64_t ps = (int64_t)part_slot(vc * a.cl + crank, 0);
+              if (chk(ps, 1, nslots, a.dev_err)) a.ws_flag[ps] = 0;
+            }
+          }
+        }
+        got = !ptx::bar_or(1, 128, !got);
+        // The pieces' partials come into shared memory (the ring, idle once this last
+        // segment's P V completed), two at a time, one bulk copy each for O (64 KB) and for
+        // (max, sum) (1 KB); each is folded into this piece's O in TMEM (online rescale).
+        float mt = m_used, L = l;
+        int vc = vcta + 1, batch = 0;
+        while (got) {
+          int ps_b[kMergeBatch], nb = 0;
+          for (; vc <= c_last && nb < kMergeBatch; ++vc) {
+            if (cta_begin(T, C, vc) == cta_begin(T, C, vc + 1)) continue;
+            ps_b[nb++] = (int)part_slot(vc * a.cl + crank, 0);
+          }
+          if (nb == 0) break;
+          if (tid == 0) {
+            ptx::fence_proxy_async_smem();  // earlier reads of the staging area are done (barrier)
+            ptx::mbar_arrive_expect_tx(bar(kMerge), (uint32_t)nb * (kMergeO + kMergeML));
+            for (int q = 0; q < nb; ++q) {
+              const int64_t ps = ps_b[q];
+              if (!chk(ps, 1, nslots, a.dev_err)) continue;  // (the wait then gives up)
+              ptx::bulk_load_g2s(sbase + kOffStages + q * kMergeO, a.ws_o + ps * kBlockRows * kD, kMergeO, bar(kMerge));
+              ptx::bulk_load_g2s(sbase + kOffStages + kMergeBatch * kMergeO + q * kMergeML,
+                                 a.ws_ml + ps * kBlockRows, kMergeML, bar(kMerge));
+            }
+          }
+          got = !ptx::bar_or(1, 128, !wait_bar(sh, bar(kMerge), batch & 1, a.dev_err, wait_ns));
+          if (!got) break;
+          if (warp_active) {
+            ptx::tc_fence_after();
+            for (int q = 0; q < nb; ++q) {
+              const float2 ml = reinterpret_cast<const float2*>(smem + kOffStages + kMergeBatch * kMergeO +
+                                                                 q * kMergeML)[row];
+              const float m_new = fmaxf(mt, ml.x);
+              const float a_self = exp2f(mt - m_new), a_p = exp2f(ml.x - m_new);
+              L = L * a_self + ml.y * a_p;
+              mt = m_new;
+              const float4* srow = reinterpret_cast<const float4*>(smem + kOffStages + q * kMergeO) + row * (kD / 4);
+#pragma unroll 1
+              for (int k = 0; k < 4; ++k) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tmem_o + 32 * k, o);
+                ptx::tmem_ld_wait(o);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const float4 v = srow[8 * k + (c ^ (row & 7))];
+                  o[4 * c] = __float_as_uint(fmaf(a_p, v.x, __uint_as_float(o[4 * c]) * a_self));
+                  o[4 * c + 1] = __float_as_uint(fmaf(a_p, v.y, __uint_as_float(o[4 * c + 1]) * a_self));
+                  o[4 * c + 2] = __float_as_uint(fmaf(a_p, v.z, __uint_as_float(o[4 * c + 2]) * a_self));
+                  o[4 * c + 3] = __float_as_uint(fmaf(a_p, v.w, __uint_as_float(o[4 * c + 3]) * a_self));
+                }
+                ptx::tmem_st32(tmem_o + 32 * k, o);
+              }
+              ptx::tmem_st_wait();  // the next piece (or the final read) loads these columns
+            }
+            ptx::tc_fence_before();
+          }
+          ++batch;
+          ptx::named_bar_sync(1, 128);  // the staging area is read before it is refilled
+        }
+        if (!got) {
+          mark_unfinished(a, it, real, orow, slot, row);
+        } else if (warp_active) {
+          ptx::tc_fence_after();
+          const bool rok = real && chk((int64_t)orow * kD, kD, (int64_t)a.batch * twoB * a.Hq * kD, a.dev_err);
+          const float inv = 1.f / L;
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tmem_o + 32 * k, o);
+            ptx::tmem_ld_wait(o);
+            if (!rok) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + 32 * k);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(pack_bf16(__uint_as_float(o[8 * c]) * inv, __uint_as_float(o[8 * c + 1]) * inv),
+                                  pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
+                                  pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
+                                  pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
+          }
+          if (rok && a.lse) a.lse[orow] = (mt + log2f(L)) * 0.69314718055994530942f;
+          ptx::tc_fence_before();
+        }
+      }
       it.advance(a);
     }
     if (aborted) {  // the segment reached and every later one of the range are unfinished
       do {
-        if (!it.full && it.i0 == 0 && !it.invalid) {
-          desc.b = it.b;
-          desc.h = it.h;
-          desc.c_last = (int)((it.pend * (int64_t)a.ctas + st.T - 1) / st.T) - 1;
-          desc.piece0 = it.first ? 0 : 1;
-        }
         const size_t orow = ((size_t)it.b * twoB + s_slot) * a.Hq + (size_t)it.h * a.G + g;
-        mark_unfinished(a, it, real, orow, part_slot(blockIdx.x, it.first ? 0 : 1), row);
+        const size_t pslot = part_slot(blockIdx.x, it.first ? 0 : 1);
+        mark_unfinished(a, it, real, orow, pslot, row);
+        if (!it.full && it.i0 > 0 && !it.invalid) publish(pslot);  // (a NaN partial)
         it.advance(a);
       } while (it.next(a));
     }
-    if (tid == 0 && chk(blockIdx.x, 1, (int64_t)a.ctas * a.cl, a.dev_err)) a.ws_desc[blockIdx.x] = desc;
     if (!loads_signalled) ptx::mbar_arrive(bar(kLoads));  // no prologue ran: release the producer
   }
 
@@ -1353,61 +1501,6 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
     ptx::tc_fence_after();
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// Merges the pieces of every pair split between units. Block (c, y) reads CTA c's merge
-// descriptor and, if a split pair starts in CTA c, combines rows 8y..8y+7 of that CTA's row
-// block of the pair: one thread per (row, 4 output elements), so every load is independent.
-__global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the attention grid has completed
-  const int c = blockIdx.x;  // CTA; schedule unit c / cl, row block c % cl
-  if (!chk(c, 1, (int64_t)a.ctas * a.cl, a.dev_err)) return;
-  const MergeDesc d = a.ws_desc[c];
-  if (d.b < 0) return;
-  const int cl = a.cl;
-  const int vc = c / cl, crank = c - vc * cl;
-  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the CTA's block
-  const int prow = crank * 128 + row;                    // row within the pair
-  const int quad = threadIdx.x & 31;
-  if (row >= kBlockRows || prow >= a.R) return;
-  const int64_t T = d.T;
-  const int C = a.ctas;
-  // pieces: unit vc (its piece0) and every later non-empty unit up to c_last (its first
-  // piece), each in the CTA of the same row block
-  float mmax = -INFINITY;
-  const int64_t nslots = (int64_t)2 * a.ctas * cl;
-#pragma unroll 4
-  for (int vcc = vc; vcc <= d.c_last; ++vcc) {
-    if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
-    const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
-    if (!chk((int64_t)slot, 1, nslots, a.dev_err)) continue;
-    mmax = fmaxf(mmax, a.ws_ml[slot * kBlockRows + row].x);
-  }
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int vcc = vc; vcc <= d.c_last; ++vcc) {
-    if (vcc > vc && cta_begin(T, C, vcc) == cta_begin(T, C, vcc + 1)) continue;
-    const size_t slot = part_slot(vcc * cl + crank, vcc == vc ? d.piece0 : 0);
-    if (!chk((int64_t)slot, 1, nslots, a.dev_err)) continue;
-    const float2 ml = a.ws_ml[slot * kBlockRows + row];
-    const float4 o = reinterpret_cast<const float4*>(a.ws_o + (slot * kBlockRows + row) * kD)[quad];
-    const float w = exp2f(ml.x - mmax);
-    L += w * ml.y;
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
-  }
-  const float inv = 1.f / L;
-  const int s_slot = prow / a.G, g = prow % a.G;
-  const size_t orow = ((size_t)d.b * 2 * a.B + s_slot) * a.Hq + (size_t)d.h * a.G + g;
-  if (!chk((int64_t)orow, 1, (int64_t)a.batch * 2 * a.B * a.Hq, a.dev_err)) return;
-  uint2 pk;
-  pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(a.out + orow * kD)[quad] = pk;
-  if (quad == 0 && a.lse) a.lse[orow] = (mmax + log2f(L)) * 0.69314718055994530942f;
 }
 
 // ------------------------------------------------------------------------------- host
@@ -1544,14 +1637,14 @@ static int grid_units(const simsd_attn_params* p, int cl) {
 }
 
 struct WsLayout {
-  size_t o, ml, desc, bytes;
+  size_t o, ml, flag, bytes;
 };
 static WsLayout ws_layout(int ctas) {
   WsLayout w;
   w.o = 0;
   w.ml = align_up(w.o + (size_t)2 * ctas * kBlockRows * kD * sizeof(float), 256);
-  w.desc = align_up(w.ml + (size_t)2 * ctas * kBlockRows * sizeof(float2), 256);
-  w.bytes = align_up(w.desc + (size_t)ctas * sizeof(MergeDesc), 256);
+  w.flag = align_up(w.ml + (size_t)2 * ctas * kBlockRows * sizeof(float2), 256);
+  w.bytes = align_up(w.flag + (size_t)2 * ctas * sizeof(uint64_t), 256);
   return w;
 }
 
@@ -1594,7 +1687,7 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
   if (!ws || ws_bytes < wl.bytes || (((uintptr_t)ws) & 255)) return SIMSD_ERR_WORKSPACE;
   a.ws_o = (float*)((char*)ws + wl.o);
   a.ws_ml = (float2*)((char*)ws + wl.ml);
-  a.ws_desc = (MergeDesc*)((char*)ws + wl.desc);
+  a.ws_flag = (uint64_t*)((char*)ws + wl.flag);
   make_rope_table(&a.rope, (double)p->rope_theta, kD);
 
   CUtensorMap tmk, tmv;
@@ -1638,24 +1731,6 @@ static simsd_status launch(const simsd_attn_params* p, void* ws, size_t ws_bytes
                r128::kThreads, fa.numRegs, fa.maxThreadsPerBlock, r128::kSmemBytes,
                fa.maxDynamicSharedSizeBytes, fa.sharedSizeBytes, fa.localSizeBytes);
     record_cuda_error(what, le);
-    return SIMSD_ERR_CUDA;
-  }
-  // blocks without a split pair exit at once. A programmatic dependent of the attention
-  // kernel: its blocks are placed while the attention CTAs run and wait (griddepcontrol)
-  // for their completion, so the launch latency is hidden.
-  cudaLaunchConfig_t mcfg = {};
-  cudaLaunchAttribute mat[1];
-  mat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  mat[0].val.programmaticStreamSerializationAllowed = 1;
-  mcfg.gridDim = dim3((unsigned)(a.ctas * a.cl), (unsigned)((min(a.R, kBlockRows) + 7) / 8));
-  mcfg.blockDim = dim3(256);
-  mcfg.dynamicSmemBytes = 0;
-  mcfg.stream = stream;
-  mcfg.attrs = mat;
-  mcfg.numAttrs = 1;
-  cudaError_t me = cudaLaunchKernelEx(&mcfg, attn_tc_merge_kernel, a);
-  if (me != cudaSuccess) {
-    record_cuda_error("merge kernel launch", me);
     return SIMSD_ERR_CUDA;
   }
   return last_launch_status();
