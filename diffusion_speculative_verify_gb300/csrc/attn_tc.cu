@@ -1184,11 +1184,16 @@ __global__ void __launch_bounds__(r128::kThreads, 1)
           }
         }
         const int pf_at = max(it.i0, it.i0 + it.n - kPrefetchAhead);
-        for (int i = it.i0; i < it.i0 + it.n; ++i, ++j) {
-          const int buf = j % NSB;
+        // S buffer j % NSB and its phase (j / NSB) & 1, advanced with j
+        int buf = (int)(j % NSB);
+        uint32_t ph = (j / NSB) & 1;
+        for (int i = it.i0; i < it.i0 + it.n;
+             ++i, ++j, buf = (buf + 1 == NSB) ? 0 : buf + 1, ph ^= (buf == 0) ? 1u : 0u) {
           if (pf_b >= 0 && i == pf_at)
             prefetch_prologue(a, pf_b, pf_h & 0xffff, pf_h >> 16, twoB, s_slot, g, real, rw, tid);
-          ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), (j / NSB) & 1, a.dev_err, wait_ns));
+          // S is usually complete already: one probe and one vote, else the bounded wait
+          if (!__all_sync(0xffffffffu, ptx::mbar_test(bar(kSFull0 + buf), ph)))
+            ok = __all_sync(0xffffffffu, wait_bar(sh, bar(kSFull0 + buf), ph, a.dev_err, wait_ns));
           if (!ok) break;
           if (!warp_active) {  // padding rows only: keep the P barrier's count, skip the work
             arrive_x(kPFull0 + buf);
