@@ -230,6 +230,20 @@ def test_attention_bf16_two_ctas_partial_second_block(Hq, Hkv, B):
     assert int(st.dev_err.item()) == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,B,P", [(8, 1, 4, 20000), (32, 4, 16, 8000)])
+def test_attention_bf16_one_pair_split_over_the_grid(Hq, Hkv, B, P):
+    # One request whose pair(s) span nearly every schedule unit: a pair split into many
+    # pieces (about one tile each), merged inside the kernel by the CTA holding its first
+    # piece through many rounds of staged partials. (8, 1, 4): one 64-row pair on the
+    # single-CTA kernel over about 150 units; (32, 4, 16): four 256-row pairs on CTA pairs.
+    w = MEDIUM.with_(batch=1, Hq=Hq, Hkv=Hkv, B=B, gamma=B)
+    inputs, meta = H.make_case(w, seed=300 + B, prompt_len=[P])
+    st = _step(w, inputs, meta)
+    _attention_parity(w, inputs, meta, st)
+    assert int(st.dev_err.item()) == 0
+    assert torch.isfinite(st.out.float()).all() and torch.isfinite(st.lse).all()
+
+
 @pytest.mark.parametrize("B", [4, 16])
 def test_attention_bf16_later_rounds(B):
     # committed slots (tau = 0) are seen by every open row through their data slot and by
