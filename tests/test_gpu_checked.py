@@ -5,7 +5,7 @@ checks the index of each global access against the extent of the array it addres
 reports a violation in the device error word (SIMSD_DEVERR_BOUNDS) instead of making the
 access. These tests swap that build in under the same Python binding and run small cases of
 every entry point (layout, bf16 attention with one and two CTAs per pair and with pairs
-split across CTAs, NHD and HND caches, fp32 attention, acceptance at T = 1 and T = 0 with
+split across CTAs or CTA pairs, NHD and HND caches, fp32 attention, acceptance at T = 1 and T = 0 with
 fp32 and bf16 logits and an odd vocabulary, coupled-noise verification, the
 expected-prefix estimate, the allocation-free acceptance entry): each must raise no error
 bit and still match the fp64 oracle. A last case checks that the checks fire: a request
@@ -71,6 +71,8 @@ CASES = {
     "one_cta_per_pair_hnd": (MEDIUM, [0, 61, 128, 1037], "HND"),
     "two_ctas_per_pair": (MEDIUM.with_(Hq=6, Hkv=2, B=32, gamma=32), [0, 61, 128, 1037], "NHD"),
     "split_pairs": (MEDIUM.with_(Hq=6, Hkv=2, B=16, gamma=16), [20000, 61, 128, 9000], "NHD"),
+    # 256-row pairs on CTA pairs, split across 2-CTA clusters and merged in the kernel
+    "split_pairs_two_ctas_hnd": (MEDIUM.with_(Hq=8, Hkv=1, B=16, gamma=16), [20000, 61, 128, 9000], "HND"),
     "fp32": (workloads.WORKLOADS["tiny_fp32"].with_(batch=3, B=8, gamma=8), [0, 33, 300], "NHD"),
 }
 
