@@ -10,12 +10,13 @@
 // Two launches:
 //   K3a accept_stats    : grid over (request, step, model, vocab chunk); streams the logit
 //                         row chunk once and writes its (max, sum exp) pair.
-//   K3b accept_finish   : grid over (request, vocab chunk); every CTA merges the chunk
+//   K3b accept_finish   : one wave of CTAs, each an equal range of the batch's (request,
+//                         group of 4 entries) pairs; per request touched, a CTA merges the chunk
 //                         pairs, re-derives the accept decisions (cheap), and if a step was
-//                         rejected runs the race over its chunk of the rejected slot's rows;
+//                         rejected runs the race over its groups of the rejected slot's rows;
 //                         winners meet in a 64-bit atomicMax; the last CTA of the request
-//                         (atomic ticket, no waiting) writes the outputs and re-zeroes the
-//                         request's scratch.
+//                         (atomic ticket, no waiting) writes the outputs. K3a zeroes the
+//                         winners and tickets at the start of every call.
 #include <cudaTypedefs.h>
 #include <float.h>
 
@@ -43,7 +44,10 @@ struct AcceptWs {
 
 struct AcceptPlan {
   int nchunk_a, chunk_a;  // K3a: chunks per row, elements per chunk (multiple of 8)
-  int nchunk_b, chunk_b;  // K3b: chunks per request, elements per chunk (multiple of 4)
+  // K3b: CTAs, each a range of the (request, group of 4 entries) pairs: nb_b > 0, request r
+  // takes CTAs r nb_b .. r nb_b + nb_b - 1, cg_b groups each (the last fewer); nb_b = 0,
+  // equal ranges across request boundaries (stream-K)
+  int ctas_b, nb_b, cg_b;
   size_t off_stats, off_winners, off_ticket, bytes;
 };
 
@@ -56,7 +60,12 @@ int resident_finish_ctas();
 // and the items are dealt to the resident warps round-robin. nchunk_a is the smallest count
 // whose items fill the warps' last round to at least 97 % (the kernel's time is set by the
 // warps that take the most items), else the best fill; chunks stay at least 512 entries.
-// K3b takes one wave of CTAs, nchunk_b per request.
+// K3b takes one wave of CTAs over the batch's (request, group of 4 entries) pairs, at least
+// 256 groups each, so no CTA's range is empty and each request's CTAs are consecutive. When
+// a whole number of CTAs per request fills at least 90 % of the resident slots, each CTA stays
+// within one request; otherwise (e.g. batch 256 on 304 slots: one CTA each, 84 %) the ranges
+// are equal and cross request boundaries, and a CTA that holds the end of one request and
+// the start of the next sets both up in turn (the statistics merge of 2 gamma rows).
 // `models` = 2 (target and draft rows: sampling) or 1 (target rows only: greedy).
 AcceptPlan make_plan(int batch, int gamma, int V, int models = 2) {
   AcceptPlan p;
@@ -77,12 +86,18 @@ AcceptPlan make_plan(int batch, int gamma, int V, int models = 2) {
   }
   p.chunk_a = (int)(((V + best_nc - 1) / best_nc + 7) / 8 * 8);  // 16-byte loads of bf16
   p.nchunk_a = (V + p.chunk_a - 1) / p.chunk_a;
-  long nb = batch > 0 ? std::max(1, resident_finish_ctas()) / batch : 1;
-  const long max_nb = (V + 1023) / 1024;
-  if (nb > max_nb) nb = max_nb;
-  if (nb < 1) nb = 1;
-  p.nchunk_b = (int)nb;
-  p.chunk_b = (int)(((V + nb - 1) / nb + 3) / 4 * 4);
+  const long long ng = (V + 3) / 4, groups = (long long)batch * ng;
+  const long long slots = std::max(1, resident_finish_ctas());
+  const long long nb = batch > 0 ? std::min<long long>(slots / batch, (V + 1023) / 1024) : 0;
+  if (nb >= 1 && 10 * batch * nb >= 9 * slots) {
+    p.nb_b = (int)nb;
+    p.cg_b = (int)((ng + nb - 1) / nb);
+    p.ctas_b = (int)(batch * nb);
+  } else {
+    p.nb_b = 0;
+    p.cg_b = 0;
+    p.ctas_b = (int)std::max<long long>(1, std::min<long long>(slots, groups / 256));
+  }
   size_t off = 0;
   p.off_stats = off;
   off = align_up(off + (size_t)batch * gamma * models * p.nchunk_a * sizeof(float2), 256);
@@ -349,7 +364,12 @@ __device__ __forceinline__ void race_range(const LT* __restrict__ trow, const LT
   }
 }
 
-// Two CTAs per SM (the grid is one wave of them).
+// Two CTAs per SM (the grid is one wave of them). The (request, counter group) pairs,
+// request-major, are cut into one contiguous range per CTA (the plan: a whole number of CTAs
+// per request, or equal ranges across request boundaries, stream-K style, where whole CTAs
+// would leave slots idle). A CTA takes the requests its range touches in turn: for each it
+// re-derives the decisions and races its groups of the rejected slot; the CTAs touching a
+// request count themselves on its ticket, and the last one writes its outputs.
 template <typename LT>
 __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     const LT* __restrict__ target, const LT* __restrict__ draft,
@@ -358,218 +378,250 @@ __global__ void __launch_bounds__(kFinishThreads, 2) accept_finish_kernel(
     AcceptPlan plan, AcceptWs ws, int32_t* __restrict__ accepted_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_pos,
     int32_t* __restrict__ n_commit, uint32_t* __restrict__ dev_err) {
-  const int chunk = blockIdx.x % plan.nchunk_b;
-  const int r = blockIdx.x / plan.nchunk_b;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  // checked build: the request's labels, tokens, outputs, scratch and chunk statistics lie
-  // inside their arrays (block-uniform; else the block does nothing)
-  if (!chk(r, 1, batch, dev_err) || !chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, dev_err) ||
-      !chk((long long)r * B, B, (long long)batch * B, dev_err) ||
-      !chk((long long)r * gamma * 2 * plan.nchunk_a, (long long)gamma * 2 * plan.nchunk_a, ws.n_stats, dev_err))
-    return;
-  const uint8_t* lab = labels + (size_t)r * 2 * B;
   const bool unit_T = (T == 1.f);
+  const int ng = (V + 3) / 4;  // counter groups of a row
+  // this CTA's range [f0, f1) of the flattened groups r * ng + g and the requests it touches,
+  // [r_lo, r_hi] (whole CTAs per request: one, found without a 64-bit division)
+  long long f0, f1;
+  int r_lo, r_hi;
+  if (plan.nb_b > 0) {
+    const int rq = blockIdx.x / plan.nb_b, ch = blockIdx.x - rq * plan.nb_b;
+    f0 = (long long)rq * ng + (long long)ch * plan.cg_b;
+    f1 = (long long)rq * ng + min((long long)ng, (long long)(ch + 1) * plan.cg_b);
+    r_lo = r_hi = rq;
+  } else {
+    const long long F = (long long)batch * ng;
+    f0 = (long long)blockIdx.x * F / gridDim.x;
+    f1 = ((long long)blockIdx.x + 1) * F / gridDim.x;
+    r_lo = (int)(f0 / ng);
+    r_hi = f1 > f0 ? (int)((f1 - 1) / ng) : r_lo - 1;
+  }
+  // CTAs whose ranges touch request r, less one (stream-K: the CTA holding flattened group f
+  // is the largest c with c F / C <= f)
+  auto others = [&](int r) -> unsigned {
+    if (plan.nb_b > 0) return (unsigned)(plan.nb_b - 1);
+    const long long F = (long long)batch * ng;
+    auto cta_of = [&](long long f) { return ((f + 1) * gridDim.x + F - 1) / F - 1; };
+    return (unsigned)(cta_of((long long)r * ng + ng - 1) - cta_of((long long)r * ng));
+  };
 
   __shared__ int s_order[kMaxB];
   __shared__ int s_a, s_bad, s_gr;
   __shared__ float s_mt, s_st, s_md, s_sd;
   __shared__ float2 s_rowstat[2 * kMaxB];  // merged (max, sum exp) per (step, model)
+  __shared__ bool s_last;
+  __shared__ unsigned long long s_win;
 
-  // Everything that does not read K3a's results comes before the grid dependency wait, so
-  // it overlaps K3a's last items: warp 0 checks the step labels, orders the steps, and loads
-  // each verified step's draft token, the two logits at that token and its uniform.
-  int bad_w = 0, k_w = 0, x_w = 0;  // warp 0: error bits, slot and token of step `lane`
-  int gr_w = gamma;                 // warp 0: steps verified, min(gamma, R)
-  float tx = 0.f, dx = 0.f, u = 0.f;
-  if (w == 0) {
-    // step labels of the data half -> order o_t; validity of the permutation
-    // labels 1..R of the open slots (0: committed in an earlier round) -> order o_t
-    const uint8_t lb = lane < B ? lab[lane] : 0;
-    const int tau = lb & 0x7F;
-    const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau <= B);
-    const int R = __popc(__ballot_sync(0xffffffffu, lane < B && tau != 0));
-    const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
-    const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
-    const unsigned full = R == 32 ? 0xffffffffu : ((1u << R) - 1u);
-    const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
-    if (perm && lane < B && tau != 0) s_order[tau - 1] = lane;
-    __syncwarp();
-    bad_w = perm ? 0 : (int)SIMSD_DEVERR_TAU;
-    gr_w = min(gamma, R);
-    if (perm && lane < gr_w) {
-      k_w = s_order[lane];
-      x_w = tokens[(size_t)r * B + k_w];
-    }
-    const bool tok_bad = perm && lane < gr_w && (x_w < 0 || x_w >= V);
-    if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
-    if (!bad_w && lane < gr_w && chk(((long long)r * B + k_w) * V + x_w, 1, (long long)batch * B * V, dev_err)) {
-      const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
-      tx = scale_logit(LogitIO<LT>::ld1(target + rowoff), T, unit_T);
-      dx = scale_logit(LogitIO<LT>::ld1(draft + rowoff), T, unit_T);
-      Philox4 c4 = {(uint32_t)r, off_lo, off_hi, (uint32_t)(lane >> 2)};
-      const Philox4 rnd = philox4x32_10(c4, key0, key1);
-      u = word_to_uniform(philox_word(rnd, lane & 3));
-    }
-  }
+  bool waited = false;
+  for (int r = r_lo; r <= r_hi && r < batch; ++r) {
+    const long long rbase = (long long)r * ng;
+    const int g_lo = (int)(max(f0, rbase) - rbase), g_hi = (int)(min(f1, rbase + ng) - rbase);
+    if (waited) __syncthreads();  // the previous request's shared state has been read
+    // checked build: the request's labels, tokens, outputs, scratch and chunk statistics lie
+    // inside their arrays (block-uniform; else the request is skipped)
+    const bool req_ok =
+        chk(r, 1, batch, dev_err) && chk((long long)r * 2 * B, 2 * B, (long long)batch * 2 * B, dev_err) &&
+        chk((long long)r * B, B, (long long)batch * B, dev_err) &&
+        chk((long long)r * gamma * 2 * plan.nchunk_a, (long long)gamma * 2 * plan.nchunk_a, ws.n_stats, dev_err);
+    const uint8_t* lab = labels + (size_t)r * 2 * B;
 
-  // launched as a programmatic dependent of K3a: wait for K3a's results before reading them
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // merge the chunk partials of every verified (step, model) row: warp w takes rows
-  // w, w + 8, ...; all of a warp's loads are issued before any is reduced
-  constexpr int kWarps = kFinishThreads / 32;
-  constexpr int kRowsPerWarp = (2 * kMaxB + kWarps - 1) / kWarps;
-  const float2* rstats = ws.stats + (size_t)r * gamma * 2 * plan.nchunk_a;
-  for (int c0 = 0; c0 < plan.nchunk_a; c0 += 32) {
-    float2 v[kRowsPerWarp];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int row = w + kWarps * i, c = c0 + lane;
-      v[i] = (row < 2 * gamma && c < plan.nchunk_a) ? rstats[(size_t)row * plan.nchunk_a + c]
-                                                   : make_float2(-INFINITY, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int row = w + kWarps * i;
-      if (row >= 2 * gamma) break;  // warp-uniform
-      float m = v[i].x, sum = v[i].y;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        lse_merge(m, sum, m2, s2);
+    // Everything that does not read K3a's results comes before the grid dependency wait, so
+    // it overlaps K3a's last items: warp 0 checks the step labels, orders the steps, and loads
+    // each verified step's draft token, the two logits at that token and its uniform.
+    int bad_w = 0, k_w = 0, x_w = 0;  // warp 0: error bits, slot and token of step `lane`
+    int gr_w = gamma;                 // warp 0: steps verified, min(gamma, R)
+    float tx = 0.f, dx = 0.f, u = 0.f;
+    if (w == 0 && req_ok) {
+      // step labels of the data half -> order o_t; validity of the permutation
+      // labels 1..R of the open slots (0: committed in an earlier round) -> order o_t
+      const uint8_t lb = lane < B ? lab[lane] : 0;
+      const int tau = lb & 0x7F;
+      const bool ok_lane = lane >= B || (lb != kLabelInvalid && !(lb & kSegMask) && tau <= B);
+      const int R = __popc(__ballot_sync(0xffffffffu, lane < B && tau != 0));
+      const unsigned bit = (lane < B && tau >= 1 && tau <= B) ? (1u << (tau - 1)) : 0u;
+      const unsigned cover = __reduce_or_sync(0xffffffffu, bit);
+      const unsigned full = R == 32 ? 0xffffffffu : ((1u << R) - 1u);
+      const bool perm = __all_sync(0xffffffffu, ok_lane) && cover == full;
+      if (perm && lane < B && tau != 0) s_order[tau - 1] = lane;
+      __syncwarp();
+      bad_w = perm ? 0 : (int)SIMSD_DEVERR_TAU;
+      gr_w = min(gamma, R);
+      if (perm && lane < gr_w) {
+        k_w = s_order[lane];
+        x_w = tokens[(size_t)r * B + k_w];
       }
-      if (lane == 0) {
-        if (c0 == 0) {
-          s_rowstat[row] = make_float2(m, sum);
-        } else {  // more than 32 chunks: fold into the earlier ones
-          float mm = s_rowstat[row].x, ss = s_rowstat[row].y;
-          lse_merge(mm, ss, m, sum);
-          s_rowstat[row] = make_float2(mm, ss);
+      const bool tok_bad = perm && lane < gr_w && (x_w < 0 || x_w >= V);
+      if (__any_sync(0xffffffffu, tok_bad)) bad_w |= (int)SIMSD_DEVERR_TOKEN;
+      if (!bad_w && lane < gr_w && chk(((long long)r * B + k_w) * V + x_w, 1, (long long)batch * B * V, dev_err)) {
+        const size_t rowoff = ((size_t)r * B + k_w) * (size_t)V + x_w;
+        tx = scale_logit(LogitIO<LT>::ld1(target + rowoff), T, unit_T);
+        dx = scale_logit(LogitIO<LT>::ld1(draft + rowoff), T, unit_T);
+        Philox4 c4 = {(uint32_t)r, off_lo, off_hi, (uint32_t)(lane >> 2)};
+        const Philox4 rnd = philox4x32_10(c4, key0, key1);
+        u = word_to_uniform(philox_word(rnd, lane & 3));
+      }
+    }
+
+    // launched as a programmatic dependent of K3a: wait for K3a's results before reading them
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+    if (!req_ok) continue;
+
+    // merge the chunk partials of every verified (step, model) row: warp w takes rows
+    // w, w + 8, ...; all of a warp's loads are issued before any is reduced
+    constexpr int kWarps = kFinishThreads / 32;
+    constexpr int kRowsPerWarp = (2 * kMaxB + kWarps - 1) / kWarps;
+    const float2* rstats = ws.stats + (size_t)r * gamma * 2 * plan.nchunk_a;
+    for (int c0 = 0; c0 < plan.nchunk_a; c0 += 32) {
+      float2 v[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int row = w + kWarps * i, c = c0 + lane;
+        v[i] = (row < 2 * gamma && c < plan.nchunk_a) ? rstats[(size_t)row * plan.nchunk_a + c]
+                                                     : make_float2(-INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int row = w + kWarps * i;
+        if (row >= 2 * gamma) break;  // warp-uniform
+        float m = v[i].x, sum = v[i].y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+          lse_merge(m, sum, m2, s2);
+        }
+        if (lane == 0) {
+          if (c0 == 0) {
+            s_rowstat[row] = make_float2(m, sum);
+          } else {  // more than 32 chunks: fold into the earlier ones
+            float mm = s_rowstat[row].x, ss = s_rowstat[row].y;
+            lse_merge(mm, ss, m, sum);
+            s_rowstat[row] = make_float2(mm, ss);
+          }
         }
       }
     }
-  }
-  __syncthreads();
-
-  if (w == 0) {
-    int a = gr_w;
-    if (!bad_w) {
-      bool acc = true;
-      float mt = 0.f, st = 0.f, md = 0.f, sd = 0.f;
-      if (lane < gr_w) {
-        const float2 rt = s_rowstat[2 * lane], rd = s_rowstat[2 * lane + 1];
-        mt = rt.x;
-        st = rt.y;
-        md = rd.x;
-        sd = rd.y;
-        const float px = __fdiv_rn(expf(tx - mt), st);
-        const float qx = __fdiv_rn(expf(dx - md), sd);
-        acc = (px >= qx) || (u * qx < px);
-      }
-      const unsigned rej = __ballot_sync(0xffffffffu, lane < gr_w && !acc);
-      a = rej ? (__ffs(rej) - 1) : gr_w;
-      if (a < gr_w && lane == a) {
-        s_mt = mt;
-        s_st = st;
-        s_md = md;
-        s_sd = sd;
-      }
-    }
-    if (lane == 0) {
-      s_a = a;
-      s_bad = bad_w;
-      s_gr = gr_w;
-    }
-  }
-  __syncthreads();
-  const int a = s_a;
-  const int bad = s_bad;
-  const int gr = s_gr;  // steps this request verifies
-  if (bad) {
-    if (chunk == 0) {
-      if (tid == 0) {
-        atomicOr(dev_err, (uint32_t)bad);
-        accepted_len[r] = -1;
-        n_commit[r] = 0;
-      }
-      for (int i = tid; i < B; i += blockDim.x) {
-        out_tokens[(size_t)r * B + i] = -1;
-        out_pos[(size_t)r * B + i] = -1;
-      }
-    }
-    return;
-  }
-
-  if (a < gr) {
-    // exponential race over this CTA's chunk of the rejected slot's vocabulary
-    const int k = s_order[a];
-    const float mt = s_mt, st = s_st, md = s_md, sd = s_sd;
-    const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
-    const LT* drow = draft + ((size_t)r * B + k) * (size_t)V;
-    const int c0 = chunk * plan.chunk_b;
-    const int c1 = min(V, c0 + plan.chunk_b);
-    unsigned long long best_res = 0ull;
-    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
-    if (chk(((long long)r * B + k) * V + min(c0, V), c1 - min(c0, V), (long long)batch * B * V, dev_err))
-      race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
-                 1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
-      best_res = b1 > best_res ? b1 : best_res;
-    }
-    // a residual entry is taken only where it is positive, and its packed key is then
-    // nonzero: a winner word still 0 at the end means the residual vanished everywhere
-    if (lane == 0 && best_res != 0ull) atomicMax(&ws.winners[2 * r], best_res);
-  }
-  // last CTA of this request writes the outputs
-  __shared__ bool s_last;
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned done = atomicAdd(&ws.ticket[r], 1u);
-    s_last = (done == (unsigned)plan.nchunk_b - 1u);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  __shared__ unsigned long long s_win;
-  if (tid == 0) s_win = atomicAdd(&ws.winners[2 * r], 0ull);
-  __syncthreads();
-  if (a < gr && s_win == 0ull) {
-    // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
-    // over the whole row, done here by the last CTA (never on typical inputs)
-    const int k = s_order[a];
-    const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
-    unsigned long long best = 0ull;
-    const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
-    if (chk(((long long)r * B + k) * V, V, (long long)batch * B * V, dev_err))
-      race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
-                 1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
-      best = b1 > best ? b1 : best;
-    }
-    if (lane == 0) atomicMax(&s_win, best);
     __syncthreads();
-  }
-  if (tid < B) {
-    int tok = -1, pos = -1;
-    if (tid < a) {
-      pos = s_order[tid];
-      tok = tokens[(size_t)r * B + pos];
-    } else if (tid == a && a < gr) {
-      pos = s_order[a];
-      tok = unpack_token(s_win);
+
+    if (w == 0) {
+      int a = gr_w;
+      if (!bad_w) {
+        bool acc = true;
+        float mt = 0.f, st = 0.f, md = 0.f, sd = 0.f;
+        if (lane < gr_w) {
+          const float2 rt = s_rowstat[2 * lane], rd = s_rowstat[2 * lane + 1];
+          mt = rt.x;
+          st = rt.y;
+          md = rd.x;
+          sd = rd.y;
+          const float px = __fdiv_rn(expf(tx - mt), st);
+          const float qx = __fdiv_rn(expf(dx - md), sd);
+          acc = (px >= qx) || (u * qx < px);
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, lane < gr_w && !acc);
+        a = rej ? (__ffs(rej) - 1) : gr_w;
+        if (a < gr_w && lane == a) {
+          s_mt = mt;
+          s_st = st;
+          s_md = md;
+          s_sd = sd;
+        }
+      }
+      if (lane == 0) {
+        s_a = a;
+        s_bad = bad_w;
+        s_gr = gr_w;
+      }
     }
-    out_tokens[(size_t)r * B + tid] = tok;
-    out_pos[(size_t)r * B + tid] = pos;
-  }
-  if (tid == 0) {
-    accepted_len[r] = a;
-    n_commit[r] = a + (a < gr ? 1 : 0);
+    __syncthreads();
+    const int a = s_a;
+    const int bad = s_bad;
+    const int gr = s_gr;  // steps this request verifies
+    if (bad) {  // sentinel outputs, by the CTA holding the request's first group
+      if (g_lo == 0) {
+        if (tid == 0) {
+          atomicOr(dev_err, (uint32_t)bad);
+          accepted_len[r] = -1;
+          n_commit[r] = 0;
+        }
+        for (int i = tid; i < B; i += blockDim.x) {
+          out_tokens[(size_t)r * B + i] = -1;
+          out_pos[(size_t)r * B + i] = -1;
+        }
+      }
+      continue;
+    }
+
+    if (a < gr) {
+      // exponential race over this CTA's groups of the rejected slot's vocabulary
+      const int k = s_order[a];
+      const float mt = s_mt, st = s_st, md = s_md, sd = s_sd;
+      const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
+      const LT* drow = draft + ((size_t)r * B + k) * (size_t)V;
+      const int c0 = 4 * g_lo;
+      const int c1 = min(V, 4 * g_hi);
+      unsigned long long best_res = 0ull;
+      const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
+      if (chk(((long long)r * B + k) * V + min(c0, V), c1 - min(c0, V), (long long)batch * B * V, dev_err))
+        race_range(trow, drow, min(c0, V), c1, tid, blockDim.x, vec_ok, T, unit_T, mt, 1.f / st, md,
+                   1.f / sd, false, (uint32_t)r, off_lo, off_hi, key0, key1, best_res);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best_res, o);
+        best_res = b1 > best_res ? b1 : best_res;
+      }
+      // a residual entry is taken only where it is positive, and its packed key is then
+      // nonzero: a winner word still 0 at the end means the residual vanished everywhere
+      if (lane == 0 && best_res != 0ull) atomicMax(&ws.winners[2 * r], best_res);
+    }
+    // last CTA of this request writes the outputs
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const unsigned done = atomicAdd(&ws.ticket[r], 1u);
+      s_last = (done == others(r));
+    }
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    if (tid == 0) s_win = atomicAdd(&ws.winners[2 * r], 0ull);
+    __syncthreads();
+    if (a < gr && s_win == 0ull) {
+      // the residual vanished in fp32 everywhere (p equal to q up to rounding): race on p
+      // over the whole row, done here by the last CTA (never on typical inputs)
+      const int k = s_order[a];
+      const LT* trow = target + ((size_t)r * B + k) * (size_t)V;
+      unsigned long long best = 0ull;
+      const bool vec_ok = (V & 3) == 0 && ((((uintptr_t)target) | ((uintptr_t)draft)) & (LogitIO<LT>::kAlign - 1)) == 0;
+      if (chk(((long long)r * B + k) * V, V, (long long)batch * B * V, dev_err))
+        race_range(trow, trow, 0, V, tid, blockDim.x, vec_ok, T, unit_T, s_mt, 1.f / s_st, s_md,
+                   1.f / s_sd, true, (uint32_t)r, off_lo, off_hi, key0, key1, best);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
+        best = b1 > best ? b1 : best;
+      }
+      if (lane == 0) atomicMax(&s_win, best);
+      __syncthreads();
+    }
+    if (tid < B) {
+      int tok = -1, pos = -1;
+      if (tid < a) {
+        pos = s_order[tid];
+        tok = tokens[(size_t)r * B + pos];
+      } else if (tid == a && a < gr) {
+        pos = s_order[a];
+        tok = unpack_token(s_win);
+      }
+      out_tokens[(size_t)r * B + tid] = tok;
+      out_pos[(size_t)r * B + tid] = pos;
+    }
+    if (tid == 0) {
+      accepted_len[r] = a;
+      n_commit[r] = a + (a < gr ? 1 : 0);
+    }
   }
 }
 
@@ -898,7 +950,7 @@ simsd_status accept_impl(const LT* target_logits, const LT* draft_logits, const 
   ws.n_stats = (long long)batch * gamma * (greedy ? 1 : 2) * plan.nchunk_a;
   ws.err = dev_err;
   const long grid_a = (long)batch * gamma * 2 * plan.nchunk_a;
-  const long grid_b = (long)batch * plan.nchunk_b;
+  const long grid_b = plan.ctas_b;
   if (grid_a > 0x7fffffffL || grid_b > 0x7fffffffL) return SIMSD_ERR_UNSUPPORTED;
   if (greedy) {  // argmax pass over the verified target rows, then one warp per request
     const NoiseKey nk = {false, 0.f, 0u, 0u, 0u};
