@@ -429,6 +429,33 @@ def test_accept_temperatures_and_odd_vocab(T):
     assert (st.accepted_len.cpu().numpy() < w.gamma).any()
 
 
+@pytest.mark.parametrize("V", [5001, 4096])
+def test_accept_more_requests_than_finish_ctas(V):
+    """More requests than the finish kernel's resident CTAs (700 against at most 304 on
+    GB300): its (request, group of 4 entries) ranges are cut across request boundaries, so
+    one CTA walks two or three requests in turn and most requests' races straddle two CTAs.
+    Every 37th request has a malformed step order; its sentinel outputs come from the CTA
+    holding its first group. V = 5001 takes the unvectorised loads."""
+    b, B = 700, 8
+    g = torch.Generator().manual_seed(71 + V)
+    tl = 2.0 * torch.randn(b, B, V, generator=g)
+    dl = tl + 0.7 * torch.randn(b, B, V, generator=g)
+    toks = torch.randint(0, V, (b, B), generator=g, dtype=torch.int32)
+    tau = torch.stack([torch.randperm(B, generator=g) + 1 for _ in range(b)]).to(torch.uint8)
+    bad = list(range(0, b, 37))
+    for r in bad:
+        tau[r, 1] = tau[r, 0]  # a repeated step: not a permutation
+    labels = torch.cat([tau, tau | 0x80], dim=1)
+    got, err = _accept_outputs("workspace", tl.cuda(), dl.cuda(), toks.cuda(), labels.cuda(), B,
+                               1.0, 123)
+    res = oracle.accept(tl.numpy(), dl.numpy(), toks.numpy(), labels.numpy(), B, 1.0, 123, 0)
+    assert err == res["err"] == oracle.ERR_TAU
+    assert all(got["accepted_len"][r] == -1 for r in bad)
+    ties = H.check_accept(res, got, range(b))
+    assert ties <= 7
+    assert (got["accepted_len"] < B).sum() > b // 2  # most requests race
+
+
 BF16_ACCEPT_CASES = {
     "tiny_fp32": dict(),
     "tiny_odd_vocab": dict(base="tiny_fp32", batch=64, B=8, gamma=6, V=1001),
